@@ -1,0 +1,509 @@
+"""Benchmark: fused Q+K RoPE forward/backward, achieved HBM GB/s and us/call.
+
+One step = the forward rotation of (Q, K) followed by the backward rotation
+of the incoming gradients (dQ, dK) of the same shapes -- one training step of
+RoPE in one attention layer.  Default workload: the Llama-3-8B-shaped GQA
+layer (bf16, split-half, Q [4,32,4096,128], K [4,8,4096,128], theta 5e5).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Throughput counts algorithmic bytes: the rotary span of every rotated Q/K
+row read and written once, plus each distinct cos/sin row and the position
+vector read once, per call.  The cos/sin table is built once before the timed
+region (it depends only on theta, rotary_dim, the number of positions and the
+interpolation factor) and its build time is reported separately.
+
+With N > 1 (torchrun) every rank runs the same workload on its own GPU: the
+method has no exchange step, so ranks are independent replicas.  ``value``
+is the bytes all ranks moved divided by the slowest rank's time.
+
+``--impl reference`` times the plain CPU oracle on this host's cores (the
+pages publish no runnable implementation), on a bounded sample of the same
+workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "fused Q+K RoPE fwd/bwd achieved HBM GB/s (% of GB300 peak) and µs/call"
+DEFAULT_WORKLOAD = "llama3_8b_gqa_bf16"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
+                  for f in ("rope_kernels.cuh", "rope_internal.cuh", "rope_api.cu")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing
+# --------------------------------------------------------------------------
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def aggregate(dist, device, local_ms: float, local_bytes: float):
+    """Max time over ranks, total bytes over ranks (replicas: no data exchange)."""
+    if dist is None:
+        return local_ms, local_bytes
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; nvidia-smi fallback)
+# --------------------------------------------------------------------------
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.samples = []          # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+        self.source = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            handle = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = str(getattr(props, "uuid", ""))
+            ok = False
+            for cand in (uuid, "GPU-" + uuid):
+                if cand and nv.nvmlDeviceGetHandleByUUID(cand.encode(), ctypes.byref(handle)) == 0:
+                    ok = True
+                    break
+            if not ok:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() \
+                    else device_index
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(handle)) == 0
+            if not ok:
+                raise OSError("no NVML handle")
+            self._nvml, self._handle = nv, handle
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.source = "nvml"
+        except (OSError, AttributeError, ValueError, IndexError):
+            self.source = "nvidia-smi"
+
+    def _sample_nvml(self):
+        mhz = ctypes.c_uint()
+        mask = ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(mhz)) == 0:
+            self._reasons_fn(self._handle, ctypes.byref(mask))
+            self.samples.append((float(mhz.value), int(mask.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample_nvml()
+            time.sleep(0.002)
+
+    def start(self):
+        if self.source == "nvml":
+            self._sample_nvml()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-i", str(torch.cuda.current_device()),
+                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._smi = None
+
+    def stop(self):
+        if self.source == "nvml":
+            self._sample_nvml()
+            self._stop.set()
+            if self._thread:
+                self._thread.join()
+        elif self._smi is not None:
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=10)
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), int(parts[2], 16)))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": self.source}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, m in self.samples:
+            mask |= m
+        reasons = [name for bit, name in REASON_BITS.items() if mask & bit and bit != 0x1]
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": self.source}
+
+
+# --------------------------------------------------------------------------
+# roofline inputs
+# --------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the rotation kernel from a committed ncu summary,
+    or None when there is none or the kernel sources changed since."""
+    path = os.path.join(PROFILE_DIR, "rope_vec_kernel_%s.md" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9,]+)", text)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return int(val.group(1).replace(",", ""))
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+def oracle_sample_step(o, w, xs, pos, cos32, sin32, n_tok: int):
+    """Oracle forward on Q, K and backward on dQ, dK restricted to batch 0 and
+    the first n_tok tokens (all heads).  Returns the algorithmic bytes of that
+    sample."""
+    import oracle as O
+
+    code = {"f32": O.F32, "bf16": O.BF16, "f16": O.F16}[w.dtype]
+    sub = w.with_sizes(B=1, S=n_tok)
+    p = None if pos is None else pos[:n_tok]
+    for (x, H), backward in zip(xs, (False, False, True, True)):
+        xb = W.bits(x[:1, :, :n_tok] if not w.seq_before_head else x[:1, :n_tok])
+        rc, _, _ = o.apply(xb, code, 1, H, n_tok, w.D, w.rotary_dim, W.LAYOUTS[w.layout],
+                           w.seq_before_head, backward, p, cos32, sin32, want_f64=False)
+        assert rc == 0
+    return 2 * W.algorithmic_bytes(sub)
+
+
+def time_oracle(w, budget_s: float, xs, pos, cos32, sin32):
+    """Run oracle steps on growing token samples until budget_s is spent."""
+    import oracle as O
+
+    o = O.load()
+    n_tok = 16
+    done_bytes = 0
+    t0 = time.perf_counter()
+    tokens = 0
+    while True:
+        n = min(n_tok, w.S)
+        done_bytes += oracle_sample_step(o, w, xs, pos, cos32, sin32, n)
+        tokens += n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+        n_tok = min(n_tok * 2, w.S)
+    return done_bytes, el, tokens
+
+
+def reference_arm(args, w):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0                               # rank 0 alone times the CPU oracle
+    import oracle as O
+
+    o = O.load()
+    q, k, pos = W.make_inputs(w)
+    dq, dk, _ = W.make_inputs(w, seed_offset=100)
+    xs = [(q, w.Hq), (k, w.Hk), (dq, w.Hq), (dk, w.Hk)]
+    cos32, sin32 = o.tables(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, "f32")
+    # size one step to ~0.25 s of CPU work
+    t0 = time.perf_counter()
+    oracle_sample_step(o, w, xs, pos, cos32, sin32, 8)
+    per_tok = (time.perf_counter() - t0) / 8
+    n_tok = int(max(1, min(w.S, 0.25 / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_sample_step(o, w, xs, pos, cos32, sin32, n_tok)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_sample_step(o, w, xs, pos, cos32, sin32, n_tok)
+    el = time.perf_counter() - t0
+    gbs = nbytes / el / 1e9
+    sample = ("batch 0, first %d of %d tokens, all %d Q + %d K heads, forward on Q,K and "
+              "backward on dQ,dK per step" % (n_tok, w.S, w.Hq, w.Hk))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "the pages publish no runnable implementation; the reference arm is the "
+                "single-threaded fp64 CPU oracle on this host",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "q_shape": list(w.q_shape), "k_shape": list(w.k_shape),
+            "dtype": w.dtype, "layout": w.layout,
+            "tensor_layout": "BSHD" if w.seq_before_head else "BHSD",
+            "rotary_dim": w.rotary_dim, "theta": w.theta, "table_rows": w.table_rows,
+            "positions": w.positions, "step": "forward(Q,K) + backward(dQ,dK), in place",
+            "bytes_per_call": W.algorithmic_bytes(w)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    from rotary_position_embedding_rope_gb300 import _build
+    if local == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    import rotary_position_embedding_rope_gb300 as R
+
+    R.load_library()
+    warmup = max(3, args.warmup)
+    stream = torch.cuda.current_stream(device)
+
+    # inputs: seeded on the CPU, copied to rotating device sets so every call
+    # reads memory last touched 3 steps (~1 GB of traffic) earlier: larger than L2
+    q, k, pos = W.make_inputs(w)
+    dq, dk, _ = W.make_inputs(w, seed_offset=100)
+    nsets = 4
+    sets = [(q.to(device), k.to(device), dq.to(device), dk.to(device)) for _ in range(nsets)]
+    pos_g = None if pos is None else torch.from_numpy(pos).to(device)
+    set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+
+    cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32, device=device)
+    sin = torch.empty_like(cos)
+    ev_t0, ev_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    R.rope_tables_build(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, cos, sin, stream)
+    ev_t0.record(stream)
+    R.rope_tables_build(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, cos, sin, stream)
+    ev_t1.record(stream)
+    torch.cuda.synchronize(device)
+    table_ms = ev_t0.elapsed_time(ev_t1)
+
+    layout, sbh, dt = W.LAYOUTS[w.layout], int(w.seq_before_head), W.DTYPES[w.dtype]
+
+    def call(qx, kx, backward):
+        R.rope_apply_qk(qx, kx, cos, sin, pos_g, w.B, w.Hq, w.Hk, w.S, w.D, w.rotary_dim, layout,
+                        sbh, backward, dt, w.table_rows, stream)
+
+    def step(i, events=None):
+        qx, kx, dqx, dkx = sets[i % nsets]
+        if events is not None:
+            events[0].record(stream)
+        call(qx, kx, 0)
+        if events is not None:
+            events[1].record(stream)
+        call(dqx, dkx, 1)
+        if events is not None:
+            events[2].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+
+    # timed region: K steps; per-launch events on the launching stream
+    n_ev = min(args.steps, 256)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    sampler.start()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    first_ev = args.steps - n_ev
+    for i in range(args.steps):
+        step(i, evs[i - first_ev] if i >= first_ev else None)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    local_ms = t_start.elapsed_time(t_end)
+    launches = 2 * args.steps
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    bytes_call = W.algorithmic_bytes(w)
+    bytes_step = 2 * bytes_call
+    max_ms, all_bytes = aggregate(dist, device, local_ms, bytes_step * args.steps)
+    ms_per_step = max_ms / args.steps
+    value = all_bytes / (max_ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: every step copies
+    # Q, K, dQ, dK from pinned host memory, rotates, and copies the results back
+    hq, hk, hdq, hdk = (t.pin_memory() for t in (q, k, dq, dk))
+    oq, ok_, odq, odk = (torch.empty_like(t).pin_memory() for t in (q, k, dq, dk))
+    dqx, dkx, ddq, ddk = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hdq, hdk))
+
+    def e2e_step():
+        dqx.copy_(hq, non_blocking=True)
+        dkx.copy_(hk, non_blocking=True)
+        ddq.copy_(hdq, non_blocking=True)
+        ddk.copy_(hdk, non_blocking=True)
+        R.apply_qk(dqx, dkx, cos, sin, pos_g, w.rotary_dim, w.layout, w.seq_before_head, False,
+                   stream)
+        R.apply_qk(ddq, ddk, cos, sin, pos_g, w.rotary_dim, w.layout, w.seq_before_head, True,
+                   stream)
+        oq.copy_(dqx, non_blocking=True)
+        ok_.copy_(dkx, non_blocking=True)
+        odq.copy_(ddq, non_blocking=True)
+        odk.copy_(ddk, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms, e2e_bytes = aggregate(dist, device, e0.elapsed_time(e1), bytes_step * args.e2e_steps)
+    e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
+
+    # roofline of the dominant kernel (the vectorised rotation kernel: 2 launches per step)
+    peak, peak_kind = hbm_peak()
+    kernel_ms = (fwd_ms + bwd_ms) / 2
+    achieved = bytes_call / (kernel_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(w.name)
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        import oracle as O
+
+        o = O.load()
+        cos32, sin32 = o.tables(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, "f32")
+        nb, el, toks = time_oracle(w, args.cpu_seconds, [(q, w.Hq), (k, w.Hk), (dq, w.Hq),
+                                                         (dk, w.Hk)], pos, cos32, sin32)
+        cpu = {"value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "batch 0, growing prefixes of the %d tokens (%d token-steps in %.1f s), "
+                         "all heads, forward on Q,K + backward on dQ,dK; host has %d cores, "
+                         "oracle is single-threaded" % (w.S, toks, el, os.cpu_count() or 0)}
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": dict(
+                config_of(w),
+                l2=("inputs larger than L2: %d rotating sets of Q,K,dQ,dK, %.0f MB each, "
+                    "%.0f MB in all vs %.0f MB L2" % (nsets, set_bytes / 1e6,
+                                                      nsets * set_bytes / 1e6, l2_bytes / 1e6)),
+                parallelism="replicas" if world > 1 else "single GPU"),
+            "us_per_call": {"forward": round(fwd_ms * 1e3, 3), "backward": round(bwd_ms * 1e3, 3)},
+            "table_build_us": round(table_ms * 1e3, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "traffic": traffic, "kernel": "rope_vec_kernel",
+                         "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": h2d, "steps": args.e2e_steps,
+                    "ms_per_step": round(e2e_ms / args.e2e_steps, 4)},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

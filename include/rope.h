@@ -1,0 +1,159 @@
+/*
+ * rope.h -- C ABI of librope: rotary position embedding (RoPE) on the GPU.
+ *
+ * What the library computes.  For a token at table row r and pair index i,
+ * the pair (x1, x2) of a query or key head row becomes
+ *     (x1 cos t - x2 sin t,  x1 sin t + x2 cos t),   t = angle(r, i)
+ * ("Rotary Embedding (RoPE) Kernel Optimization", Overview).  Queries and
+ * keys are rotated in one launch ("How Unsloth Optimizes RoPE Embedding
+ * Computations in Triton Kernels", Triton Kernel Architecture for RoPE:
+ * the fused Q+K kernel), and the backward pass is the same rotation by -t
+ * (same page, Frequently Asked Questions: gradients use the same kernel
+ * with the backward flag).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" must point to memory of the current CUDA
+ *     device.  The caller owns every buffer; the library allocates nothing
+ *     and never synchronises the stream, except in rope_check_errors.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the default stream.
+ *     Work is enqueued asynchronously on that stream.
+ *   - Tensors are dense and contiguous.  seq_before_head = 0: [B, H, S, D]
+ *     (Unsloth page, Usage Examples; "rotary-embedding-torch", Input Tensor
+ *     Shapes); seq_before_head = 1: [B, S, H, D] ("rotary-embedding-torch",
+ *     RotaryEmbedding / Key Parameters: seq_before_head_dim).
+ *   - Element types: ROPE_F32, ROPE_BF16, ROPE_F16.  Arithmetic is fp32;
+ *     each output element is rounded once to the element type.
+ *   - Pair layouts ("Rotary Embedding (RoPE) Kernel Optimization", Core
+ *     Technique / Paired Element Layout): ROPE_SPLIT_HALF pairs
+ *     (x[i], x[i + rotary_dim/2]); ROPE_INTERLEAVED pairs (x[2i], x[2i+1]).
+ *   - Partial rotation ("rotary-embedding-torch", RotaryEmbedding / Key
+ *     Parameters: dim is the size of the rotated part): only the first
+ *     rotary_dim features of each head row are rotated; features
+ *     [rotary_dim, D) are neither read nor written.
+ *   - Errors detected on the host are returned before anything is enqueued;
+ *     nothing is modified then.
+ */
+#ifndef ROPE_H
+#define ROPE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ROPE_OK = 0,
+    ROPE_ERR_INVALID_ARG = 1,      /* bad size, null pointer, overlap, ...       */
+    ROPE_ERR_UNSUPPORTED = 2,      /* dtype or layout value outside the enums    */
+    ROPE_ERR_CUDA = 3,             /* a CUDA call failed (launch, sync, ...)     */
+    ROPE_ERR_POS_OUT_OF_RANGE = 4  /* a position index was outside the table     */
+} rope_status;
+
+typedef enum { ROPE_SPLIT_HALF = 0, ROPE_INTERLEAVED = 1 } rope_layout;
+typedef enum { ROPE_F32 = 0, ROPE_BF16 = 1, ROPE_F16 = 2 } rope_dtype;
+
+/*
+ * rope_tables_build -- fill the cos/sin table.
+ *
+ * Source: "rotary-embedding-torch", RotaryEmbedding / Key Parameters (theta
+ * is the frequency base, default 10000; interpolate_factor scales sequence
+ * positions, default 1.0); "Rotary Embedding (RoPE) Kernel Optimization",
+ * Common Pitfalls (cos/sin are [seq_len, D/2] and broadcast over batch and
+ * heads).  The pages do not print the frequency formula; the library uses
+ * the standard one: for row m and pair i (0 <= i < rotary_dim/2)
+ *     angle = (m / interpolate_factor) * theta^(-2i / rotary_dim),
+ * evaluated in fp64, and stores cos(angle), sin(angle) rounded to fp32.
+ *
+ * cos_out, sin_out: device, caller-owned, float[max_pos * rotary_dim/2]
+ *   each, row-major [max_pos, rotary_dim/2].
+ * Errors: ROPE_ERR_INVALID_ARG if theta <= 0, interpolate_factor <= 0 (or
+ *   either is not finite), rotary_dim < 2 or odd, max_pos < 0, a null
+ *   output with max_pos > 0, or overlapping outputs.  max_pos = 0 is a
+ *   no-op.  ROPE_ERR_CUDA if the launch fails.
+ */
+rope_status rope_tables_build(double theta, int32_t rotary_dim, int64_t max_pos,
+                              double interpolate_factor, float *cos_out, float *sin_out,
+                              void *stream);
+
+/*
+ * rope_apply_qk -- rotate Q and K in place, in one launch.
+ *
+ * Source: Unsloth page, Triton Kernel Architecture for RoPE (Q and K in one
+ * kernel) and Usage Examples (fast_rope_embedding(Q, K, cos, sin,
+ * position_ids)); "rotary-embedding-torch", flash_attn_with_rotary / Key
+ * Features (heads_q != heads_kv for GQA/MQA).
+ *
+ * q: device, [B, Hq, S, D] or [B, S, Hq, D] of `dtype`, updated in place.
+ * k: device, [B, Hk, S, D] or [B, S, Hk, D] of `dtype`, updated in place;
+ *    may be NULL when Hk = 0.  q and k must not overlap each other or the
+ *    tables.
+ * cos, sin: device, float[table_rows, rotary_dim/2] (as written by
+ *    rope_tables_build with max_pos = table_rows).
+ * pos_idx: device int32[S] or NULL.  Token s (in every batch) uses table
+ *    row pos_idx[s] (Unsloth page, Support for Custom Position IDs;
+ *    "rotary-embedding-torch", Input Tensor Shapes: rotary_pos_emb_indices
+ *    (seq_len,)).  The value -1 leaves the token unrotated (the pos_mask of
+ *    "rotary-embedding-torch", flash_attn_with_rotary): its rows are not
+ *    written.  With NULL, token s uses row s and S <= table_rows is required.
+ *    Any other value outside [0, table_rows) leaves that token unrotated and
+ *    raises a device-side flag reported by rope_check_errors as
+ *    ROPE_ERR_POS_OUT_OF_RANGE.
+ * B, S >= 0; Hq, Hk >= 0; D >= 1; rotary_dim even, 2 <= rotary_dim <= D.
+ *    An empty problem (B, S or Hq + Hk zero) returns ROPE_OK and enqueues
+ *    nothing.
+ * layout: rope_layout.  seq_before_head, backward: 0 or 1.  backward = 1
+ *    rotates by the negated angle (the gradient of the forward rotation).
+ * dtype: rope_dtype of q and k.
+ * table_rows: rows of cos and sin (>= 1 for a non-empty problem).
+ * Errors: ROPE_ERR_UNSUPPORTED for dtype/layout outside the enums;
+ *    ROPE_ERR_INVALID_ARG for the size, flag, pointer and overlap rules
+ *    above; ROPE_ERR_CUDA if the launch fails.  Pointers or rows that are
+ *    not 16-byte aligned take a slower element-wise kernel, same results.
+ */
+rope_status rope_apply_qk(void *q, void *k, const float *cos, const float *sin,
+                          const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk, int64_t S,
+                          int32_t D, int32_t rotary_dim, int32_t layout, int32_t seq_before_head,
+                          int32_t backward, int32_t dtype, int64_t table_rows, void *stream);
+
+/*
+ * rope_apply_q -- rotate one tensor in place (the query-only kernel of the
+ * Unsloth page, Triton Kernel Architecture for RoPE).  Same rules as
+ * rope_apply_qk with x in place of q, H in place of Hq, and no k.
+ */
+rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int32_t *pos_idx,
+                         int64_t B, int32_t H, int64_t S, int32_t D, int32_t rotary_dim,
+                         int32_t layout, int32_t seq_before_head, int32_t backward, int32_t dtype,
+                         int64_t table_rows, void *stream);
+
+/*
+ * rope_check_errors -- synchronise `stream`, then report and clear the
+ * current device's position-range flag.
+ * Returns ROPE_ERR_CUDA if the stream reports an error, else
+ * ROPE_ERR_POS_OUT_OF_RANGE if any launch since the last check met an
+ * out-of-range position index, else ROPE_OK.  The flag is shared by all
+ * streams of the device.
+ */
+rope_status rope_check_errors(void *stream);
+
+/* rope_status_string -- static, NUL-terminated name of a status value. */
+const char *rope_status_string(rope_status status);
+
+/*
+ * rope_qk_kernel_variant -- which kernel rope_apply_qk would launch for
+ * these arguments, without launching anything or touching the device.
+ * Returns 0 when nothing would be launched (error or empty problem),
+ * 1 for the 16-byte vectorised kernel, 2 for the element-wise kernel.
+ * Useful for tests and for callers checking that their tensors are aligned.
+ */
+int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, const float *sin,
+                               const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk,
+                               int64_t S, int32_t D, int32_t rotary_dim, int32_t layout,
+                               int32_t seq_before_head, int32_t backward, int32_t dtype,
+                               int64_t table_rows);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_H */

@@ -1,0 +1,244 @@
+"""Python binding of librope: rotary position embedding on GB300 (sm_103a).
+
+The functions named like the C ABI (``rope_tables_build``, ``rope_apply_qk``,
+``rope_apply_q``, ``rope_check_errors``, ``rope_status_string``,
+``rope_qk_kernel_variant``) take the same arguments as ``include/rope.h``,
+with torch tensors (or raw integer addresses) in place of pointers and a
+torch stream (or raw handle, or None for torch's current stream) in place of
+``void* stream``.  They only marshal arguments: every step runs in the CUDA
+library, and a missing library is an error, never a fallback.
+
+``build_tables``, ``apply_qk`` and ``apply_q`` are conveniences that read the
+sizes from tensor shapes and allocate the tables with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "RopeError", "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
+    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
+    "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
+    "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
+    "library_path", "load_library",
+]
+
+ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE = range(5)
+ROPE_SPLIT_HALF, ROPE_INTERLEAVED = 0, 1
+ROPE_F32, ROPE_BF16, ROPE_F16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: ROPE_F32, torch.bfloat16: ROPE_BF16, torch.float16: ROPE_F16}
+_LAYOUT_CODE = {"split_half": ROPE_SPLIT_HALF, "interleaved": ROPE_INTERLEAVED}
+
+
+class RopeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, rope_status_string(status)))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load_library() -> ctypes.CDLL:
+    """Load lib/librope.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "librope.so is not built (%s); run `python -c \"import __graft_entry__ as g; "
+            "g.build()\"` first" % path)
+    lib = ctypes.CDLL(path)
+    c = ctypes
+    P = c.c_void_p
+    lib.rope_tables_build.argtypes = [c.c_double, c.c_int32, c.c_int64, c.c_double, P, P, P]
+    lib.rope_tables_build.restype = c.c_int
+    lib.rope_apply_qk.argtypes = [P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32, c.c_int64,
+                                  c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                  c.c_int32, c.c_int64, P]
+    lib.rope_apply_qk.restype = c.c_int
+    lib.rope_apply_q.argtypes = [P, P, P, P, c.c_int64, c.c_int32, c.c_int64, c.c_int32,
+                                 c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                 c.c_int64, P]
+    lib.rope_apply_q.restype = c.c_int
+    lib.rope_check_errors.argtypes = [P]
+    lib.rope_check_errors.restype = c.c_int
+    lib.rope_status_string.argtypes = [c.c_int]
+    lib.rope_status_string.restype = c.c_char_p
+    lib.rope_qk_kernel_variant.argtypes = [P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32,
+                                           c.c_int64, c.c_int32, c.c_int32, c.c_int32,
+                                           c.c_int32, c.c_int32, c.c_int32, c.c_int64]
+    lib.rope_qk_kernel_variant.restype = c.c_int32
+    _lib = lib
+    return lib
+
+
+# --------------------------------------------------------------------------
+# marshalling
+# --------------------------------------------------------------------------
+def _addr(x, name: str, device_required: bool = True):
+    """Device address of a tensor (checked contiguous, on CUDA) or a raw int."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        if device_required and not x.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not x.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+        return x.data_ptr() if x.numel() > 0 else None
+    raise TypeError("%s: expected a tensor, an int address or None" % name)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != ROPE_OK:
+        raise RopeError(status, where)
+
+
+# --------------------------------------------------------------------------
+# functions of the C ABI, same names and arguments
+# --------------------------------------------------------------------------
+def rope_tables_build(theta, rotary_dim, max_pos, interpolate_factor, cos_out, sin_out,
+                      stream=None):
+    lib = load_library()
+    for t, n in ((cos_out, "cos_out"), (sin_out, "sin_out")):
+        if isinstance(t, torch.Tensor) and (t.dtype != torch.float32 or
+                                            t.numel() < max_pos * (rotary_dim // 2)):
+            raise ValueError("%s must be float32 with at least max_pos*rotary_dim/2 elements" % n)
+    st = lib.rope_tables_build(float(theta), int(rotary_dim), int(max_pos),
+                               float(interpolate_factor), _addr(cos_out, "cos_out"),
+                               _addr(sin_out, "sin_out"), _stream(stream))
+    _check(st, "rope_tables_build")
+
+
+def rope_apply_qk(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim, layout,
+                  seq_before_head, backward, dtype, table_rows, stream=None):
+    lib = load_library()
+    st = lib.rope_apply_qk(_addr(q, "q"), _addr(k, "k"), _addr(cos, "cos"), _addr(sin, "sin"),
+                           _addr(pos_idx, "pos_idx"), int(B), int(Hq), int(Hk), int(S), int(D),
+                           int(rotary_dim), int(layout), int(seq_before_head), int(backward),
+                           int(dtype), int(table_rows), _stream(stream))
+    _check(st, "rope_apply_qk")
+
+
+def rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rotary_dim, layout, seq_before_head,
+                 backward, dtype, table_rows, stream=None):
+    lib = load_library()
+    st = lib.rope_apply_q(_addr(x, "x"), _addr(cos, "cos"), _addr(sin, "sin"),
+                          _addr(pos_idx, "pos_idx"), int(B), int(H), int(S), int(D),
+                          int(rotary_dim), int(layout), int(seq_before_head), int(backward),
+                          int(dtype), int(table_rows), _stream(stream))
+    _check(st, "rope_apply_q")
+
+
+def rope_check_errors(stream=None) -> int:
+    """Synchronise the stream; returns the status (does not raise)."""
+    return load_library().rope_check_errors(_stream(stream))
+
+
+def rope_status_string(status: int) -> str:
+    return load_library().rope_status_string(int(status)).decode()
+
+
+def rope_qk_kernel_variant(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim, layout,
+                           seq_before_head, backward, dtype, table_rows) -> int:
+    lib = load_library()
+    return lib.rope_qk_kernel_variant(
+        _addr(q, "q", False), _addr(k, "k", False), _addr(cos, "cos", False),
+        _addr(sin, "sin", False), _addr(pos_idx, "pos_idx", False), int(B), int(Hq), int(Hk),
+        int(S), int(D), int(rotary_dim), int(layout), int(seq_before_head), int(backward),
+        int(dtype), int(table_rows))
+
+
+# --------------------------------------------------------------------------
+# conveniences
+# --------------------------------------------------------------------------
+def build_tables(theta: float, rotary_dim: int, max_pos: int, interpolate_factor: float = 1.0,
+                 device=None, stream=None):
+    """Allocate and fill fp32 cos/sin tables [max_pos, rotary_dim // 2]."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    h = rotary_dim // 2
+    cos = torch.empty((max_pos, h), dtype=torch.float32, device=device)
+    sin = torch.empty((max_pos, h), dtype=torch.float32, device=device)
+    rope_tables_build(theta, rotary_dim, max_pos, interpolate_factor, cos, sin, stream)
+    return cos, sin
+
+
+def _shape4(x: torch.Tensor, seq_before_head: bool):
+    if x.dim() != 4:
+        raise ValueError("expected a 4-D tensor, got shape %s" % (tuple(x.shape),))
+    if seq_before_head:
+        B, S, H, D = x.shape
+    else:
+        B, H, S, D = x.shape
+    return B, H, S, D
+
+
+def apply_qk(q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor, sin: torch.Tensor,
+             pos_idx: torch.Tensor | None = None, rotary_dim: int | None = None,
+             layout: str = "split_half", seq_before_head: bool = False, backward: bool = False,
+             stream=None):
+    """Rotate q and k in place; sizes are read from the tensors.
+
+    q: [B, Hq, S, D] (or [B, S, Hq, D] with seq_before_head); k likewise with
+    Hk heads, or None.  cos/sin: float32 [rows, rotary_dim // 2].
+    pos_idx: int32 [S] or None.  rotary_dim defaults to 2 * cos.shape[1].
+    """
+    B, Hq, S, D = _shape4(q, seq_before_head)
+    Hk = 0
+    if k is not None:
+        Bk, Hk, Sk, Dk = _shape4(k, seq_before_head)
+        if (Bk, Sk, Dk) != (B, S, D) or k.dtype != q.dtype:
+            raise ValueError("q and k must agree in batch, sequence, head_dim and dtype")
+    if q.dtype not in _DTYPE_CODE:
+        raise TypeError("unsupported dtype %s" % q.dtype)
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or cos.shape != sin.shape:
+        raise ValueError("cos and sin must be float32 tables of the same shape")
+    rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+    if cos.shape[1] != rd // 2:
+        raise ValueError("table width %d does not match rotary_dim %d" % (cos.shape[1], rd))
+    if pos_idx is not None and (pos_idx.dtype != torch.int32 or pos_idx.numel() != S):
+        raise ValueError("pos_idx must be int32 with S elements")
+    rope_apply_qk(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rd, _LAYOUT_CODE[layout],
+                  int(seq_before_head), int(backward), _DTYPE_CODE[q.dtype], cos.shape[0],
+                  stream)
+    return q, k
+
+
+def apply_q(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
+            pos_idx: torch.Tensor | None = None, rotary_dim: int | None = None,
+            layout: str = "split_half", seq_before_head: bool = False, backward: bool = False,
+            stream=None):
+    """Rotate one tensor in place through the query-only entry point."""
+    B, H, S, D = _shape4(x, seq_before_head)
+    if x.dtype not in _DTYPE_CODE:
+        raise TypeError("unsupported dtype %s" % x.dtype)
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or cos.shape != sin.shape:
+        raise ValueError("cos and sin must be float32 tables of the same shape")
+    rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+    if cos.shape[1] != rd // 2:
+        raise ValueError("table width %d does not match rotary_dim %d" % (cos.shape[1], rd))
+    if pos_idx is not None and (pos_idx.dtype != torch.int32 or pos_idx.numel() != S):
+        raise ValueError("pos_idx must be int32 with S elements")
+    rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rd, _LAYOUT_CODE[layout],
+                 int(seq_before_head), int(backward), _DTYPE_CODE[x.dtype], cos.shape[0], stream)
+    return x

@@ -1,0 +1,54 @@
+// rope_internal.cuh -- declarations shared by the translation units of librope.
+// Not part of the public ABI (include/rope.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rope {
+
+// One rotated tensor: base pointer and element strides of its batch, head and
+// sequence dimensions (the feature dimension is contiguous).
+struct TensorRef {
+    void *base;
+    int32_t heads;
+    int64_t stride_b;
+    int64_t stride_h;
+    int64_t stride_s;
+};
+
+// Everything a rotation launch needs.  Passed by value as a kernel parameter.
+struct ApplyArgs {
+    TensorRef t[2];            // Q then K; ntensors of them are valid
+    int32_t ntensors;
+    const float *cos;          // [table_rows, rotary_dim/2]
+    const float *sin;
+    const int32_t *pos_idx;    // [S] or nullptr
+    int64_t B;
+    int64_t S;
+    int32_t D;
+    int32_t rotary_dim;
+    int64_t table_rows;
+    int32_t backward;          // 1: rotate by the negated angle
+    int32_t *range_flag;       // device word set when a position is out of range
+};
+
+enum Variant : int32_t { kNone = 0, kVector = 1, kScalar = 2 };
+
+// Threads per CTA of the vectorised kernel and heads in flight per thread.
+#ifndef ROPE_VEC_THREADS
+#define ROPE_VEC_THREADS 256
+#endif
+#ifndef ROPE_VEC_UNROLL
+#define ROPE_VEC_UNROLL 4
+#endif
+constexpr int kVecThreads = ROPE_VEC_THREADS;
+constexpr int kVecUnroll = ROPE_VEC_UNROLL;
+constexpr int kMaxVectorsPerHalf = 256;   // NJ limit of the vectorised kernel
+
+// Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).
+cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);
+cudaError_t launch_apply_bf16(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);
+cudaError_t launch_apply_f16(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);
+
+}  // namespace rope

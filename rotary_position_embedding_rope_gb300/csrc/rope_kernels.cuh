@@ -1,0 +1,344 @@
+// rope_kernels.cuh -- the rotation kernels of librope (sm_103a).
+//
+// What is computed ("Rotary Embedding (RoPE) Kernel Optimization", Overview):
+// each pair (x1, x2) of a head row at table row r becomes
+//     (x1 c - x2 s, x1 s + x2 c),  c = cos[r][i], s = sin[r][i]
+// and the backward pass uses -s ("How Unsloth Optimizes RoPE Embedding
+// Computations in Triton Kernels", Frequently Asked Questions).
+//
+// Design (GB300): RoPE moves 4 bytes per bf16 pair each way and does a few
+// flops, so it is bound by HBM bandwidth.  The vectorised kernel therefore:
+//   * gives each token a row of the CTA (NJ threads) and keeps that token's
+//     cos/sin values in registers for all Hq + Hk heads, so the table row is
+//     read once per token (the Unsloth page motivates head grouping, Triton
+//     Kernel Architecture for RoPE; here the group is all heads);
+//   * moves data in 16-byte vectors: thread j owns vector j of the first
+//     half of the rotary span and vector j of the second half.  For
+//     split-half pairs (x[i], x[i+rd/2]) the partner of every element is the
+//     same lane of the other vector; for interleaved pairs (x[2i], x[2i+1])
+//     both elements sit in one vector.  Pairing is a register swizzle, no
+//     strided scalar loads and no shuffles;
+//   * issues the loads of kVecUnroll heads before any arithmetic so each
+//     thread has 2 * kVecUnroll 16-byte requests in flight;
+//   * uses streaming (evict-first) loads and stores: every byte is touched
+//     exactly once;
+//   * never reads or writes features past rotary_dim, nor tokens whose
+//     position is -1 (pass-through without arithmetic).
+// The element-wise kernel handles shapes and pointers the vector kernel
+// cannot (rotary span not a multiple of 32 bytes, rows or pointers not
+// 16-byte aligned).  Both use the same arithmetic, so their results are
+// bit-identical.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "rope_internal.cuh"
+
+namespace rope {
+
+// ---------------------------------------------------------------------------
+// Element types: number of elements in a 16-byte vector and conversions.
+// Widening to fp32 is exact; narrowing rounds to nearest even, once.
+// ---------------------------------------------------------------------------
+template <typename T> struct Elt;
+
+template <> struct Elt<float> {
+    static constexpr int V = 4;
+    __device__ __forceinline__ static float to_f(float x) { return x; }
+    __device__ __forceinline__ static float from_f(float x) { return x; }
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[V]) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[V]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+
+template <> struct Elt<__nv_bfloat16> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+    __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
+        __nv_bfloat162 h;
+        memcpy(&h, &w, 4);
+        return __bfloat1622float2(h);
+    }
+    __device__ __forceinline__ static uint32_t f2_to_word(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // a -> low half, b -> high half
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[V]) {
+        float2 p;
+        p = word_to_f2(u.x); f[0] = p.x; f[1] = p.y;
+        p = word_to_f2(u.y); f[2] = p.x; f[3] = p.y;
+        p = word_to_f2(u.z); f[4] = p.x; f[5] = p.y;
+        p = word_to_f2(u.w); f[6] = p.x; f[7] = p.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[V]) {
+        return make_uint4(f2_to_word(f[0], f[1]), f2_to_word(f[2], f[3]),
+                          f2_to_word(f[4], f[5]), f2_to_word(f[6], f[7]));
+    }
+};
+
+template <> struct Elt<__half> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static float to_f(__half x) { return __half2float(x); }
+    __device__ __forceinline__ static __half from_f(float x) { return __float2half_rn(x); }
+    __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static uint32_t f2_to_word(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[V]) {
+        float2 p;
+        p = word_to_f2(u.x); f[0] = p.x; f[1] = p.y;
+        p = word_to_f2(u.y); f[2] = p.x; f[3] = p.y;
+        p = word_to_f2(u.z); f[4] = p.x; f[5] = p.y;
+        p = word_to_f2(u.w); f[6] = p.x; f[7] = p.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[V]) {
+        return make_uint4(f2_to_word(f[0], f[1]), f2_to_word(f[2], f[3]),
+                          f2_to_word(f[4], f[5]), f2_to_word(f[6], f[7]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// a*b - c*d with Kahan's fma-based compensation: the rounding error of c*d
+// is recovered exactly by an fma and added back, so the result has a
+// relative error of at most 2 units in the last place of fp32 (Jeannerod,
+// Louvet & Muller, "Further analysis of Kahan's algorithm for the accurate
+// computation of 2x2 determinants", Math. Comp. 82, 2013).  That keeps a
+// bf16/fp16 output within one unit of the correctly rounded value even when
+// the two products nearly cancel.  Explicit _rn intrinsics keep the compiler
+// from contracting or reordering the steps.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+    const float w = __fmul_rn(c, d);
+    const float e = __fmaf_rn(-c, d, w);      // w - c*d, exact
+    const float f = __fmaf_rn(a, b, -w);      // a*b - w, one rounding
+    return __fadd_rn(f, e);
+}
+
+// (x1, x2) <- (x1 c - x2 s, x1 s + x2 c)
+__device__ __forceinline__ void rotate_pair(float &x1, float &x2, float c, float s) {
+    const float y1 = diff_of_products(x1, c, x2, s);
+    const float y2 = diff_of_products(x1, s, -x2, c);
+    x1 = y1;
+    x2 = y2;
+}
+
+// ---------------------------------------------------------------------------
+// Vectorised kernel.
+//   blockDim = (NJ, TS): NJ = 16-byte vectors per half of the rotary span,
+//   TS = tokens per CTA.  CTA `blk` covers batch blk / tiles_per_b and tokens
+//   (blk % tiles_per_b) * TS + [0, TS).
+//   Split-half: vector j holds elements [jV, jV+V) and vector j+NJ holds
+//   their partners [rd/2 + jV, ...); cos/sin columns [jV, jV+V).
+//   Interleaved: vector j holds pairs [jV/2, jV/2 + V/2) and vector j+NJ
+//   holds pairs [(j+NJ)V/2, ...); the thread keeps both column ranges.
+// ---------------------------------------------------------------------------
+template <typename T, int LAYOUT, int U>
+__global__ void __launch_bounds__(kVecThreads)
+rope_vec_kernel(const ApplyArgs p, int64_t tiles_per_b, int64_t total_blocks)
+{
+    constexpr int V = Elt<T>::V;
+    const int NJ = blockDim.x;
+    const int TS = blockDim.y;
+    const int j = threadIdx.x;
+    const int h = p.rotary_dim >> 1;
+
+    for (int64_t blk = blockIdx.x; blk < total_blocks; blk += gridDim.x) {
+        const int64_t b = blk / tiles_per_b;
+        const int64_t s = (blk - b * tiles_per_b) * TS + threadIdx.y;
+        if (s >= p.S)
+            continue;
+
+        // position of this token: table row, -1 = leave unrotated
+        int64_t r = s;
+        if (p.pos_idx != nullptr) {
+            r = __ldg(p.pos_idx + s);
+            if (r == -1)
+                continue;
+            if (r < 0 || r >= p.table_rows) {
+                if (j == 0)
+                    atomicOr(p.range_flag, 1);
+                continue;
+            }
+        }
+
+        // this thread's cos/sin values, kept in registers for every head
+        float c[V], sn[V];
+        const float *crow = p.cos + r * h;
+        const float *srow = p.sin + r * h;
+        if constexpr (LAYOUT == 0) {
+#pragma unroll
+            for (int q = 0; q < V / 4; ++q) {
+                const float4 cv = __ldg(reinterpret_cast<const float4 *>(crow + j * V) + q);
+                const float4 sv = __ldg(reinterpret_cast<const float4 *>(srow + j * V) + q);
+                c[4 * q] = cv.x; c[4 * q + 1] = cv.y; c[4 * q + 2] = cv.z; c[4 * q + 3] = cv.w;
+                sn[4 * q] = sv.x; sn[4 * q + 1] = sv.y; sn[4 * q + 2] = sv.z; sn[4 * q + 3] = sv.w;
+            }
+        } else if constexpr (V == 8) {
+            const float4 c0 = __ldg(reinterpret_cast<const float4 *>(crow + j * 4));
+            const float4 c1 = __ldg(reinterpret_cast<const float4 *>(crow + (j + NJ) * 4));
+            const float4 s0 = __ldg(reinterpret_cast<const float4 *>(srow + j * 4));
+            const float4 s1 = __ldg(reinterpret_cast<const float4 *>(srow + (j + NJ) * 4));
+            c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+            c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+            sn[0] = s0.x; sn[1] = s0.y; sn[2] = s0.z; sn[3] = s0.w;
+            sn[4] = s1.x; sn[5] = s1.y; sn[6] = s1.z; sn[7] = s1.w;
+        } else {
+            const float2 c0 = __ldg(reinterpret_cast<const float2 *>(crow + j * 2));
+            const float2 c1 = __ldg(reinterpret_cast<const float2 *>(crow + (j + NJ) * 2));
+            const float2 s0 = __ldg(reinterpret_cast<const float2 *>(srow + j * 2));
+            const float2 s1 = __ldg(reinterpret_cast<const float2 *>(srow + (j + NJ) * 2));
+            c[0] = c0.x; c[1] = c0.y; c[2] = c1.x; c[3] = c1.y;
+            sn[0] = s0.x; sn[1] = s0.y; sn[2] = s1.x; sn[3] = s1.y;
+        }
+        if (p.backward) {
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                sn[e] = -sn[e];
+        }
+
+#pragma unroll
+        for (int ti = 0; ti < 2; ++ti) {
+            if (ti >= p.ntensors)
+                break;
+            const TensorRef t = p.t[ti];
+            T *row0 = static_cast<T *>(t.base) + b * t.stride_b + s * t.stride_s;
+            for (int h0 = 0; h0 < t.heads; h0 += U) {
+                uint4 va[U], vb[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (h0 + u < t.heads) {
+                        const uint4 *ptr =
+                            reinterpret_cast<const uint4 *>(row0 + (int64_t)(h0 + u) * t.stride_h);
+                        va[u] = __ldcs(ptr + j);
+                        vb[u] = __ldcs(ptr + j + NJ);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (h0 + u < t.heads) {
+                        float fa[V], fb[V];
+                        Elt<T>::unpack(va[u], fa);
+                        Elt<T>::unpack(vb[u], fb);
+                        if constexpr (LAYOUT == 0) {
+#pragma unroll
+                            for (int e = 0; e < V; ++e)
+                                rotate_pair(fa[e], fb[e], c[e], sn[e]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < V / 2; ++e) {
+                                rotate_pair(fa[2 * e], fa[2 * e + 1], c[e], sn[e]);
+                                rotate_pair(fb[2 * e], fb[2 * e + 1], c[V / 2 + e], sn[V / 2 + e]);
+                            }
+                        }
+                        uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * t.stride_h);
+                        __stcs(ptr + j, Elt<T>::pack(fa));
+                        __stcs(ptr + j + NJ, Elt<T>::pack(fb));
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Element-wise kernel: one pair per loop iteration, any alignment and any
+// even rotary_dim.  Rows are enumerated tensor by tensor as (b, head, s),
+// s fastest; pairs within a row are consecutive indices.
+// ---------------------------------------------------------------------------
+template <typename T, int LAYOUT>
+__global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t total_pairs)
+{
+    const int h = p.rotary_dim >> 1;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_pairs;
+         idx += stride) {
+        const int64_t i = idx % h;
+        int64_t row = idx / h;
+        const int ti = row < rows0 ? 0 : 1;
+        if (ti)
+            row -= rows0;
+        const TensorRef t = p.t[ti];
+        const int64_t s = row % p.S;
+        row /= p.S;
+        const int64_t head = row % t.heads;
+        const int64_t b = row / t.heads;
+
+        int64_t r = s;
+        if (p.pos_idx != nullptr) {
+            r = __ldg(p.pos_idx + s);
+            if (r == -1)
+                continue;
+            if (r < 0 || r >= p.table_rows) {
+                if (i == 0)
+                    atomicOr(p.range_flag, 1);
+                continue;
+            }
+        }
+        const float c = __ldg(p.cos + r * h + i);
+        float sn = __ldg(p.sin + r * h + i);
+        if (p.backward)
+            sn = -sn;
+
+        T *x = static_cast<T *>(t.base) + b * t.stride_b + head * t.stride_h + s * t.stride_s;
+        const int64_t i1 = LAYOUT == 0 ? i : 2 * i;
+        const int64_t i2 = LAYOUT == 0 ? i + h : 2 * i + 1;
+        float x1 = Elt<T>::to_f(x[i1]);
+        float x2 = Elt<T>::to_f(x[i2]);
+        rotate_pair(x1, x2, c, sn);
+        x[i1] = Elt<T>::from_f(x1);
+        x[i2] = Elt<T>::from_f(x2);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launcher for one element type.
+// ---------------------------------------------------------------------------
+template <typename T>
+cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st)
+{
+    if (v == kVector) {
+        constexpr int V = Elt<T>::V;
+        const int NJ = (a.rotary_dim / 2) / V;                 // vectors per half span
+        const int TS = NJ >= kVecThreads ? 1 : kVecThreads / NJ;
+        const int64_t tiles_per_b = (a.S + TS - 1) / TS;
+        const int64_t total_blocks = a.B * tiles_per_b;
+        const unsigned grid = (unsigned)(total_blocks < 0x7fffffffLL ? total_blocks : 0x7fffffffLL);
+        const dim3 block(NJ, TS);
+        if (layout == 0)
+            rope_vec_kernel<T, 0, kVecUnroll><<<grid, block, 0, st>>>(a, tiles_per_b, total_blocks);
+        else
+            rope_vec_kernel<T, 1, kVecUnroll><<<grid, block, 0, st>>>(a, tiles_per_b, total_blocks);
+        return cudaGetLastError();
+    }
+    const int64_t rows0 = a.B * a.S * a.t[0].heads;
+    const int64_t rows1 = a.ntensors > 1 ? a.B * a.S * a.t[1].heads : 0;
+    const int64_t total = (rows0 + rows1) * (a.rotary_dim / 2);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 64)
+        blocks = 152LL * 64;                                   // grid-stride beyond this
+    if (layout == 0)
+        rope_scalar_kernel<T, 0><<<(unsigned)blocks, threads, 0, st>>>(a, rows0, total);
+    else
+        rope_scalar_kernel<T, 1><<<(unsigned)blocks, threads, 0, st>>>(a, rows0, total);
+    return cudaGetLastError();
+}
+
+}  // namespace rope

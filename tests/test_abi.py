@@ -1,0 +1,151 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the
+header declares, rejects bad arguments before touching the device, and picks
+the kernel variant by its documented rules.  No call here launches work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rotary_position_embedding_rope_gb300 as R
+from rotary_position_embedding_rope_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return R.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rope_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for want in ("rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
+                 "rope_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    assert R.rope_status_string(R.ROPE_OK) == "ROPE_OK"
+    assert R.rope_status_string(R.ROPE_ERR_POS_OUT_OF_RANGE) == "ROPE_ERR_POS_OUT_OF_RANGE"
+    assert R.rope_status_string(99) == "ROPE_STATUS_UNKNOWN"
+
+
+A16 = 0x10000  # fake, 16-byte aligned "device" addresses: never dereferenced on these paths
+GOOD = dict(q=A16 * 1, k=A16 * 1000, cos=A16 * 2000, sin=A16 * 3000, pos=None, B=2, Hq=4, Hk=2,
+            S=16, D=64, rd=64, layout=0, sbh=0, bwd=0, dtype=1, rows=16)
+
+
+def qk_args(**over):
+    a = dict(GOOD, **over)
+    return (a["q"], a["k"], a["cos"], a["sin"], a["pos"], a["B"], a["Hq"], a["Hk"], a["S"],
+            a["D"], a["rd"], a["layout"], a["sbh"], a["bwd"], a["dtype"], a["rows"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(dtype=3), R.ROPE_ERR_UNSUPPORTED),
+    (dict(dtype=-1), R.ROPE_ERR_UNSUPPORTED),
+    (dict(layout=2), R.ROPE_ERR_UNSUPPORTED),
+    (dict(sbh=2), R.ROPE_ERR_INVALID_ARG),
+    (dict(bwd=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(B=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(S=-5), R.ROPE_ERR_INVALID_ARG),
+    (dict(Hq=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(Hk=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(D=0), R.ROPE_ERR_INVALID_ARG),
+    (dict(rd=0), R.ROPE_ERR_INVALID_ARG),
+    (dict(rd=63), R.ROPE_ERR_INVALID_ARG),
+    (dict(rd=66), R.ROPE_ERR_INVALID_ARG),
+    (dict(q=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(k=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(cos=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(sin=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(rows=0), R.ROPE_ERR_INVALID_ARG),
+    (dict(rows=15), R.ROPE_ERR_INVALID_ARG),             # S > table_rows without pos_idx
+    (dict(rows=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(k=A16 * 1 + 64), R.ROPE_ERR_INVALID_ARG),      # q and k overlap
+    (dict(cos=A16 * 1 + 128), R.ROPE_ERR_INVALID_ARG),   # q overlaps the table
+    (dict(B=1 << 40, S=1 << 40), R.ROPE_ERR_INVALID_ARG),  # size overflow
+])
+def test_apply_rejects_bad_arguments(lib, over, status):
+    args = qk_args(**over)
+    assert lib.rope_qk_kernel_variant(*args) == 0
+    assert lib.rope_apply_qk(*args, None) == status
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(S=0), dict(Hq=0, Hk=0),
+                                  dict(B=0, q=None, k=None, cos=None, sin=None)])
+def test_empty_problems_are_noops(lib, over):
+    args = qk_args(**over)
+    assert lib.rope_qk_kernel_variant(*args) == 0
+    assert lib.rope_apply_qk(*args, None) == R.ROPE_OK
+
+
+def test_q_only_rejects_bad_arguments(lib):
+    assert lib.rope_apply_q(None, A16, A16 * 2, None, 1, 4, 8, 64, 64, 0, 0, 0, 1, 8, None) \
+        == R.ROPE_ERR_INVALID_ARG
+    assert lib.rope_apply_q(A16, A16 * 2, A16 * 3, None, 1, 4, 8, 64, 64, 0, 0, 0, 7, 8, None) \
+        == R.ROPE_ERR_UNSUPPORTED
+    assert lib.rope_apply_q(A16, A16 * 20, A16 * 30, None, 0, 4, 8, 64, 64, 0, 0, 0, 1, 8, None) \
+        == R.ROPE_OK
+
+
+@pytest.mark.parametrize("theta,rd,max_pos,f,cos,sin,status", [
+    (0.0, 64, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (-1.0, 64, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (float("nan"), 64, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (float("inf"), 64, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 64, 8, 0.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 63, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 0, 8, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 64, -1, 1.0, A16, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 64, 8, 1.0, None, A16 * 2, R.ROPE_ERR_INVALID_ARG),
+    (1e4, 64, 8, 1.0, A16, A16 + 16, R.ROPE_ERR_INVALID_ARG),   # cos and sin overlap
+    (1e4, 64, 0, 1.0, None, None, R.ROPE_OK),                  # empty table: no-op
+])
+def test_tables_build_rejects_bad_arguments(lib, theta, rd, max_pos, f, cos, sin, status):
+    assert lib.rope_tables_build(theta, rd, max_pos, f, cos, sin, None) == status
+
+
+@pytest.mark.parametrize("over,variant", [
+    (dict(), 1),                                   # bf16 split-half, rd*2 = 128 B: vectorised
+    (dict(layout=1), 1),
+    (dict(dtype=0), 1),                            # fp32 rd=64: 256 B span
+    (dict(dtype=2, sbh=1), 1),
+    (dict(q=A16 + 2), 2),                          # q not 16-byte aligned
+    (dict(k=A16 * 1000 + 8), 2),
+    (dict(cos=A16 * 2000 + 4), 2),
+    (dict(sin=A16 * 3000 + 4), 2),
+    (dict(rd=8, D=64), 2),                         # 16-byte span: not whole vector pairs
+    (dict(rd=16, D=64), 1),                        # 32-byte span (bf16)
+    (dict(rd=16, D=64, dtype=0), 1),               # 64-byte span (fp32)
+    (dict(rd=8, D=64, dtype=0), 1),                # 32-byte span (fp32)
+    (dict(rd=2, D=34), 2),                         # odd sizes
+    (dict(rd=32, D=36), 2),                        # rows of 72 B: not 16-byte aligned
+    (dict(rd=32, D=40), 1),                        # rows of 80 B
+    (dict(Hk=0, k=None), 1),
+    (dict(pos=A16 * 4000, rows=8), 1),             # gather: S may exceed table_rows
+])
+def test_kernel_variant_rules(lib, over, variant):
+    assert lib.rope_qk_kernel_variant(*qk_args(**over)) == variant
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(R, "_lib", None)
+    monkeypatch.setattr(R, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        R.load_library()

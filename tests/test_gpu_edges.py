@@ -1,0 +1,297 @@
+"""Edge cases of the CUDA library, through the C ABI.
+
+Vectorised vs element-wise kernels (bit-identical), odd and maximum sizes,
+layout permutation, backward as the negated sine, position gathers, the
+out-of-range flag, guard bands around every buffer, empty problems, streams.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import (assert_matches, gpu_bits, lib, oracle_apply, oracle_tables, pos_tensor,
+                      require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096
+FILL = 0xA5
+
+
+def case(B, Hq, Hk, S, D, rd, dtype, layout="split_half", sbh=False, rows=None, theta=1e4, seed=7):
+    return W.Workload("edge", B, Hq, Hk, S, D, rd, theta, dtype, layout, sbh,
+                      rows if rows is not None else S, "none", seed)
+
+
+class Guarded:
+    """A tensor placed inside a larger byte buffer filled with a sentinel."""
+
+    def __init__(self, src: torch.Tensor, byte_offset: int = 0):
+        nbytes = src.numel() * src.element_size()
+        self.buf = torch.full((2 * GUARD + nbytes + 64,), FILL, dtype=torch.uint8, device="cuda")
+        self.start = GUARD + byte_offset
+        self.nbytes = nbytes
+        raw = self.buf[self.start:self.start + nbytes]
+        self.t = raw.view(src.dtype).view(src.shape) if nbytes else torch.empty_like(src, device="cuda")
+        self.t.copy_(src)
+
+    def intact(self) -> bool:
+        torch.cuda.synchronize()
+        before = self.buf[:self.start]
+        after = self.buf[self.start + self.nbytes:]
+        return bool((before == FILL).all()) and bool((after == FILL).all())
+
+
+def apply(w, q, k, cos, sin, pos=None, backward=False, stream=None, rows=None):
+    R = lib()
+    R.rope_apply_qk(q, k, cos, sin, pos, w.B, w.Hq, w.Hk if k is not None else 0, w.S, w.D,
+                    w.rotary_dim, W.LAYOUTS[w.layout], int(w.seq_before_head), int(backward),
+                    W.DTYPES[w.dtype], rows if rows is not None else cos.shape[0], stream)
+
+
+def variant(w, q, k, cos, sin, pos=None):
+    R = lib()
+    return R.rope_qk_kernel_variant(q, k, cos, sin, pos, w.B, w.Hq, w.Hk, w.S, w.D, w.rotary_dim,
+                                    W.LAYOUTS[w.layout], int(w.seq_before_head), 0,
+                                    W.DTYPES[w.dtype], cos.shape[0])
+
+
+def tables(w):
+    c, s = oracle_tables(w.theta, w.rotary_dim, w.table_rows)
+    return c, s, torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+
+
+def check_vs_oracle(w, x_cpu, x_gpu, H, pos, backward, c32, s32, what=""):
+    yb, y64 = oracle_apply(w, W.bits(x_cpu), H, pos, backward, c32, s32)
+    assert_matches(w.dtype, gpu_bits(x_gpu), yb, y64, what)
+
+
+@pytest.mark.parametrize("sbh", [False, True])
+@pytest.mark.parametrize("layout", ["split_half", "interleaved"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_vector_and_elementwise_kernels_bit_identical(dtype, layout, sbh):
+    require_gpu()
+    w = case(2, 5, 3, 37, 128, 96, dtype, layout, sbh)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    e = q.element_size()
+    for backward in (False, True):
+        qa, ka = Guarded(q), Guarded(k)                 # 16-byte aligned
+        qm, km = Guarded(q, e), Guarded(k, e)           # one element off
+        assert variant(w, qa.t, ka.t, cg, sg) == 1
+        assert variant(w, qm.t, km.t, cg, sg) == 2
+        apply(w, qa.t, ka.t, cg, sg, backward=backward)
+        apply(w, qm.t, km.t, cg, sg, backward=backward)
+        assert np.array_equal(gpu_bits(qa.t), gpu_bits(qm.t))
+        assert np.array_equal(gpu_bits(ka.t), gpu_bits(km.t))
+        for g in (qa, ka, qm, km):
+            assert g.intact()
+        check_vs_oracle(w, q, qa.t, w.Hq, None, backward, c32, s32, "Q")
+        check_vs_oracle(w, k, ka.t, w.Hk, None, backward, c32, s32, "K")
+
+
+@pytest.mark.parametrize("D,rd,dtype,layout,want_variant", [
+    (34, 2, "bf16", "split_half", 2),
+    (10, 6, "f16", "interleaved", 2),
+    (8, 8, "bf16", "split_half", 2),            # 16-byte rotary span
+    (6, 4, "f32", "interleaved", 2),
+    (130, 130, "f16", "split_half", 2),
+    (64, 16, "bf16", "interleaved", 1),         # smallest vector span: one pair of vectors
+    (40, 32, "bf16", "split_half", 1),          # 80-byte rows
+    (2048, 2048, "f32", "split_half", 1),       # 256 vectors per half: largest vector CTA row
+    (2064, 2064, "f32", "interleaved", 2),      # 258 vectors per half: element-wise
+    (1024, 512, "bf16", "interleaved", 1),
+])
+def test_odd_and_large_shapes(D, rd, dtype, layout, want_variant):
+    require_gpu()
+    w = case(2, 3, 2, 19, D, rd, dtype, layout)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    qg, kg = Guarded(q), Guarded(k)
+    assert variant(w, qg.t, kg.t, cg, sg) == want_variant
+    for backward in (False, True):
+        qg.t.copy_(q)
+        kg.t.copy_(k)
+        apply(w, qg.t, kg.t, cg, sg, backward=backward)
+        check_vs_oracle(w, q, qg.t, w.Hq, None, backward, c32, s32, "Q")
+        check_vs_oracle(w, k, kg.t, w.Hk, None, backward, c32, s32, "K")
+        assert np.array_equal(gpu_bits(qg.t)[..., rd:], W.bits(q)[..., rd:])
+    assert qg.intact() and kg.intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_layout_permutation_bit_exact(dtype):
+    """Split-half of x equals interleaved of P x (P: 2i -> i, 2i+1 -> i + rd/2)."""
+    require_gpu()
+    w = case(1, 4, 2, 50, 128, 128, dtype)
+    q, k, _ = W.make_inputs(w)
+    _, _, cg, sg = tables(w)
+    h = w.rotary_dim // 2
+    perm = torch.arange(w.D)
+    perm[0:w.rotary_dim:2] = torch.arange(h)
+    perm[1:w.rotary_dim:2] = torch.arange(h) + h
+    qs, ks = q.cuda(), k.cuda()
+    qi, ki = q[..., perm].contiguous().cuda(), k[..., perm].contiguous().cuda()
+    apply(w, qs, ks, cg, sg)
+    apply(w.with_sizes(layout="interleaved"), qi, ki, cg, sg)
+    assert np.array_equal(gpu_bits(qi), gpu_bits(qs[..., perm].contiguous()))
+    assert np.array_equal(gpu_bits(ki), gpu_bits(ks[..., perm].contiguous()))
+
+
+@pytest.mark.parametrize("layout", ["split_half", "interleaved"])
+def test_backward_is_forward_with_negated_sine(layout):
+    require_gpu()
+    w = case(2, 4, 4, 64, 64, 64, "bf16", layout)
+    q, k, _ = W.make_inputs(w)
+    _, _, cg, sg = tables(w)
+    a, b = q.cuda(), k.cuda()
+    c, d = q.cuda(), k.cuda()
+    apply(w, a, b, cg, sg, backward=True)
+    apply(w, c, d, cg, -sg, backward=False)
+    assert torch.equal(a, c) and torch.equal(b, d)
+
+
+def test_gather_identity_and_prefix_shift():
+    """pos_idx = arange(S) equals no index; arange(S) + p equals rows p.. of
+    the table ("Custom Position IDs for Prefix-Tuning")."""
+    require_gpu()
+    p = 5
+    w = case(2, 6, 2, 100, 128, 128, "bf16", rows=100 + p)
+    q, k, _ = W.make_inputs(w)
+    _, _, cg, sg = tables(w)
+    ref_q, ref_k = q.cuda(), k.cuda()
+    apply(w, ref_q, ref_k, cg, sg)
+    a_q, a_k = q.cuda(), k.cuda()
+    apply(w, a_q, a_k, cg, sg, pos=pos_tensor(np.arange(w.S)))
+    assert torch.equal(a_q, ref_q) and torch.equal(a_k, ref_k)
+    s_q, s_k = q.cuda(), k.cuda()
+    apply(w, s_q, s_k, cg, sg, pos=pos_tensor(np.arange(w.S) + p))
+    t_q, t_k = q.cuda(), k.cuda()
+    apply(w, t_q, t_k, cg[p:].contiguous(), sg[p:].contiguous())
+    assert torch.equal(s_q, t_q) and torch.equal(s_k, t_k)
+    assert not torch.equal(s_q, ref_q)
+
+
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_out_of_range_positions_flagged_and_untouched(misaligned):
+    require_gpu()
+    R = lib()
+    assert R.rope_check_errors() == R.ROPE_OK
+    w = case(2, 4, 2, 20, 64, 64, "f16", rows=16)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    pos = np.arange(w.S, dtype=np.int32) % 16
+    pos[3] = 16            # one past the table
+    pos[5] = -7            # negative, not the -1 mask
+    pos[8] = -1            # masked: fine
+    qg, kg = Guarded(q, 2 if misaligned else 0), Guarded(k)
+    assert variant(w, qg.t, kg.t, cg, sg, pos_tensor(pos)) == (2 if misaligned else 1)
+    apply(w, qg.t, kg.t, cg, sg, pos=pos_tensor(pos))
+    assert R.rope_check_errors() == R.ROPE_ERR_POS_OUT_OF_RANGE
+    assert R.rope_check_errors() == R.ROPE_OK            # reading clears the flag
+    got = gpu_bits(qg.t)
+    xb = W.bits(q)
+    for s in (3, 5, 8):
+        assert np.array_equal(got[:, :, s], xb[:, :, s])
+    good = np.flatnonzero((pos >= 0))
+    yb, y64 = oracle_apply(w.with_sizes(S=len(good)), np.ascontiguousarray(xb[:, :, good]), w.Hq,
+                           pos[good], False, c32, s32)
+    assert_matches("f16", np.ascontiguousarray(got[:, :, good]), yb, y64)
+    assert qg.intact() and kg.intact()
+
+
+@pytest.mark.parametrize("vector", [True, False])
+def test_guard_bands_untouched(vector):
+    require_gpu()
+    w = case(3, 7, 3, 41, 64, 32, "bf16", rows=64)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, _, _ = tables(w)
+    off = 0 if vector else 2
+    qg, kg = Guarded(q, off), Guarded(k, off)
+    cg, sg = Guarded(torch.from_numpy(c32)), Guarded(torch.from_numpy(s32))
+    pos = np.arange(w.S, dtype=np.int32) + 3
+    pos[0] = -1
+    pg = Guarded(torch.from_numpy(pos))
+    assert variant(w, qg.t, kg.t, cg.t, sg.t, pg.t) == (1 if vector else 2)
+    for backward in (False, True):
+        apply(w, qg.t, kg.t, cg.t, sg.t, pos=pg.t, backward=backward)
+    for g in (qg, kg, cg, sg, pg):
+        assert g.intact()
+    assert torch.equal(cg.t.cpu(), torch.from_numpy(c32)) and torch.equal(pg.t.cpu(), torch.from_numpy(pos))
+
+
+def test_empty_problems_change_nothing():
+    require_gpu()
+    R = lib()
+    w = case(1, 2, 2, 8, 64, 64, "bf16")
+    q, k, _ = W.make_inputs(w)
+    _, _, cg, sg = tables(w)
+    qg, kg = q.cuda(), k.cuda()
+    for B, S, Hq, Hk in ((0, 8, 2, 2), (1, 0, 2, 2), (1, 8, 0, 0)):
+        R.rope_apply_qk(qg, kg, cg, sg, None, B, Hq, Hk, S, 64, 64, 0, 0, 0, R.ROPE_BF16, 8)
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(qg.cpu(), q) and torch.equal(kg.cpu(), k)
+
+
+def test_q_only_entry_and_gqa_without_k():
+    require_gpu()
+    R = lib()
+    w = case(2, 8, 0, 33, 128, 128, "bf16")
+    q, _, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    a, b = q.cuda(), q.cuda()
+    R.apply_q(a, cg, sg)
+    R.rope_apply_qk(b, None, cg, sg, None, w.B, w.Hq, 0, w.S, w.D, w.rotary_dim, 0, 0, 0,
+                    R.ROPE_BF16, cg.shape[0])
+    assert torch.equal(a, b)
+    check_vs_oracle(w, q, a, w.Hq, None, False, c32, s32)
+
+
+def test_single_token_single_head():
+    require_gpu()
+    w = case(1, 1, 1, 1, 128, 128, "f16")
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    qg, kg = q.cuda(), k.cuda()
+    apply(w, qg, kg, cg, sg)
+    check_vs_oracle(w, q, qg, 1, None, False, c32, s32)
+    assert torch.equal(qg.cpu(), q)           # position 0 is the identity
+
+
+def test_runs_on_the_given_stream():
+    require_gpu()
+    w = case(2, 8, 2, 300, 128, 128, "bf16")
+    q, k, _ = W.make_inputs(w)
+    _, _, cg, sg = tables(w)
+    a, b = q.cuda(), k.cuda()
+    c, d = q.cuda(), k.cuda()
+    apply(w, a, b, cg, sg)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        apply(w, c, d, cg, sg, stream=side)
+    side.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a, c) and torch.equal(b, d)
+
+
+def test_interpolate_factor_halves_positions_on_gpu():
+    require_gpu()
+    R = lib()
+    c2, s2 = R.build_tables(1e4, 64, 200, 2.0)
+    c1, s1 = R.build_tables(1e4, 64, 100, 1.0)
+    assert torch.equal(c2[0::2], c1) and torch.equal(s2[0::2], s1)
+
+
+def test_convenience_wrappers_match_abi_call():
+    require_gpu()
+    R = lib()
+    w = case(2, 4, 2, 64, 128, 128, "f16", layout="interleaved", sbh=True)
+    q, k, _ = W.make_inputs(w)
+    cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+    a, b = q.cuda(), k.cuda()
+    c, d = q.cuda(), k.cuda()
+    R.apply_qk(a, b, cos, sin, layout="interleaved", seq_before_head=True)
+    apply(w, c, d, cos, sin)
+    assert torch.equal(a, c) and torch.equal(b, d)
