@@ -42,8 +42,19 @@ enum Variant : int32_t { kNone = 0, kVector = 1, kScalar = 2 };
 #ifndef ROPE_VEC_UNROLL
 #define ROPE_VEC_UNROLL 4
 #endif
+// Resident CTAs per SM the register allocation must allow (launch bounds).
+#ifndef ROPE_VEC_MIN_BLOCKS
+#define ROPE_VEC_MIN_BLOCKS 1
+#endif
+// 0: one token per thread row (grid = ceil(B*S / tokens per CTA));
+// 1: persistent grid of SMs x resident CTAs, each with a balanced token range.
+#ifndef ROPE_VEC_PERSISTENT
+#define ROPE_VEC_PERSISTENT 0
+#endif
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
+constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;
+constexpr bool kVecPersistent = ROPE_VEC_PERSISTENT != 0;
 constexpr int kMaxVectorsPerHalf = 256;   // NJ limit of the vectorised kernel
 
 // Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).

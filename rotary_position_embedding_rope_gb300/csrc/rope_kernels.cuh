@@ -142,16 +142,20 @@ __device__ __forceinline__ void rotate_pair(float &x1, float &x2, float c, float
 // ---------------------------------------------------------------------------
 // Vectorised kernel.
 //   blockDim = (NJ, TS): NJ = 16-byte vectors per half of the rotary span,
-//   TS = tokens per CTA.  CTA `blk` covers batch blk / tiles_per_b and tokens
-//   (blk % tiles_per_b) * TS + [0, TS).
+//   TS = token rows per CTA.  Tokens are flattened as t = b * S + s.  CTA c
+//   of G owns the contiguous range [t0, t1) of a balanced split of the B*S
+//   tokens (sizes differ by at most one), and its thread row y takes tokens
+//   t0 + y, t0 + y + TS, ...  With G = ceil(B*S / TS) each row takes at most
+//   one token; with a persistent grid (G = SMs x resident CTAs) every SM
+//   gets the same share of the work in a single wave.
 //   Split-half: vector j holds elements [jV, jV+V) and vector j+NJ holds
 //   their partners [rd/2 + jV, ...); cos/sin columns [jV, jV+V).
 //   Interleaved: vector j holds pairs [jV/2, jV/2 + V/2) and vector j+NJ
 //   holds pairs [(j+NJ)V/2, ...); the thread keeps both column ranges.
 // ---------------------------------------------------------------------------
 template <typename T, int LAYOUT, int U>
-__global__ void __launch_bounds__(kVecThreads)
-rope_vec_kernel(const ApplyArgs p, int64_t tiles_per_b, int64_t total_blocks)
+__global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
+rope_vec_kernel(const ApplyArgs p, int64_t total_tokens)
 {
     constexpr int V = Elt<T>::V;
     const int NJ = blockDim.x;
@@ -159,11 +163,16 @@ rope_vec_kernel(const ApplyArgs p, int64_t tiles_per_b, int64_t total_blocks)
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
 
-    for (int64_t blk = blockIdx.x; blk < total_blocks; blk += gridDim.x) {
-        const int64_t b = blk / tiles_per_b;
-        const int64_t s = (blk - b * tiles_per_b) * TS + threadIdx.y;
-        if (s >= p.S)
-            continue;
+    const int64_t G = gridDim.x;
+    const int64_t c = blockIdx.x;
+    const int64_t share = total_tokens / G;
+    const int64_t extra = total_tokens - share * G;
+    const int64_t t0 = c * share + (c < extra ? c : extra);
+    const int64_t t1 = t0 + share + (c < extra ? 1 : 0);
+
+    for (int64_t t = t0 + threadIdx.y; t < t1; t += TS) {
+        const int64_t b = t / p.S;
+        const int64_t s = t - b * p.S;
 
         // position of this token: table row, -1 = leave unrotated
         int64_t r = s;
@@ -310,6 +319,20 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
 // ---------------------------------------------------------------------------
 // Host-side launcher for one element type.
 // ---------------------------------------------------------------------------
+// CTAs of `kernel` (with `threads` threads, no dynamic shared memory) that
+// the current device holds at once: SM count x resident CTAs per SM.
+inline cudaError_t resident_grid(const void *kernel, int threads, int *out)
+{
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    *out = sms * (per_sm > 0 ? per_sm : 1);
+    return e;
+}
+
 template <typename T>
 cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st)
 {
@@ -317,14 +340,23 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         constexpr int V = Elt<T>::V;
         const int NJ = (a.rotary_dim / 2) / V;                 // vectors per half span
         const int TS = NJ >= kVecThreads ? 1 : kVecThreads / NJ;
-        const int64_t tiles_per_b = (a.S + TS - 1) / TS;
-        const int64_t total_blocks = a.B * tiles_per_b;
-        const unsigned grid = (unsigned)(total_blocks < 0x7fffffffLL ? total_blocks : 0x7fffffffLL);
+        const int64_t tokens = a.B * a.S;
+        int64_t grid = (tokens + TS - 1) / TS;                 // one token per thread row
+        if (grid > 0x7fffffffLL)
+            grid = 0x7fffffffLL;
         const dim3 block(NJ, TS);
-        if (layout == 0)
-            rope_vec_kernel<T, 0, kVecUnroll><<<grid, block, 0, st>>>(a, tiles_per_b, total_blocks);
-        else
-            rope_vec_kernel<T, 1, kVecUnroll><<<grid, block, 0, st>>>(a, tiles_per_b, total_blocks);
+        auto kernel = layout == 0 ? rope_vec_kernel<T, 0, kVecUnroll>
+                                  : rope_vec_kernel<T, 1, kVecUnroll>;
+        if (kVecPersistent) {
+            int resident = 0;
+            cudaError_t e = resident_grid(reinterpret_cast<const void *>(kernel),
+                                          NJ * TS, &resident);
+            if (e != cudaSuccess)
+                return e;
+            if (grid > resident)
+                grid = resident;
+        }
+        kernel<<<(unsigned)grid, block, 0, st>>>(a, tokens);
         return cudaGetLastError();
     }
     const int64_t rows0 = a.B * a.S * a.t[0].heads;

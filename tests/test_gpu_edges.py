@@ -194,7 +194,7 @@ def test_out_of_range_positions_flagged_and_untouched(misaligned):
     xb = W.bits(q)
     for s in (3, 5, 8):
         assert np.array_equal(got[:, :, s], xb[:, :, s])
-    good = np.flatnonzero((pos >= 0))
+    good = np.flatnonzero((pos >= 0) & (pos < 16))
     yb, y64 = oracle_apply(w.with_sizes(S=len(good)), np.ascontiguousarray(xb[:, :, good]), w.Hq,
                            pos[good], False, c32, s32)
     assert_matches("f16", np.ascontiguousarray(got[:, :, good]), yb, y64)

@@ -61,13 +61,25 @@ def test_table_matches_oracle(theta, rd, rows, f):
     cos, sin = R.build_tables(theta, rd, rows, f)
     torch.cuda.synchronize()
     c64, s64 = oracle_tables(theta, rd, rows, f, "f64")
+    # Both sides evaluate theta^(-2i/rd) with their platform's fp64 pow (CUDA:
+    # within 2 ulp; glibc: within 1), so their fp64 angles may differ by up to
+    # about 2^-51 |angle|, and cos/sin by as much.  Bar per entry: 1 fp32 ulp
+    # of the oracle's fp64 value plus 2^-50 |angle|.  The angle term matters
+    # only near zeros of cos/sin at large angles (long-context tables).
+    h = rd // 2
+    angle = (np.arange(rows, dtype=np.float64)[:, None] / f) * \
+        np.power(float(theta), -2.0 * np.arange(h, dtype=np.float64) / rd)[None, :]
+    angle_term = 2.0 ** -50 * np.abs(angle)
     for name, g, e in (("cos", cos.cpu().numpy(), c64), ("sin", sin.cpu().numpy(), s64)):
         ulp32 = np.spacing(np.abs(e).astype(np.float32)).astype(np.float64)
         err = np.abs(g.astype(np.float64) - e)
-        assert np.all(err <= ulp32), "%s: %d entries beyond 1 fp32 ulp" % (name, np.sum(err > ulp32))
+        bad = err > ulp32 + angle_term
+        assert not bad.any(), "%s: %d entries beyond the bar" % (name, np.count_nonzero(bad))
         off = int(np.count_nonzero(g != e.astype(np.float32)))
+        beyond_ulp = int(np.count_nonzero(err > ulp32))
         print("table theta=%g rd=%d rows=%d f=%g %s: %d of %d entries differ from the oracle's "
-              "fp32 rounding (each by 1 ulp)" % (theta, rd, rows, f, name, off, g.size))
+              "fp32 rounding; %d need the angle term" % (theta, rd, rows, f, name, off, g.size,
+                                                         beyond_ulp))
 
 
 @pytest.mark.parametrize("backward", [False, True], ids=["fwd", "bwd"])
