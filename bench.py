@@ -45,9 +45,10 @@ import workloads as W  # noqa: E402
 METRIC = "fused Q+K RoPE fwd/bwd achieved HBM GB/s (% of GB300 peak) and µs/call"
 DEFAULT_WORKLOAD = "llama3_8b_gqa_bf16"
 FALLBACK_HBM_GBS = 6800.0
+EVENT_EVERY = 8
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
-                  for f in ("rope_kernels.cuh", "rope_internal.cuh", "rope_api.cu")]
+                  for f in ("rope_kernels.cuh", "rope_bulk.cuh", "rope_internal.cuh", "rope_api.cu")]
 
 
 def kernel_source_hash() -> str:
@@ -205,10 +206,13 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(workload: str):
+KERNEL_NAMES = {1: "rope_bulk_kernel", 2: "rope_scalar_kernel", 3: "rope_vec_kernel"}
+
+
+def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of the rotation kernel from a committed ncu summary,
     or None when there is none or the kernel sources changed since."""
-    path = os.path.join(PROFILE_DIR, "rope_vec_kernel_%s.md" % workload)
+    path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel, workload))
     try:
         text = open(path).read()
     except OSError:
@@ -387,9 +391,13 @@ def main():
     torch.cuda.synchronize(device)
     assert R.rope_check_errors(stream) == R.ROPE_OK
 
-    # timed region: K steps; per-launch events on the launching stream
-    n_ev = min(args.steps, 256)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
+    # timed region: K steps.  Per-launch events on the launching stream are
+    # recorded around every EVENT_EVERY-th step only: an event between two
+    # launches stops the next launch from becoming resident early (programmatic
+    # dependent launch), so the other steps run as a user's stream would.
+    ev_steps = [i for i in range(args.steps) if i % EVENT_EVERY == EVENT_EVERY - 1][-256:] or \
+        [args.steps - 1]
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in ev_steps}
     sampler = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -397,9 +405,8 @@ def main():
     sampler.start()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    first_ev = args.steps - n_ev
     for i in range(args.steps):
-        step(i, evs[i - first_ev] if i >= first_ev else None)
+        step(i, evs.get(i))
     t_end.record(stream)
     torch.cuda.synchronize(device)
     sampler.stop()
@@ -409,8 +416,8 @@ def main():
     launches = 2 * args.steps
     assert R.rope_check_errors(stream) == R.ROPE_OK
 
-    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs.values()]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs.values()]))
     bytes_call = W.algorithmic_bytes(w)
     bytes_step = 2 * bytes_call
     max_ms, all_bytes = aggregate(dist, device, local_ms, bytes_step * args.steps)
@@ -452,11 +459,15 @@ def main():
     e2e_ms, e2e_bytes = aggregate(dist, device, e0.elapsed_time(e1), bytes_step * args.e2e_steps)
     e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
 
-    # roofline of the dominant kernel (the vectorised rotation kernel: 2 launches per step)
+    # roofline of the dominant kernel (the rotation kernel: 2 launches per step)
     peak, peak_kind = hbm_peak()
     kernel_ms = (fwd_ms + bwd_ms) / 2
     achieved = bytes_call / (kernel_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(w.name)
+    qx0, kx0 = sets[0][0], sets[0][1]
+    variant = R.rope_qk_kernel_variant(qx0, kx0, cos, sin, pos_g, w.B, w.Hq, w.Hk, w.S, w.D,
+                                       w.rotary_dim, layout, sbh, 0, dt, w.table_rows)
+    kernel_name = KERNEL_NAMES.get(variant, "unknown")
+    traffic = profiled_traffic(kernel_name, w.name)
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -489,12 +500,13 @@ def main():
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic, "kernel": "rope_vec_kernel",
+                         "traffic": traffic, "kernel": kernel_name,
                          "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": h2d, "steps": args.e2e_steps,
                     "ms_per_step": round(e2e_ms / args.e2e_steps, 4)},
             "gpu_launches": launches,
+            "kernel_variant": variant,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -47,7 +47,8 @@ typedef enum {
     ROPE_ERR_INVALID_ARG = 1,      /* bad size, null pointer, overlap, ...       */
     ROPE_ERR_UNSUPPORTED = 2,      /* dtype or layout value outside the enums    */
     ROPE_ERR_CUDA = 3,             /* a CUDA call failed (launch, sync, ...)     */
-    ROPE_ERR_POS_OUT_OF_RANGE = 4  /* a position index was outside the table     */
+    ROPE_ERR_POS_OUT_OF_RANGE = 4, /* a position index was outside the table     */
+    ROPE_ERR_KERNEL_TIMEOUT = 5    /* a bounded wait inside a kernel expired      */
 } rope_status;
 
 typedef enum { ROPE_SPLIT_HALF = 0, ROPE_INTERLEAVED = 1 } rope_layout;
@@ -128,8 +129,10 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
 
 /*
  * rope_check_errors -- synchronise `stream`, then report and clear the
- * current device's position-range flag.
+ * current device's error flag.
  * Returns ROPE_ERR_CUDA if the stream reports an error, else
+ * ROPE_ERR_KERNEL_TIMEOUT if a wait inside the bulk-staged kernel expired
+ * (about 2 s; that launch stopped early and its output is incomplete), else
  * ROPE_ERR_POS_OUT_OF_RANGE if any launch since the last check met an
  * out-of-range position index, else ROPE_OK.  The flag is shared by all
  * streams of the device.
@@ -143,7 +146,10 @@ const char *rope_status_string(rope_status status);
  * rope_qk_kernel_variant -- which kernel rope_apply_qk would launch for
  * these arguments, without launching anything or touching the device.
  * Returns 0 when nothing would be launched (error or empty problem),
- * 1 for the 16-byte vectorised kernel, 2 for the element-wise kernel.
+ * 1 for the bulk-copy staged kernel (rows move between HBM and shared memory
+ * through the copy engine; the default for 16-byte aligned shapes),
+ * 2 for the element-wise kernel (any shape or alignment),
+ * 3 for the register-staged 16-byte vector kernel.
  * Useful for tests and for callers checking that their tensors are aligned.
  */
 int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, const float *sin,
@@ -151,6 +157,16 @@ int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, c
                                int64_t S, int32_t D, int32_t rotary_dim, int32_t layout,
                                int32_t seq_before_head, int32_t backward, int32_t dtype,
                                int64_t table_rows);
+
+/*
+ * rope_force_kernel_variant -- process-wide choice of the rotation kernel,
+ * for tests and tuning: 0 = automatic (default), 1, 2 or 3 as returned by
+ * rope_qk_kernel_variant.  While 1 or 3 is forced, calls whose shapes or
+ * pointers do not qualify for it return ROPE_ERR_UNSUPPORTED.  All three
+ * kernels compute bit-identical results.  ROPE_ERR_INVALID_ARG for other
+ * values.
+ */
+rope_status rope_force_kernel_variant(int32_t variant);
 
 #ifdef __cplusplus
 }

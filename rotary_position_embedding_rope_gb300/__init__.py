@@ -22,13 +22,16 @@ from . import _build
 
 __all__ = [
     "RopeError", "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
-    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
+    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_ERR_KERNEL_TIMEOUT", "VARIANT_BULK", "VARIANT_ELEMENTWISE",
+    "VARIANT_VECTOR", "rope_force_kernel_variant", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
     "library_path", "load_library",
 ]
 
-ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE = range(5)
+(ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
+ ROPE_ERR_KERNEL_TIMEOUT) = range(6)
+VARIANT_BULK, VARIANT_ELEMENTWISE, VARIANT_VECTOR = 1, 2, 3
 ROPE_SPLIT_HALF, ROPE_INTERLEAVED = 0, 1
 ROPE_F32, ROPE_BF16, ROPE_F16 = 0, 1, 2
 _DTYPE_CODE = {torch.float32: ROPE_F32, torch.bfloat16: ROPE_BF16, torch.float16: ROPE_F16}
@@ -79,6 +82,8 @@ def load_library() -> ctypes.CDLL:
                                            c.c_int64, c.c_int32, c.c_int32, c.c_int32,
                                            c.c_int32, c.c_int32, c.c_int32, c.c_int64]
     lib.rope_qk_kernel_variant.restype = c.c_int32
+    lib.rope_force_kernel_variant.argtypes = [c.c_int32]
+    lib.rope_force_kernel_variant.restype = c.c_int
     _lib = lib
     return lib
 
@@ -167,6 +172,10 @@ def rope_qk_kernel_variant(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim,
         _addr(sin, "sin", False), _addr(pos_idx, "pos_idx", False), int(B), int(Hq), int(Hk),
         int(S), int(D), int(rotary_dim), int(layout), int(seq_before_head), int(backward),
         int(dtype), int(table_rows))
+
+
+def rope_force_kernel_variant(variant: int):
+    _check(load_library().rope_force_kernel_variant(int(variant)), "rope_force_kernel_variant")
 
 
 # --------------------------------------------------------------------------

@@ -12,6 +12,7 @@ import os
 import shutil
 import subprocess
 import sys
+import uuid
 from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -58,7 +59,7 @@ def build(force: bool = False, extra_flags: list[str] | None = None, output: str
     os.makedirs(os.path.dirname(output), exist_ok=True)
     cc = nvcc()
     flags = NVCC_FLAGS + ARCH + list(extra_flags or [])
-    tag = "%d" % os.getpid()
+    tag = "%d_%s" % (os.getpid(), uuid.uuid4().hex[:8])   # unique per build, even in one process
 
     def compile_one(src):
         obj = os.path.join(OBJDIR, os.path.basename(src) + "." + tag + ".o")

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -13,8 +14,9 @@
 namespace rope {
 
 // ---------------------------------------------------------------------------
-// Device range flag: set (atomicOr) by the rotation kernels when a position
-// index is outside [0, table_rows) and not -1.  One word per device; the
+// Device flag word: bit 0 is set (atomicOr) by the rotation kernels when a
+// position index is outside [0, table_rows) and not -1; bit 1 when a wait of
+// the bulk-staged kernel ran out of its time budget.  One word per device; the
 // kernels get its address as an argument.  g_flag_taken receives the value
 // read-and-cleared by rope_check_errors.
 // ---------------------------------------------------------------------------
@@ -101,6 +103,9 @@ static bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Kernel variant forced by rope_force_kernel_variant (0 = automatic choice).
+static std::atomic<int32_t> g_forced_variant{0};
+
 struct Plan {
     ApplyArgs args;
     int32_t layout;
@@ -184,10 +189,18 @@ static rope_status plan_apply(void *q, void *k, const float *cos, const float *s
     // aligned rows, aligned base pointers and tables, and NJ within a CTA.
     const int64_t span_bytes = rotary_dim * elt;
     bool vec = (span_bytes % 32) == 0 && ((int64_t)D * elt) % 16 == 0 && aligned16(cos) &&
-               aligned16(sin) && span_bytes / 32 <= kVecThreads;
+               aligned16(sin) && span_bytes / 32 <= kMaxVectorsPerHalf;
     for (int t = 0; t < n; ++t)
         vec = vec && aligned16(a.t[t].base);
-    plan->variant = vec ? kVector : kScalar;
+    const int32_t forced = g_forced_variant.load(std::memory_order_relaxed);
+    if (forced == kScalar)
+        plan->variant = kScalar;
+    else if (forced == kBulk || forced == kVector) {
+        if (!vec)
+            return ROPE_ERR_UNSUPPORTED;
+        plan->variant = static_cast<Variant>(forced);
+    } else
+        plan->variant = vec ? kVector : kScalar;
     return ROPE_OK;
 }
 
@@ -284,7 +297,17 @@ rope_status rope_check_errors(void *stream)
     if (cudaMemcpyAsync(&value, taken, sizeof value, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return ROPE_ERR_CUDA;
+    if (value & 2)
+        return ROPE_ERR_KERNEL_TIMEOUT;
     return value ? ROPE_ERR_POS_OUT_OF_RANGE : ROPE_OK;
+}
+
+rope_status rope_force_kernel_variant(int32_t variant)
+{
+    if (variant < 0 || variant > 3)
+        return ROPE_ERR_INVALID_ARG;
+    g_forced_variant.store(variant, std::memory_order_relaxed);
+    return ROPE_OK;
 }
 
 const char *rope_status_string(rope_status status)
@@ -295,6 +318,7 @@ const char *rope_status_string(rope_status status)
     case ROPE_ERR_UNSUPPORTED: return "ROPE_ERR_UNSUPPORTED";
     case ROPE_ERR_CUDA: return "ROPE_ERR_CUDA";
     case ROPE_ERR_POS_OUT_OF_RANGE: return "ROPE_ERR_POS_OUT_OF_RANGE";
+    case ROPE_ERR_KERNEL_TIMEOUT: return "ROPE_ERR_KERNEL_TIMEOUT";
     default: return "ROPE_STATUS_UNKNOWN";
     }
 }

@@ -33,29 +33,51 @@ struct ApplyArgs {
     int32_t *range_flag;       // device word set when a position is out of range
 };
 
-enum Variant : int32_t { kNone = 0, kVector = 1, kScalar = 2 };
+// Kernel variants: kBulk stages rows through shared memory with bulk copies
+// (the default for aligned shapes), kVector moves 16-byte vectors through
+// registers, kScalar handles any shape one pair at a time.
+enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
 
 // Threads per CTA of the vectorised kernel and heads in flight per thread.
 #ifndef ROPE_VEC_THREADS
-#define ROPE_VEC_THREADS 256
+#define ROPE_VEC_THREADS 128
 #endif
 #ifndef ROPE_VEC_UNROLL
 #define ROPE_VEC_UNROLL 4
 #endif
 // Resident CTAs per SM the register allocation must allow (launch bounds).
 #ifndef ROPE_VEC_MIN_BLOCKS
-#define ROPE_VEC_MIN_BLOCKS 1
+#define ROPE_VEC_MIN_BLOCKS 4
 #endif
 // 0: one token per thread row (grid = ceil(B*S / tokens per CTA));
 // 1: persistent grid of SMs x resident CTAs, each with a balanced token range.
 #ifndef ROPE_VEC_PERSISTENT
 #define ROPE_VEC_PERSISTENT 0
 #endif
+// Threads the register kernel aims to run at once; below that, a token's
+// heads are split into groups handled by separate thread rows.
+#ifndef ROPE_VEC_TARGET_THREADS
+#define ROPE_VEC_TARGET_THREADS (152 * 32)
+#endif
+// Launch the hot kernels with programmatic dependent launch.
+#ifndef ROPE_PDL
+#define ROPE_PDL 1
+#endif
+// Register kernel: keep the next batch of heads' loads in flight while
+// rotating the current batch.
+#ifndef ROPE_VEC_PIPELINE
+#define ROPE_VEC_PIPELINE 1
+#endif
+constexpr bool kVecPipeline = ROPE_VEC_PIPELINE != 0;
+constexpr int64_t kVecTargetThreads = ROPE_VEC_TARGET_THREADS;
+constexpr bool kPdl = ROPE_PDL != 0;
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
 constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;
 constexpr bool kVecPersistent = ROPE_VEC_PERSISTENT != 0;
-constexpr int kMaxVectorsPerHalf = 256;   // NJ limit of the vectorised kernel
+// NJ (16-byte vectors per half span) must fit in one CTA row: the register
+// and bulk kernels take rotary spans of up to 32 * kVecThreads bytes.
+constexpr int kMaxVectorsPerHalf = kVecThreads;
 
 // Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).
 cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);

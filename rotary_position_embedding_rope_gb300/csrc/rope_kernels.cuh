@@ -140,14 +140,135 @@ __device__ __forceinline__ void rotate_pair(float &x1, float &x2, float c, float
 }
 
 // ---------------------------------------------------------------------------
-// Vectorised kernel.
+// Programmatic dependent launch.  The hot kernels are launched with the
+// programmatic-stream-serialisation attribute: the next launch in the stream
+// may become resident while this one drains.  Every kernel waits for the
+// previous grid to complete (and its memory to be visible) before it reads or
+// writes global memory, so results do not depend on the overlap.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_hot(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = kPdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Rotate the rotary spans of heads [lo, hi) of one token, whose head 0 row
+// starts at row0 (heads stride_h elements apart).  U heads' loads are issued
+// before any arithmetic; with kVecPipeline the loads of the next U heads are
+// issued before the current ones are rotated, so two batches are in flight.
+template <typename T, int LAYOUT>
+__device__ __forceinline__ void rotate_vectors(uint4 &va, uint4 &vb, const float *c,
+                                               const float *sn)
+{
+    constexpr int V = Elt<T>::V;
+    float fa[V], fb[V];
+    Elt<T>::unpack(va, fa);
+    Elt<T>::unpack(vb, fb);
+    if constexpr (LAYOUT == 0) {
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            rotate_pair(fa[e], fb[e], c[e], sn[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < V / 2; ++e) {
+            rotate_pair(fa[2 * e], fa[2 * e + 1], c[e], sn[e]);
+            rotate_pair(fb[2 * e], fb[2 * e + 1], c[V / 2 + e], sn[V / 2 + e]);
+        }
+    }
+    va = Elt<T>::pack(fa);
+    vb = Elt<T>::pack(fb);
+}
+
+template <typename T, int LAYOUT, int U>
+__device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t lo, int32_t hi,
+                                             int j, int NJ, const float *c, const float *sn)
+{
+    if constexpr (!kVecPipeline) {
+        for (int32_t h0 = lo; h0 < hi; h0 += U) {
+            uint4 va[U], vb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (h0 + u < hi) {
+                    const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
+                    va[u] = __ldcs(ptr + j);
+                    vb[u] = __ldcs(ptr + j + NJ);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (h0 + u < hi) {
+                    rotate_vectors<T, LAYOUT>(va[u], vb[u], c, sn);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
+                    __stcs(ptr + j, va[u]);
+                    __stcs(ptr + j + NJ, vb[u]);
+                }
+            }
+        }
+    } else {
+        uint4 ca[U], cb[U], na[U], nb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (lo + u < hi) {
+                const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(lo + u) * stride_h);
+                ca[u] = __ldcs(ptr + j);
+                cb[u] = __ldcs(ptr + j + NJ);
+            }
+        }
+        for (int32_t h0 = lo; h0 < hi; h0 += U) {
+            const int32_t h1 = h0 + U;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (h1 + u < hi) {
+                    const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(h1 + u) * stride_h);
+                    na[u] = __ldcs(ptr + j);
+                    nb[u] = __ldcs(ptr + j + NJ);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (h0 + u < hi) {
+                    rotate_vectors<T, LAYOUT>(ca[u], cb[u], c, sn);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
+                    __stcs(ptr + j, ca[u]);
+                    __stcs(ptr + j + NJ, cb[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                ca[u] = na[u];
+                cb[u] = nb[u];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Register-staged vector kernel.
 //   blockDim = (NJ, TS): NJ = 16-byte vectors per half of the rotary span,
-//   TS = token rows per CTA.  Tokens are flattened as t = b * S + s.  CTA c
-//   of G owns the contiguous range [t0, t1) of a balanced split of the B*S
-//   tokens (sizes differ by at most one), and its thread row y takes tokens
-//   t0 + y, t0 + y + TS, ...  With G = ceil(B*S / TS) each row takes at most
-//   one token; with a persistent grid (G = SMs x resident CTAs) every SM
-//   gets the same share of the work in a single wave.
+//   TS = item rows per CTA.  An item is (token, head group): token t = b*S+s
+//   and the group's heads [g*HPG, min(P, (g+1)*HPG)) of the P = Hq + Hk
+//   heads.  With one group (the default for long head lists is several) a
+//   token's cos/sin values are loaded once and reused for all P heads; more
+//   groups shorten each thread's chain of dependent memory round trips.
+//   CTA c of G owns a balanced contiguous range of the items; its row y takes
+//   items i0 + y, i0 + y + TS, ...
 //   Split-half: vector j holds elements [jV, jV+V) and vector j+NJ holds
 //   their partners [rd/2 + jV, ...); cos/sin columns [jV, jV+V).
 //   Interleaved: vector j holds pairs [jV/2, jV/2 + V/2) and vector j+NJ
@@ -155,24 +276,30 @@ __device__ __forceinline__ void rotate_pair(float &x1, float &x2, float c, float
 // ---------------------------------------------------------------------------
 template <typename T, int LAYOUT, int U>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
-rope_vec_kernel(const ApplyArgs p, int64_t total_tokens)
+rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t heads_per_group)
 {
     constexpr int V = Elt<T>::V;
     const int NJ = blockDim.x;
     const int TS = blockDim.y;
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
+    const int32_t P = p.t[0].heads + (p.ntensors > 1 ? p.t[1].heads : 0);
 
     const int64_t G = gridDim.x;
     const int64_t c = blockIdx.x;
-    const int64_t share = total_tokens / G;
-    const int64_t extra = total_tokens - share * G;
-    const int64_t t0 = c * share + (c < extra ? c : extra);
-    const int64_t t1 = t0 + share + (c < extra ? 1 : 0);
+    const int64_t share = total_items / G;
+    const int64_t extra = total_items - share * G;
+    const int64_t i0 = c * share + (c < extra ? c : extra);
+    const int64_t i1 = i0 + share + (c < extra ? 1 : 0);
 
-    for (int64_t t = t0 + threadIdx.y; t < t1; t += TS) {
-        const int64_t b = t / p.S;
-        const int64_t s = t - b * p.S;
+    pdl_wait();
+    pdl_trigger();
+
+    for (int64_t item = i0 + threadIdx.y; item < i1; item += TS) {
+        const int64_t tok = groups == 1 ? item : item / groups;
+        const int32_t g = static_cast<int32_t>(item - tok * groups);
+        const int64_t b = tok / p.S;
+        const int64_t s = tok - b * p.S;
 
         // position of this token: table row, -1 = leave unrotated
         int64_t r = s;
@@ -181,13 +308,13 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_tokens)
             if (r == -1)
                 continue;
             if (r < 0 || r >= p.table_rows) {
-                if (j == 0)
+                if (j == 0 && g == 0)
                     atomicOr(p.range_flag, 1);
                 continue;
             }
         }
 
-        // this thread's cos/sin values, kept in registers for every head
+        // this thread's cos/sin values, kept in registers for the group's heads
         float c[V], sn[V];
         const float *crow = p.cos + r * h;
         const float *srow = p.sin + r * h;
@@ -222,46 +349,20 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_tokens)
                 sn[e] = -sn[e];
         }
 
+        const int32_t hb = g * heads_per_group;
+        const int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
 #pragma unroll
         for (int ti = 0; ti < 2; ++ti) {
             if (ti >= p.ntensors)
                 break;
-            const TensorRef t = p.t[ti];
+            const TensorRef t = p.t[ti];                  // static index after unrolling
+            const int32_t off = ti ? p.t[0].heads : 0;
+            const int32_t lo = (hb > off ? hb : off) - off;
+            const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
+            if (lo >= hi)
+                continue;
             T *row0 = static_cast<T *>(t.base) + b * t.stride_b + s * t.stride_s;
-            for (int h0 = 0; h0 < t.heads; h0 += U) {
-                uint4 va[U], vb[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (h0 + u < t.heads) {
-                        const uint4 *ptr =
-                            reinterpret_cast<const uint4 *>(row0 + (int64_t)(h0 + u) * t.stride_h);
-                        va[u] = __ldcs(ptr + j);
-                        vb[u] = __ldcs(ptr + j + NJ);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (h0 + u < t.heads) {
-                        float fa[V], fb[V];
-                        Elt<T>::unpack(va[u], fa);
-                        Elt<T>::unpack(vb[u], fb);
-                        if constexpr (LAYOUT == 0) {
-#pragma unroll
-                            for (int e = 0; e < V; ++e)
-                                rotate_pair(fa[e], fb[e], c[e], sn[e]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < V / 2; ++e) {
-                                rotate_pair(fa[2 * e], fa[2 * e + 1], c[e], sn[e]);
-                                rotate_pair(fb[2 * e], fb[2 * e + 1], c[V / 2 + e], sn[V / 2 + e]);
-                            }
-                        }
-                        uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * t.stride_h);
-                        __stcs(ptr + j, Elt<T>::pack(fa));
-                        __stcs(ptr + j + NJ, Elt<T>::pack(fb));
-                    }
-                }
-            }
+            rotate_heads<T, LAYOUT, U>(row0, t.stride_h, lo, hi, j, NJ, c, sn);
         }
     }
 }
@@ -340,24 +441,30 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         constexpr int V = Elt<T>::V;
         const int NJ = (a.rotary_dim / 2) / V;                 // vectors per half span
         const int TS = NJ >= kVecThreads ? 1 : kVecThreads / NJ;
-        const int64_t tokens = a.B * a.S;
-        int64_t grid = (tokens + TS - 1) / TS;                 // one token per thread row
+        const int32_t P = a.t[0].heads + (a.ntensors > 1 ? a.t[1].heads : 0);
+        // Split the heads into groups only when one thread row per token
+        // leaves the GPU short of threads (small batches, few tokens, narrow
+        // rotary spans); at most one group per kVecUnroll heads.
+        const int64_t rows_threads = a.B * a.S * NJ;
+        int64_t want = rows_threads > 0 ? (kVecTargetThreads + rows_threads - 1) / rows_threads : 1;
+        const int32_t max_groups = (P + kVecUnroll - 1) / kVecUnroll;
+        const int32_t groups = (int32_t)(want < 1 ? 1 : (want > max_groups ? max_groups : want));
+        const int32_t hpg = (P + groups - 1) / groups;
+        const int64_t items = a.B * a.S * groups;
+        int64_t grid = (items + TS - 1) / TS;                  // one item per thread row
         if (grid > 0x7fffffffLL)
             grid = 0x7fffffffLL;
-        const dim3 block(NJ, TS);
         auto kernel = layout == 0 ? rope_vec_kernel<T, 0, kVecUnroll>
                                   : rope_vec_kernel<T, 1, kVecUnroll>;
         if (kVecPersistent) {
             int resident = 0;
-            cudaError_t e = resident_grid(reinterpret_cast<const void *>(kernel),
-                                          NJ * TS, &resident);
+            cudaError_t e = resident_grid(reinterpret_cast<const void *>(kernel), NJ * TS, &resident);
             if (e != cudaSuccess)
                 return e;
             if (grid > resident)
                 grid = resident;
         }
-        kernel<<<(unsigned)grid, block, 0, st>>>(a, tokens);
-        return cudaGetLastError();
+        return launch_hot(kernel, dim3((unsigned)grid), dim3(NJ, TS), 0, st, a, items, groups, hpg);
     }
     const int64_t rows0 = a.B * a.S * a.t[0].heads;
     const int64_t rows1 = a.ntensors > 1 ? a.B * a.S * a.t[1].heads : 0;

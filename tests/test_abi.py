@@ -122,23 +122,25 @@ def test_tables_build_rejects_bad_arguments(lib, theta, rd, max_pos, f, cos, sin
 
 
 @pytest.mark.parametrize("over,variant", [
-    (dict(), 1),                                   # bf16 split-half, rd*2 = 128 B: vectorised
-    (dict(layout=1), 1),
-    (dict(dtype=0), 1),                            # fp32 rd=64: 256 B span
-    (dict(dtype=2, sbh=1), 1),
+    (dict(), 3),                                   # bf16 split-half, rd*2 = 128 B: vectorised
+    (dict(layout=1), 3),
+    (dict(dtype=0), 3),                            # fp32 rd=64: 256 B span
+    (dict(dtype=2, sbh=1), 3),
     (dict(q=A16 + 2), 2),                          # q not 16-byte aligned
     (dict(k=A16 * 1000 + 8), 2),
     (dict(cos=A16 * 2000 + 4), 2),
     (dict(sin=A16 * 3000 + 4), 2),
     (dict(rd=8, D=64), 2),                         # 16-byte span: not whole vector pairs
-    (dict(rd=16, D=64), 1),                        # 32-byte span (bf16)
-    (dict(rd=16, D=64, dtype=0), 1),               # 64-byte span (fp32)
-    (dict(rd=8, D=64, dtype=0), 1),                # 32-byte span (fp32)
+    (dict(rd=16, D=64), 3),                        # 32-byte span (bf16)
+    (dict(rd=16, D=64, dtype=0), 3),               # 64-byte span (fp32)
+    (dict(rd=8, D=64, dtype=0), 3),                # 32-byte span (fp32)
     (dict(rd=2, D=34), 2),                         # odd sizes
     (dict(rd=32, D=36), 2),                        # rows of 72 B: not 16-byte aligned
-    (dict(rd=32, D=40), 1),                        # rows of 80 B
-    (dict(Hk=0, k=None), 1),
-    (dict(pos=A16 * 4000, rows=8), 1),             # gather: S may exceed table_rows
+    (dict(rd=32, D=40), 3),                        # rows of 80 B
+    (dict(Hk=0, k=None), 3),
+    (dict(pos=A16 * 4000, rows=8), 3),             # gather: S may exceed table_rows
+    (dict(rd=1024, D=1024, dtype=0, cos=A16 * 2000, sin=A16 * 2100), 3),   # 128 vectors per half
+    (dict(rd=1032, D=1032, dtype=0, cos=A16 * 2000, sin=A16 * 2100), 2),   # 129: element-wise
 ])
 def test_kernel_variant_rules(lib, over, variant):
     assert lib.rope_qk_kernel_variant(*qk_args(**over)) == variant
@@ -149,3 +151,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(R, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         R.load_library()
+
+
+def test_force_kernel_variant_rules(lib):
+    try:
+        assert lib.rope_force_kernel_variant(4) == R.ROPE_ERR_INVALID_ARG
+        assert lib.rope_force_kernel_variant(-1) == R.ROPE_ERR_INVALID_ARG
+        for forced, aligned_want, unaligned_want in ((0, 3, 2), (1, 1, 0), (2, 2, 2), (3, 3, 0)):
+            assert lib.rope_force_kernel_variant(forced) == R.ROPE_OK
+            assert lib.rope_qk_kernel_variant(*qk_args()) == aligned_want
+            assert lib.rope_qk_kernel_variant(*qk_args(q=A16 + 2)) == unaligned_want
+        assert lib.rope_force_kernel_variant(3) == R.ROPE_OK
+        # a forced kernel that does not fit the arguments is refused before any launch
+        assert lib.rope_apply_qk(*qk_args(q=A16 + 2), None) == R.ROPE_ERR_UNSUPPORTED
+    finally:
+        lib.rope_force_kernel_variant(0)
+    assert R.rope_status_string(R.ROPE_ERR_KERNEL_TIMEOUT) == "ROPE_ERR_KERNEL_TIMEOUT"

@@ -79,7 +79,7 @@ def test_vector_and_elementwise_kernels_bit_identical(dtype, layout, sbh):
     for backward in (False, True):
         qa, ka = Guarded(q), Guarded(k)                 # 16-byte aligned
         qm, km = Guarded(q, e), Guarded(k, e)           # one element off
-        assert variant(w, qa.t, ka.t, cg, sg) == 1
+        assert variant(w, qa.t, ka.t, cg, sg) == 3
         assert variant(w, qm.t, km.t, cg, sg) == 2
         apply(w, qa.t, ka.t, cg, sg, backward=backward)
         apply(w, qm.t, km.t, cg, sg, backward=backward)
@@ -97,11 +97,12 @@ def test_vector_and_elementwise_kernels_bit_identical(dtype, layout, sbh):
     (8, 8, "bf16", "split_half", 2),            # 16-byte rotary span
     (6, 4, "f32", "interleaved", 2),
     (130, 130, "f16", "split_half", 2),
-    (64, 16, "bf16", "interleaved", 1),         # smallest vector span: one pair of vectors
-    (40, 32, "bf16", "split_half", 1),          # 80-byte rows
-    (2048, 2048, "f32", "split_half", 1),       # 256 vectors per half: largest vector CTA row
-    (2064, 2064, "f32", "interleaved", 2),      # 258 vectors per half: element-wise
-    (1024, 512, "bf16", "interleaved", 1),
+    (64, 16, "bf16", "interleaved", 3),         # smallest vector span: one pair of vectors
+    (40, 32, "bf16", "split_half", 3),          # 80-byte rows
+    (1024, 1024, "f32", "split_half", 3),       # 128 vectors per half: widest vector CTA row
+    (1032, 1032, "f32", "interleaved", 2),      # 129 vectors per half: element-wise
+    (2048, 2048, "f32", "split_half", 2),
+    (1024, 512, "bf16", "interleaved", 3),
 ])
 def test_odd_and_large_shapes(D, rd, dtype, layout, want_variant):
     require_gpu()
@@ -186,7 +187,7 @@ def test_out_of_range_positions_flagged_and_untouched(misaligned):
     pos[5] = -7            # negative, not the -1 mask
     pos[8] = -1            # masked: fine
     qg, kg = Guarded(q, 2 if misaligned else 0), Guarded(k)
-    assert variant(w, qg.t, kg.t, cg, sg, pos_tensor(pos)) == (2 if misaligned else 1)
+    assert variant(w, qg.t, kg.t, cg, sg, pos_tensor(pos)) == (2 if misaligned else 3)
     apply(w, qg.t, kg.t, cg, sg, pos=pos_tensor(pos))
     assert R.rope_check_errors() == R.ROPE_ERR_POS_OUT_OF_RANGE
     assert R.rope_check_errors() == R.ROPE_OK            # reading clears the flag
@@ -213,7 +214,7 @@ def test_guard_bands_untouched(vector):
     pos = np.arange(w.S, dtype=np.int32) + 3
     pos[0] = -1
     pg = Guarded(torch.from_numpy(pos))
-    assert variant(w, qg.t, kg.t, cg.t, sg.t, pg.t) == (1 if vector else 2)
+    assert variant(w, qg.t, kg.t, cg.t, sg.t, pg.t) == (3 if vector else 2)
     for backward in (False, True):
         apply(w, qg.t, kg.t, cg.t, sg.t, pos=pg.t, backward=backward)
     for g in (qg, kg, cg, sg, pg):
@@ -295,3 +296,70 @@ def test_convenience_wrappers_match_abi_call():
     R.apply_qk(a, b, cos, sin, layout="interleaved", seq_before_head=True)
     apply(w, c, d, cos, sin)
     assert torch.equal(a, c) and torch.equal(b, d)
+
+
+@pytest.fixture
+def restore_variant():
+    yield
+    lib().rope_force_kernel_variant(0)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(B=2, Hq=5, Hk=3, S=70, D=128, rd=128, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=3, Hq=4, Hk=2, S=45, D=128, rd=128, dtype="f16", layout="interleaved", sbh=True),
+    dict(B=2, Hq=6, Hk=6, S=300, D=64, rd=32, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=1, Hq=3, Hk=0, S=33, D=64, rd=64, dtype="f32", layout="interleaved", sbh=False),
+    dict(B=2, Hq=2, Hk=1, S=17, D=96, rd=64, dtype="f32", layout="split_half", sbh=True),
+    dict(B=1, Hq=2, Hk=2, S=9, D=1024, rd=1024, dtype="f32", layout="split_half", sbh=False),
+])
+@pytest.mark.parametrize("positions", ["none", "masked", "out_of_range"])
+def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
+    """Bulk-staged, register-vector and element-wise kernels give the same bits,
+    and touch nothing outside the rotated spans."""
+    require_gpu()
+    R = lib()
+    rows = cfg["S"] + 8
+    w = case(cfg["B"], cfg["Hq"], cfg["Hk"], cfg["S"], cfg["D"], cfg["rd"], cfg["dtype"],
+             cfg["layout"], cfg["sbh"], rows=rows)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    pos = None
+    if positions != "none":
+        pos = (np.arange(w.S, dtype=np.int32) * 7 + 3) % rows
+        pos[:2] = -1
+        pos[w.S // 2] = -1
+        if positions == "out_of_range":
+            pos[w.S - 1] = rows + 5
+    pos_g = None if pos is None else pos_tensor(pos)
+    results = {}
+    for v in (1, 3, 2):
+        R.rope_force_kernel_variant(v)
+        for backward in (False, True):
+            qg = Guarded(q)
+            kg = Guarded(k) if k is not None else None
+            assert variant(w, qg.t, None if kg is None else kg.t, cg, sg, pos_g) == v
+            apply(w, qg.t, None if kg is None else kg.t, cg, sg, pos=pos_g, backward=backward)
+            st = R.rope_check_errors()
+            want = R.ROPE_ERR_POS_OUT_OF_RANGE if positions == "out_of_range" else R.ROPE_OK
+            assert st == want, (v, st)
+            assert qg.intact() and (kg is None or kg.intact())
+            results[(v, backward)] = (gpu_bits(qg.t), None if kg is None else gpu_bits(kg.t))
+    for backward in (False, True):
+        for v in (3, 2):
+            a, b = results[(1, backward)], results[(v, backward)]
+            assert np.array_equal(a[0], b[0]), (v, backward)
+            if a[1] is not None:
+                assert np.array_equal(a[1], b[1]), (v, backward)
+    # and the bulk result against the oracle on the rows the oracle accepts
+    good = np.ones(w.S, bool) if pos is None else (pos >= 0) & (pos < rows)
+    sa = 1 if w.seq_before_head else 2
+    for x, H, got in ((q, w.Hq, results[(1, False)][0]), (k, w.Hk, results[(1, False)][1])):
+        if x is None or H == 0:
+            continue
+        idx = np.flatnonzero(good)
+        xb = np.ascontiguousarray(np.take(W.bits(x), idx, axis=sa))
+        yb, y64 = oracle_apply(w.with_sizes(S=len(idx)), xb, H, None if pos is None else pos[idx],
+                               False, c32, s32)
+        assert_matches(w.dtype, np.ascontiguousarray(np.take(got, idx, axis=sa)), yb, y64)
+        bad = np.flatnonzero(~good)
+        assert np.array_equal(np.take(got, bad, axis=sa), np.take(W.bits(x), bad, axis=sa))
