@@ -45,7 +45,6 @@ import workloads as W  # noqa: E402
 METRIC = "fused Q+K RoPE fwd/bwd achieved HBM GB/s (% of GB300 peak) and µs/call"
 DEFAULT_WORKLOAD = "llama3_8b_gqa_bf16"
 FALLBACK_HBM_GBS = 6800.0
-EVENT_EVERY = 8
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
                   for f in ("rope_kernels.cuh", "rope_bulk.cuh", "rope_internal.cuh", "rope_api.cu")]
@@ -391,13 +390,10 @@ def main():
     torch.cuda.synchronize(device)
     assert R.rope_check_errors(stream) == R.ROPE_OK
 
-    # timed region: K steps.  Per-launch events on the launching stream are
-    # recorded around every EVENT_EVERY-th step only: an event between two
-    # launches stops the next launch from becoming resident early (programmatic
-    # dependent launch), so the other steps run as a user's stream would.
-    ev_steps = [i for i in range(args.steps) if i % EVENT_EVERY == EVENT_EVERY - 1][-256:] or \
-        [args.steps - 1]
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in ev_steps}
+    # timed region: K steps and nothing else on the stream, bracketed by two
+    # events.  No event sits between launches inside it: an event there would
+    # stop the next launch from becoming resident early (programmatic
+    # dependent launch), which a user's stream does not do.
     sampler = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -406,7 +402,7 @@ def main():
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(i, evs.get(i))
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize(device)
     sampler.stop()
@@ -416,8 +412,14 @@ def main():
     launches = 2 * args.steps
     assert R.rope_check_errors(stream) == R.ROPE_OK
 
-    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs.values()]))
-    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs.values()]))
+    # per-call durations in isolation (an event on each side of every launch),
+    # after the timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(64)]
+    for i, e in enumerate(evs):
+        step(i, e)
+    torch.cuda.synchronize(device)
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     bytes_call = W.algorithmic_bytes(w)
     bytes_step = 2 * bytes_call
     max_ms, all_bytes = aggregate(dist, device, local_ms, bytes_step * args.steps)
@@ -459,9 +461,11 @@ def main():
     e2e_ms, e2e_bytes = aggregate(dist, device, e0.elapsed_time(e1), bytes_step * args.e2e_steps)
     e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
 
-    # roofline of the dominant kernel (the rotation kernel: 2 launches per step)
+    # roofline of the dominant kernel.  The timed region holds only its
+    # launches (2 per step), so its average launch duration is the region's
+    # event time over the launch count.
     peak, peak_kind = hbm_peak()
-    kernel_ms = (fwd_ms + bwd_ms) / 2
+    kernel_ms = local_ms / launches
     achieved = bytes_call / (kernel_ms * 1e-3) / 1e9
     qx0, kx0 = sets[0][0], sets[0][1]
     variant = R.rope_qk_kernel_variant(qx0, kx0, cos, sin, pos_g, w.B, w.Hq, w.Hk, w.S, w.D,
@@ -494,7 +498,10 @@ def main():
                     "%.0f MB in all vs %.0f MB L2" % (nsets, set_bytes / 1e6,
                                                       nsets * set_bytes / 1e6, l2_bytes / 1e6)),
                 parallelism="replicas" if world > 1 else "single GPU"),
-            "us_per_call": {"forward": round(fwd_ms * 1e3, 3), "backward": round(bwd_ms * 1e3, 3)},
+            "us_per_call": round(kernel_ms * 1e3, 3),
+            "us_per_call_isolated": {"forward": round(fwd_ms * 1e3, 3),
+                                     "backward": round(bwd_ms * 1e3, 3),
+                                     "note": "an event on each side of every launch"},
             "table_build_us": round(table_ms * 1e3, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
