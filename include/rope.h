@@ -118,6 +118,37 @@ rope_status rope_apply_qk(void *q, void *k, const float *cos, const float *sin,
                           int32_t backward, int32_t dtype, int64_t table_rows, void *stream);
 
 /*
+ * rope_apply_qk_out -- rotate Q and K out of place (or in place), with
+ * optional per-sequence position indices.
+ *
+ * Same computation as rope_apply_qk, reading q and k and writing q_out and
+ * k_out.  An output may be exactly its input (that tensor is rotated in
+ * place); otherwise it must not overlap any input, the tables, pos_idx or
+ * the other output.  Out of place, the output receives every element: the
+ * rotated span, the tail [rotary_dim, D) copied unchanged, and the rows of
+ * unrotated tokens (position -1 or out of range) copied unchanged.
+ *
+ * Position indices (Unsloth page, Support for Custom Position IDs:
+ * prefix-tuning and context shifting; "rotary-embedding-torch", Input Tensor
+ * Shapes: indices into a padded frequency buffer):
+ *   pos_batch_stride = 0: pos_idx is int32[S], shared by every batch (as in
+ *     rope_apply_qk);
+ *   pos_batch_stride >= S: pos_idx is int32[B][pos_batch_stride] and token
+ *     (b, s) uses pos_idx[b * pos_batch_stride + s] -- one position vector per
+ *     sequence, e.g. sequences decoded at different offsets.
+ * Other strides return ROPE_ERR_INVALID_ARG.  Everything else (sizes, flags,
+ * errors, range flag) as for rope_apply_qk.  The bulk-copy kernel (variant 1)
+ * rotates in place only: forcing it with an out-of-place output returns
+ * ROPE_ERR_UNSUPPORTED.
+ */
+rope_status rope_apply_qk_out(const void *q, const void *k, void *q_out, void *k_out,
+                              const float *cos, const float *sin, const int32_t *pos_idx,
+                              int64_t pos_batch_stride, int64_t B, int32_t Hq, int32_t Hk,
+                              int64_t S, int32_t D, int32_t rotary_dim, int32_t layout,
+                              int32_t seq_before_head, int32_t backward, int32_t dtype,
+                              int64_t table_rows, void *stream);
+
+/*
  * rope_apply_q -- rotate one tensor in place (the query-only kernel of the
  * Unsloth page, Triton Kernel Architecture for RoPE).  Same rules as
  * rope_apply_qk with x in place of q, H in place of Hq, and no k.

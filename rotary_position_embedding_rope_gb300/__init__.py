@@ -8,8 +8,10 @@ torch stream (or raw handle, or None for torch's current stream) in place of
 ``void* stream``.  They only marshal arguments: every step runs in the CUDA
 library, and a missing library is an error, never a fallback.
 
-``build_tables``, ``apply_qk`` and ``apply_q`` are conveniences that read the
-sizes from tensor shapes and allocate the tables with torch.
+``build_tables``, ``apply_qk``, ``apply_q`` and ``rotate_qk`` are conveniences
+that read the sizes from tensor shapes and allocate tables and outputs with
+torch.  ``autograd.rotary_qk`` wraps the out-of-place call in a
+``torch.autograd.Function`` (backward = rotation by the negated angle).
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ __all__ = [
     "VARIANT_VECTOR", "rope_force_kernel_variant", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
-    "library_path", "load_library",
+    "library_path", "load_library", "rope_apply_qk_out", "rotate_qk",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
@@ -82,6 +84,10 @@ def load_library() -> ctypes.CDLL:
                                            c.c_int64, c.c_int32, c.c_int32, c.c_int32,
                                            c.c_int32, c.c_int32, c.c_int32, c.c_int64]
     lib.rope_qk_kernel_variant.restype = c.c_int32
+    lib.rope_apply_qk_out.argtypes = [P, P, P, P, P, P, P, c.c_int64, c.c_int64, c.c_int32,
+                                      c.c_int32, c.c_int64, c.c_int32, c.c_int32, c.c_int32,
+                                      c.c_int32, c.c_int32, c.c_int32, c.c_int64, P]
+    lib.rope_apply_qk_out.restype = c.c_int
     lib.rope_force_kernel_variant.argtypes = [c.c_int32]
     lib.rope_force_kernel_variant.restype = c.c_int
     _lib = lib
@@ -143,6 +149,19 @@ def rope_apply_qk(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim, layout,
                            int(rotary_dim), int(layout), int(seq_before_head), int(backward),
                            int(dtype), int(table_rows), _stream(stream))
     _check(st, "rope_apply_qk")
+
+
+def rope_apply_qk_out(q, k, q_out, k_out, cos, sin, pos_idx, pos_batch_stride, B, Hq, Hk, S, D,
+                      rotary_dim, layout, seq_before_head, backward, dtype, table_rows,
+                      stream=None):
+    lib = load_library()
+    st = lib.rope_apply_qk_out(_addr(q, "q"), _addr(k, "k"), _addr(q_out, "q_out"),
+                               _addr(k_out, "k_out"), _addr(cos, "cos"), _addr(sin, "sin"),
+                               _addr(pos_idx, "pos_idx"), int(pos_batch_stride), int(B), int(Hq),
+                               int(Hk), int(S), int(D), int(rotary_dim), int(layout),
+                               int(seq_before_head), int(backward), int(dtype), int(table_rows),
+                               _stream(stream))
+    _check(st, "rope_apply_qk_out")
 
 
 def rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rotary_dim, layout, seq_before_head,
@@ -251,3 +270,53 @@ def apply_q(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
     rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rd, _LAYOUT_CODE[layout],
                  int(seq_before_head), int(backward), _DTYPE_CODE[x.dtype], cos.shape[0], stream)
     return x
+
+
+def _positions(pos_idx, B: int, S: int):
+    """(tensor, batch stride) for an int32 [S] or [B, S'] (S' >= S) position tensor."""
+    if pos_idx is None:
+        return None, 0
+    if pos_idx.dtype != torch.int32:
+        raise ValueError("pos_idx must be int32")
+    if pos_idx.dim() == 1:
+        if pos_idx.numel() != S:
+            raise ValueError("pos_idx [S] must have S elements")
+        return pos_idx, 0
+    if pos_idx.dim() == 2 and pos_idx.shape[0] == B and pos_idx.shape[1] >= S:
+        return pos_idx, pos_idx.shape[1]
+    raise ValueError("pos_idx must be [S] or [B, >=S]")
+
+
+def rotate_qk(q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor, sin: torch.Tensor,
+              pos_idx: torch.Tensor | None = None, rotary_dim: int | None = None,
+              layout: str = "split_half", seq_before_head: bool = False, backward: bool = False,
+              q_out: torch.Tensor | None = None, k_out: torch.Tensor | None = None, stream=None):
+    """Out-of-place rotation: returns (q_out, k_out), allocated when not given.
+
+    pos_idx: int32 [S] (shared by all sequences) or [B, S] (one row per
+    sequence).  Passing q_out=q (k_out=k) rotates that tensor in place.
+    """
+    B, Hq, S, D = _shape4(q, seq_before_head)
+    Hk = 0
+    if k is not None:
+        Bk, Hk, Sk, Dk = _shape4(k, seq_before_head)
+        if (Bk, Sk, Dk) != (B, S, D) or k.dtype != q.dtype:
+            raise ValueError("q and k must agree in batch, sequence, head_dim and dtype")
+    if q.dtype not in _DTYPE_CODE:
+        raise TypeError("unsupported dtype %s" % q.dtype)
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or cos.shape != sin.shape:
+        raise ValueError("cos and sin must be float32 tables of the same shape")
+    rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+    if cos.shape[1] != rd // 2:
+        raise ValueError("table width %d does not match rotary_dim %d" % (cos.shape[1], rd))
+    pos, stride = _positions(pos_idx, B, S)
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    for o, x, n in ((q_out, q, "q_out"), (k_out, k, "k_out")):
+        if x is not None and (o.shape != x.shape or o.dtype != x.dtype):
+            raise ValueError("%s must match its input's shape and dtype" % n)
+    rope_apply_qk_out(q, k, q_out, k_out if k is not None else None, cos, sin, pos, stride, B, Hq,
+                      Hk, S, D, rd, _LAYOUT_CODE[layout], int(seq_before_head), int(backward),
+                      _DTYPE_CODE[q.dtype], cos.shape[0], stream)
+    return q_out, k_out

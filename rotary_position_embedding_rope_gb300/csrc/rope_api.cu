@@ -113,90 +113,129 @@ struct Plan {
     Variant variant;
 };
 
-static rope_status plan_apply(void *q, void *k, const float *cos, const float *sin,
-                              const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk, int64_t S,
-                              int32_t D, int32_t rotary_dim, int32_t layout,
-                              int32_t seq_before_head, int32_t backward, int32_t dtype,
-                              int64_t table_rows, Plan *plan)
+// All arguments of a rotation call (in place: q_out == q, k_out == k).
+struct CallArgs {
+    const void *q, *k;
+    void *q_out, *k_out;
+    const float *cos, *sin;
+    const int32_t *pos_idx;
+    int64_t pos_stride_b;
+    int64_t B;
+    int32_t Hq, Hk;
+    int64_t S;
+    int32_t D, rotary_dim, layout, seq_before_head, backward, dtype;
+    int64_t table_rows;
+};
+
+static rope_status plan_apply(const CallArgs &c, Plan *plan)
 {
     std::memset(plan, 0, sizeof *plan);
     plan->variant = kNone;
-    if (dtype != ROPE_F32 && dtype != ROPE_BF16 && dtype != ROPE_F16)
+    if (c.dtype != ROPE_F32 && c.dtype != ROPE_BF16 && c.dtype != ROPE_F16)
         return ROPE_ERR_UNSUPPORTED;
-    if (layout != ROPE_SPLIT_HALF && layout != ROPE_INTERLEAVED)
+    if (c.layout != ROPE_SPLIT_HALF && c.layout != ROPE_INTERLEAVED)
         return ROPE_ERR_UNSUPPORTED;
-    if ((seq_before_head != 0 && seq_before_head != 1) || (backward != 0 && backward != 1))
+    if ((c.seq_before_head != 0 && c.seq_before_head != 1) || (c.backward != 0 && c.backward != 1))
         return ROPE_ERR_INVALID_ARG;
-    if (B < 0 || S < 0 || Hq < 0 || Hk < 0 || D < 1 || table_rows < 0)
+    if (c.B < 0 || c.S < 0 || c.Hq < 0 || c.Hk < 0 || c.D < 1 || c.table_rows < 0)
         return ROPE_ERR_INVALID_ARG;
-    if (rotary_dim < 2 || (rotary_dim & 1) || rotary_dim > D)
+    if (c.rotary_dim < 2 || (c.rotary_dim & 1) || c.rotary_dim > c.D)
+        return ROPE_ERR_INVALID_ARG;
+    if (c.pos_stride_b != 0 && c.pos_stride_b < c.S)
         return ROPE_ERR_INVALID_ARG;
 
-    const int64_t elt = dtype == ROPE_F32 ? 4 : 2;
-    const int64_t h = rotary_dim / 2;
-    int64_t tok = 0, nq = 0, nk = 0, qbytes = 0, kbytes = 0, tab = 0, tabbytes = 0;
-    if (!mul_ok(B, S, &tok) || !mul_ok(tok, (int64_t)Hq * D, &nq) ||
-        !mul_ok(tok, (int64_t)Hk * D, &nk) || !mul_ok(nq, elt, &qbytes) ||
-        !mul_ok(nk, elt, &kbytes) || !mul_ok(table_rows, h, &tab) || !mul_ok(tab, 4, &tabbytes))
+    const int64_t elt = c.dtype == ROPE_F32 ? 4 : 2;
+    const int64_t h = c.rotary_dim / 2;
+    int64_t tok = 0, nq = 0, nk = 0, qbytes = 0, kbytes = 0, tab = 0, tabbytes = 0, posn = 0;
+    if (!mul_ok(c.B, c.S, &tok) || !mul_ok(tok, (int64_t)c.Hq * c.D, &nq) ||
+        !mul_ok(tok, (int64_t)c.Hk * c.D, &nk) || !mul_ok(nq, elt, &qbytes) ||
+        !mul_ok(nk, elt, &kbytes) || !mul_ok(c.table_rows, h, &tab) || !mul_ok(tab, 4, &tabbytes) ||
+        !mul_ok(c.B > 0 ? c.B - 1 : 0, c.pos_stride_b, &posn))
         return ROPE_ERR_INVALID_ARG;
-    if (tok == 0 || (int64_t)Hq + Hk == 0)
+    if (tok == 0 || (int64_t)c.Hq + c.Hk == 0)
         return ROPE_OK;                                  // empty: nothing to launch
 
-    if ((Hq > 0 && q == nullptr) || (Hk > 0 && k == nullptr) || cos == nullptr || sin == nullptr)
+    if ((c.Hq > 0 && (c.q == nullptr || c.q_out == nullptr)) ||
+        (c.Hk > 0 && (c.k == nullptr || c.k_out == nullptr)) || c.cos == nullptr || c.sin == nullptr)
         return ROPE_ERR_INVALID_ARG;
-    if (table_rows < 1 || (pos_idx == nullptr && S > table_rows))
+    if (c.table_rows < 1 || (c.pos_idx == nullptr && c.S > c.table_rows))
         return ROPE_ERR_INVALID_ARG;
-    if (ranges_overlap(q, qbytes, k, kbytes) || ranges_overlap(q, qbytes, cos, tabbytes) ||
-        ranges_overlap(q, qbytes, sin, tabbytes) || ranges_overlap(k, kbytes, cos, tabbytes) ||
-        ranges_overlap(k, kbytes, sin, tabbytes) || ranges_overlap(q, qbytes, pos_idx, S * 4) ||
-        ranges_overlap(k, kbytes, pos_idx, S * 4))
+    const int64_t posbytes = c.pos_idx ? (posn + c.S) * 4 : 0;
+    const void *q = c.Hq > 0 ? c.q : nullptr, *k = c.Hk > 0 ? c.k : nullptr;
+    const void *qo = c.Hq > 0 ? c.q_out : nullptr, *ko = c.Hk > 0 ? c.k_out : nullptr;
+    // every written range must be disjoint from every other range, except an
+    // output that is exactly its own input (in place)
+    const struct { const void *p; int64_t n; } ins[5] = {
+        {q, qbytes}, {k, kbytes}, {c.cos, tabbytes}, {c.sin, tabbytes}, {c.pos_idx, posbytes}};
+    const struct { const void *p; int64_t n; const void *self; } outs[2] = {
+        {qo, qbytes, q}, {ko, kbytes, k}};
+    for (int o = 0; o < 2; ++o) {
+        const bool in_place = outs[o].p == outs[o].self;
+        for (int i = 0; i < 5; ++i) {
+            if (in_place && ins[i].p == outs[o].self)
+                continue;                              // the tensor rotated in place
+            if (ranges_overlap(outs[o].p, outs[o].n, ins[i].p, ins[i].n))
+                return ROPE_ERR_INVALID_ARG;
+        }
+    }
+    if (ranges_overlap(qo, qbytes, ko, kbytes))
+        return ROPE_ERR_INVALID_ARG;
+    if (qo == q && ranges_overlap(q, qbytes, k, kbytes))
         return ROPE_ERR_INVALID_ARG;
 
     ApplyArgs &a = plan->args;
     int n = 0;
-    const int32_t heads[2] = {Hq, Hk};
-    void *bases[2] = {q, k};
+    const int32_t heads[2] = {c.Hq, c.Hk};
+    const void *bases[2] = {c.q, c.k};
+    void *outp[2] = {c.q_out, c.k_out};
     for (int t = 0; t < 2; ++t) {
         if (heads[t] == 0)
             continue;
-        TensorRef &r = a.t[n++];
-        r.base = bases[t];
+        TensorRef &r = a.t[n];
+        r.base = const_cast<void *>(bases[t]);
         r.heads = heads[t];
-        if (seq_before_head) {                      // [B, S, H, D]
-            r.stride_h = D;
-            r.stride_s = (int64_t)heads[t] * D;
-            r.stride_b = S * r.stride_s;
+        if (c.seq_before_head) {                    // [B, S, H, D]
+            r.stride_h = c.D;
+            r.stride_s = (int64_t)heads[t] * c.D;
+            r.stride_b = c.S * r.stride_s;
         } else {                                    // [B, H, S, D]
-            r.stride_s = D;
-            r.stride_h = S * D;
+            r.stride_s = c.D;
+            r.stride_h = c.S * c.D;
             r.stride_b = (int64_t)heads[t] * r.stride_h;
         }
+        a.out[n] = outp[t];
+        a.copy_through[n] = outp[t] != bases[t];
+        ++n;
     }
     a.ntensors = n;
-    a.cos = cos;
-    a.sin = sin;
-    a.pos_idx = pos_idx;
-    a.B = B;
-    a.S = S;
-    a.D = D;
-    a.rotary_dim = rotary_dim;
-    a.table_rows = table_rows;
-    a.backward = backward;
-    plan->layout = layout;
-    plan->dtype = dtype;
+    a.cos = c.cos;
+    a.sin = c.sin;
+    a.pos_idx = c.pos_idx;
+    a.pos_stride_b = c.pos_idx ? c.pos_stride_b : 0;
+    a.B = c.B;
+    a.S = c.S;
+    a.D = c.D;
+    a.rotary_dim = c.rotary_dim;
+    a.table_rows = c.table_rows;
+    a.backward = c.backward;
+    plan->layout = c.layout;
+    plan->dtype = c.dtype;
 
     // 16-byte vectors need: a rotary span of whole vector pairs, 16-byte
     // aligned rows, aligned base pointers and tables, and NJ within a CTA.
-    const int64_t span_bytes = rotary_dim * elt;
-    bool vec = (span_bytes % 32) == 0 && ((int64_t)D * elt) % 16 == 0 && aligned16(cos) &&
-               aligned16(sin) && span_bytes / 32 <= kMaxVectorsPerHalf;
-    for (int t = 0; t < n; ++t)
-        vec = vec && aligned16(a.t[t].base);
+    const int64_t span_bytes = c.rotary_dim * elt;
+    bool vec = (span_bytes % 32) == 0 && ((int64_t)c.D * elt) % 16 == 0 && aligned16(c.cos) &&
+               aligned16(c.sin) && span_bytes / 32 <= kMaxVectorsPerHalf;
+    bool copies = false;
+    for (int t = 0; t < n; ++t) {
+        vec = vec && aligned16(a.t[t].base) && aligned16(a.out[t]);
+        copies = copies || a.copy_through[t];
+    }
     const int32_t forced = g_forced_variant.load(std::memory_order_relaxed);
     if (forced == kScalar)
         plan->variant = kScalar;
     else if (forced == kBulk || forced == kVector) {
-        if (!vec)
+        if (!vec || (forced == kBulk && copies))       // the bulk kernel works in place only
             return ROPE_ERR_UNSUPPORTED;
         plan->variant = static_cast<Variant>(forced);
     } else
@@ -244,20 +283,26 @@ rope_status rope_tables_build(double theta, int32_t rotary_dim, int64_t max_pos,
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA;
 }
 
-rope_status rope_apply_qk(void *q, void *k, const float *cos, const float *sin,
-                          const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk, int64_t S,
-                          int32_t D, int32_t rotary_dim, int32_t layout, int32_t seq_before_head,
-                          int32_t backward, int32_t dtype, int64_t table_rows, void *stream)
+static rope_status apply_call(const CallArgs &c, void *stream)
 {
     Plan plan;
-    rope_status st = plan_apply(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim, layout,
-                                seq_before_head, backward, dtype, table_rows, &plan);
+    rope_status st = plan_apply(c, &plan);
     if (st != ROPE_OK || plan.variant == kNone)
         return st;
     int32_t *taken = nullptr;
     if (flag_addresses(&plan.args.range_flag, &taken) != cudaSuccess)
         return ROPE_ERR_CUDA;
     return launch_plan(plan, static_cast<cudaStream_t>(stream));
+}
+
+rope_status rope_apply_qk(void *q, void *k, const float *cos, const float *sin,
+                          const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk, int64_t S,
+                          int32_t D, int32_t rotary_dim, int32_t layout, int32_t seq_before_head,
+                          int32_t backward, int32_t dtype, int64_t table_rows, void *stream)
+{
+    const CallArgs c = {q, k, q, k, cos, sin, pos_idx, 0, B, Hq, Hk, S, D, rotary_dim, layout,
+                        seq_before_head, backward, dtype, table_rows};
+    return apply_call(c, stream);
 }
 
 rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int32_t *pos_idx,
@@ -269,17 +314,29 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
                          seq_before_head, backward, dtype, table_rows, stream);
 }
 
+rope_status rope_apply_qk_out(const void *q, const void *k, void *q_out, void *k_out,
+                              const float *cos, const float *sin, const int32_t *pos_idx,
+                              int64_t pos_batch_stride, int64_t B, int32_t Hq, int32_t Hk,
+                              int64_t S, int32_t D, int32_t rotary_dim, int32_t layout,
+                              int32_t seq_before_head, int32_t backward, int32_t dtype,
+                              int64_t table_rows, void *stream)
+{
+    const CallArgs c = {q, k, q_out, k_out, cos, sin, pos_idx, pos_batch_stride, B, Hq, Hk, S, D,
+                        rotary_dim, layout, seq_before_head, backward, dtype, table_rows};
+    return apply_call(c, stream);
+}
+
 int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, const float *sin,
                                const int32_t *pos_idx, int64_t B, int32_t Hq, int32_t Hk,
                                int64_t S, int32_t D, int32_t rotary_dim, int32_t layout,
                                int32_t seq_before_head, int32_t backward, int32_t dtype,
                                int64_t table_rows)
 {
+    const CallArgs c = {q, k, const_cast<void *>(q), const_cast<void *>(k), cos, sin, pos_idx, 0,
+                        B, Hq, Hk, S, D, rotary_dim, layout, seq_before_head, backward, dtype,
+                        table_rows};
     Plan plan;
-    rope_status st = plan_apply(const_cast<void *>(q), const_cast<void *>(k), cos, sin, pos_idx,
-                                B, Hq, Hk, S, D, rotary_dim, layout, seq_before_head, backward,
-                                dtype, table_rows, &plan);
-    return st == ROPE_OK ? (int32_t)plan.variant : 0;
+    return plan_apply(c, &plan) == ROPE_OK ? (int32_t)plan.variant : 0;
 }
 
 rope_status rope_check_errors(void *stream)

@@ -168,6 +168,7 @@ __device__ __forceinline__ void unit_next(const BulkPlan &bp, UnitIter &it)
 
 struct Unit {
     int32_t t;              // tensor: 0 = Q, 1 = K
+    int64_t b;              // batch
     int64_t s0;             // first token of the tile
     int32_t rows;           // rows in this tile (TS, or fewer at the end of a batch)
     const uint8_t *row0;    // address of the first row's rotary span
@@ -180,6 +181,7 @@ __device__ __forceinline__ Unit unit_of(const ApplyArgs &p, const BulkPlan &bp, 
     Unit x;
     x.t = it.head < p.t[0].heads ? 0 : 1;
     const int32_t hh = x.t ? it.head - p.t[0].heads : it.head;
+    x.b = it.b;
     x.s0 = it.tib * bp.ts;
     const int64_t left = p.S - x.s0;
     x.rows = static_cast<int32_t>(left < bp.ts ? left : bp.ts);
@@ -193,13 +195,13 @@ __device__ __forceinline__ Unit unit_of(const ApplyArgs &p, const BulkPlan &bp, 
     return x;
 }
 
-// Table row of token s: s itself, or pos_idx[s]; -1 when the row must not be
+// Table row of token (b, s): s itself, or its position index; -1 when the row must not be
 // touched (masked or out of range).  Out-of-range positions raise the flag.
-__device__ __forceinline__ int64_t token_row(const ApplyArgs &p, int64_t s, bool report)
+__device__ __forceinline__ int64_t token_row(const ApplyArgs &p, int64_t b, int64_t s, bool report)
 {
     if (p.pos_idx == nullptr)
         return s;
-    const int64_t r = __ldg(p.pos_idx + s);
+    const int64_t r = __ldg(p.pos_idx + b * p.pos_stride_b + s);
     if (r == -1)
         return -1;
     if (r < 0 || r >= p.table_rows) {
@@ -215,7 +217,7 @@ __device__ __forceinline__ uint32_t lane_rows_valid(const ApplyArgs &p, const Un
 {
     uint32_t m = 0;
     for (int r = lane, i = 0; r < x.rows; r += 32, ++i)
-        if (token_row(p, x.s0 + r, false) >= 0)
+        if (token_row(p, x.b, x.s0 + r, false) >= 0)
             m |= 1u << i;
     return m;
 }
@@ -323,7 +325,7 @@ rope_bulk_kernel(const ApplyArgs p, const BulkPlan bp)
         const uint32_t parity = static_cast<uint32_t>((k / kBulkStages) & 1);
         if (cons.tile != cur_tile) {                  // new tile: this token's cos/sin
             cur_tile = cons.tile;
-            my_row = y < x.rows ? token_row(p, x.s0 + y, j == 0) : -1;
+            my_row = y < x.rows ? token_row(p, x.b, x.s0 + y, j == 0) : -1;
             if (my_row >= 0) {
                 const float *crow = p.cos + my_row * h;
                 const float *srow = p.sin + my_row * h;

@@ -20,10 +20,13 @@ struct TensorRef {
 // Everything a rotation launch needs.  Passed by value as a kernel parameter.
 struct ApplyArgs {
     TensorRef t[2];            // Q then K; ntensors of them are valid
+    void *out[2];              // output base of each tensor (same strides); == t[i].base in place
     int32_t ntensors;
+    int32_t copy_through[2];   // 1: tensor written out of place (pass-through values are copied)
     const float *cos;          // [table_rows, rotary_dim/2]
     const float *sin;
-    const int32_t *pos_idx;    // [S] or nullptr
+    const int32_t *pos_idx;    // [S], [B, pos_stride_b] or nullptr
+    int64_t pos_stride_b;      // 0: one position vector shared by all batches
     int64_t B;
     int64_t S;
     int32_t D;
@@ -69,6 +72,11 @@ enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
 #define ROPE_VEC_PIPELINE 1
 #endif
 constexpr bool kVecPipeline = ROPE_VEC_PIPELINE != 0;
+// Cache hints of the register kernel's Q/K loads (see load_stream).
+#ifndef ROPE_VEC_LOAD_MODE
+#define ROPE_VEC_LOAD_MODE 2
+#endif
+constexpr int kVecLoadMode = ROPE_VEC_LOAD_MODE;
 constexpr int64_t kVecTargetThreads = ROPE_VEC_TARGET_THREADS;
 constexpr bool kPdl = ROPE_PDL != 0;
 constexpr int kVecThreads = ROPE_VEC_THREADS;

@@ -169,10 +169,37 @@ cudaError_t launch_hot(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Streaming 16-byte accesses of Q/K.  Every byte is read once and written
+// once, so nothing is kept in L1; kVecLoadMode picks the cache hints:
+//   0: ld/st.global.cs (evict-first streaming)
+//   1: ld.global.L1::no_allocate.L2::256B (fetch the whole 256-byte segment
+//      into L2, so the second-half load of a row hits L2) / st.global.cs
+//   2: ld.global.cs.L2::256B / st.global.cs
+__device__ __forceinline__ uint4 load_stream(const uint4 *p)
+{
+    if constexpr (kVecLoadMode == 1) {
+        uint4 v;
+        asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p));
+        return v;
+    } else if constexpr (kVecLoadMode == 2) {
+        uint4 v;
+        asm volatile("ld.global.cs.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p));
+        return v;
+    } else {
+        return __ldcs(p);
+    }
+}
+__device__ __forceinline__ void store_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
 // Rotate the rotary spans of heads [lo, hi) of one token, whose head 0 row
-// starts at row0 (heads stride_h elements apart).  U heads' loads are issued
-// before any arithmetic; with kVecPipeline the loads of the next U heads are
-// issued before the current ones are rotated, so two batches are in flight.
+// starts at in0 (read) and out0 (written; == in0 in place), heads stride_h
+// elements apart.  U heads' loads are issued before any arithmetic; with
+// kVecPipeline the loads of the next U heads are issued before the current
+// ones are rotated, so two batches are in flight.
 template <typename T, int LAYOUT>
 __device__ __forceinline__ void rotate_vectors(uint4 &va, uint4 &vb, const float *c,
                                                const float *sn)
@@ -197,8 +224,9 @@ __device__ __forceinline__ void rotate_vectors(uint4 &va, uint4 &vb, const float
 }
 
 template <typename T, int LAYOUT, int U>
-__device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t lo, int32_t hi,
-                                             int j, int NJ, const float *c, const float *sn)
+__device__ __forceinline__ void rotate_heads(const T *in0, T *out0, int64_t stride_h, int32_t lo,
+                                             int32_t hi, int j, int NJ, const float *c,
+                                             const float *sn)
 {
     if constexpr (!kVecPipeline) {
         for (int32_t h0 = lo; h0 < hi; h0 += U) {
@@ -206,18 +234,18 @@ __device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t 
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (h0 + u < hi) {
-                    const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
-                    va[u] = __ldcs(ptr + j);
-                    vb[u] = __ldcs(ptr + j + NJ);
+                    const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(h0 + u) * stride_h);
+                    va[u] = load_stream(ptr + j);
+                    vb[u] = load_stream(ptr + j + NJ);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (h0 + u < hi) {
                     rotate_vectors<T, LAYOUT>(va[u], vb[u], c, sn);
-                    uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
-                    __stcs(ptr + j, va[u]);
-                    __stcs(ptr + j + NJ, vb[u]);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(out0 + (int64_t)(h0 + u) * stride_h);
+                    store_stream(ptr + j, va[u]);
+                    store_stream(ptr + j + NJ, vb[u]);
                 }
             }
         }
@@ -226,9 +254,9 @@ __device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (lo + u < hi) {
-                const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(lo + u) * stride_h);
-                ca[u] = __ldcs(ptr + j);
-                cb[u] = __ldcs(ptr + j + NJ);
+                const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(lo + u) * stride_h);
+                ca[u] = load_stream(ptr + j);
+                cb[u] = load_stream(ptr + j + NJ);
             }
         }
         for (int32_t h0 = lo; h0 < hi; h0 += U) {
@@ -236,18 +264,18 @@ __device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t 
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (h1 + u < hi) {
-                    const uint4 *ptr = reinterpret_cast<const uint4 *>(row0 + (int64_t)(h1 + u) * stride_h);
-                    na[u] = __ldcs(ptr + j);
-                    nb[u] = __ldcs(ptr + j + NJ);
+                    const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(h1 + u) * stride_h);
+                    na[u] = load_stream(ptr + j);
+                    nb[u] = load_stream(ptr + j + NJ);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (h0 + u < hi) {
                     rotate_vectors<T, LAYOUT>(ca[u], cb[u], c, sn);
-                    uint4 *ptr = reinterpret_cast<uint4 *>(row0 + (int64_t)(h0 + u) * stride_h);
-                    __stcs(ptr + j, ca[u]);
-                    __stcs(ptr + j + NJ, cb[u]);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(out0 + (int64_t)(h0 + u) * stride_h);
+                    store_stream(ptr + j, ca[u]);
+                    store_stream(ptr + j + NJ, cb[u]);
                 }
             }
 #pragma unroll
@@ -256,6 +284,21 @@ __device__ __forceinline__ void rotate_heads(T *row0, int64_t stride_h, int32_t 
                 cb[u] = nb[u];
             }
         }
+    }
+}
+
+// Out of place only: copy 16-byte vectors [v0, v1) of head rows [lo, hi)
+// from in0 to out0 unchanged (the tail past rotary_dim, or whole rows of
+// tokens that are not rotated); the CTA row's NJ threads stride the vectors.
+template <typename T>
+__device__ __forceinline__ void copy_heads(const T *in0, T *out0, int64_t stride_h, int32_t lo,
+                                           int32_t hi, int j, int NJ, int32_t v0, int32_t v1)
+{
+    for (int32_t hd = lo; hd < hi; ++hd) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(in0 + (int64_t)hd * stride_h);
+        uint4 *dst = reinterpret_cast<uint4 *>(out0 + (int64_t)hd * stride_h);
+        for (int32_t v = v0 + j; v < v1; v += NJ)
+            store_stream(dst + v, load_stream(src + v));
     }
 }
 
@@ -301,17 +344,41 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
         const int64_t b = tok / p.S;
         const int64_t s = tok - b * p.S;
 
+        const int32_t hb = g * heads_per_group;
+        const int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
+
         // position of this token: table row, -1 = leave unrotated
         int64_t r = s;
+        bool rotate = true;
         if (p.pos_idx != nullptr) {
-            r = __ldg(p.pos_idx + s);
-            if (r == -1)
-                continue;
-            if (r < 0 || r >= p.table_rows) {
+            r = __ldg(p.pos_idx + b * p.pos_stride_b + s);
+            if (r != -1 && (r < 0 || r >= p.table_rows)) {
                 if (j == 0 && g == 0)
                     atomicOr(p.range_flag, 1);
-                continue;
+                rotate = false;
             }
+            rotate = rotate && r != -1;
+        }
+        if (!rotate) {
+            {                                         // out of place: pass whole rows through
+#pragma unroll
+                for (int ti = 0; ti < 2; ++ti) {
+                    if (ti >= p.ntensors)
+                        break;
+                    if (!p.copy_through[ti])
+                        continue;
+                    const TensorRef t = p.t[ti];
+                    const int32_t off = ti ? p.t[0].heads : 0;
+                    const int32_t lo = (hb > off ? hb : off) - off;
+                    const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
+                    const int64_t o = b * t.stride_b + s * t.stride_s;
+                    if (lo < hi)
+                        copy_heads<T>(static_cast<const T *>(t.base) + o,
+                                      static_cast<T *>(p.out[ti]) + o, t.stride_h, lo, hi, j, NJ,
+                                      0, (p.D * (int32_t)sizeof(T)) / 16);
+                }
+            }
+            continue;
         }
 
         // this thread's cos/sin values, kept in registers for the group's heads
@@ -349,8 +416,6 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
                 sn[e] = -sn[e];
         }
 
-        const int32_t hb = g * heads_per_group;
-        const int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
 #pragma unroll
         for (int ti = 0; ti < 2; ++ti) {
             if (ti >= p.ntensors)
@@ -361,43 +426,71 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
             const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
             if (lo >= hi)
                 continue;
-            T *row0 = static_cast<T *>(t.base) + b * t.stride_b + s * t.stride_s;
-            rotate_heads<T, LAYOUT, U>(row0, t.stride_h, lo, hi, j, NJ, c, sn);
+            const int64_t o = b * t.stride_b + s * t.stride_s;
+            const T *in0 = static_cast<const T *>(t.base) + o;
+            T *out0 = static_cast<T *>(p.out[ti]) + o;
+            rotate_heads<T, LAYOUT, U>(in0, out0, t.stride_h, lo, hi, j, NJ, c, sn);
+            if (p.copy_through[ti] && p.rotary_dim < p.D)  // pass the tail through
+                copy_heads<T>(in0, out0, t.stride_h, lo, hi, j, NJ,
+                              (p.rotary_dim * (int32_t)sizeof(T)) / 16,
+                              (p.D * (int32_t)sizeof(T)) / 16);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Element-wise kernel: one pair per loop iteration, any alignment and any
-// even rotary_dim.  Rows are enumerated tensor by tensor as (b, head, s),
-// s fastest; pairs within a row are consecutive indices.
+// Element-wise kernel: any alignment and any even rotary_dim.  Rows are
+// enumerated tensor by tensor as (b, head, s), s fastest; each row has
+// rotary_dim/2 pair units and, out of place, D - rotary_dim tail units
+// (copied).  One unit per loop iteration.
 // ---------------------------------------------------------------------------
 template <typename T, int LAYOUT>
-__global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t total_pairs)
+__global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t total_units,
+                                   int32_t units_per_row)
 {
     const int h = p.rotary_dim >> 1;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_pairs;
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_units;
          idx += stride) {
-        const int64_t i = idx % h;
-        int64_t row = idx / h;
+        const int64_t unit = idx % units_per_row;
+        int64_t row = idx / units_per_row;
         const int ti = row < rows0 ? 0 : 1;
         if (ti)
             row -= rows0;
-        const TensorRef t = p.t[ti];
+        const int32_t heads = ti ? p.t[1].heads : p.t[0].heads;
+        const int64_t sb = ti ? p.t[1].stride_b : p.t[0].stride_b;
+        const int64_t sh = ti ? p.t[1].stride_h : p.t[0].stride_h;
+        const int64_t ss = ti ? p.t[1].stride_s : p.t[0].stride_s;
         const int64_t s = row % p.S;
         row /= p.S;
-        const int64_t head = row % t.heads;
-        const int64_t b = row / t.heads;
+        const int64_t head = row % heads;
+        const int64_t b = row / heads;
+        const int64_t o = b * sb + head * sh + s * ss;
+        const T *x = static_cast<const T *>(ti ? p.t[1].base : p.t[0].base) + o;
+        T *y = static_cast<T *>(ti ? p.out[1] : p.out[0]) + o;
 
+        if (unit >= h) {                              // tail element, out of place only
+            if (!(ti ? p.copy_through[1] : p.copy_through[0]))
+                continue;
+            const int64_t d = p.rotary_dim + (unit - h);
+            y[d] = x[d];
+            continue;
+        }
+        const int64_t i = unit;
+        const int64_t i1 = LAYOUT == 0 ? i : 2 * i;
+        const int64_t i2 = LAYOUT == 0 ? i + h : 2 * i + 1;
         int64_t r = s;
         if (p.pos_idx != nullptr) {
-            r = __ldg(p.pos_idx + s);
-            if (r == -1)
-                continue;
-            if (r < 0 || r >= p.table_rows) {
-                if (i == 0)
+            r = __ldg(p.pos_idx + b * p.pos_stride_b + s);
+            if (r == -1 || r < 0 || r >= p.table_rows) {
+                if (r != -1 && i == 0)
                     atomicOr(p.range_flag, 1);
+                if (ti ? p.copy_through[1] : p.copy_through[0]) {   // pass the pair through
+                    y[i1] = x[i1];
+                    y[i2] = x[i2];
+                }
                 continue;
             }
         }
@@ -405,15 +498,11 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
         float sn = __ldg(p.sin + r * h + i);
         if (p.backward)
             sn = -sn;
-
-        T *x = static_cast<T *>(t.base) + b * t.stride_b + head * t.stride_h + s * t.stride_s;
-        const int64_t i1 = LAYOUT == 0 ? i : 2 * i;
-        const int64_t i2 = LAYOUT == 0 ? i + h : 2 * i + 1;
         float x1 = Elt<T>::to_f(x[i1]);
         float x2 = Elt<T>::to_f(x[i2]);
         rotate_pair(x1, x2, c, sn);
-        x[i1] = Elt<T>::from_f(x1);
-        x[i2] = Elt<T>::from_f(x2);
+        y[i1] = Elt<T>::from_f(x1);
+        y[i2] = Elt<T>::from_f(x2);
     }
 }
 
@@ -468,16 +557,16 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
     }
     const int64_t rows0 = a.B * a.S * a.t[0].heads;
     const int64_t rows1 = a.ntensors > 1 ? a.B * a.S * a.t[1].heads : 0;
-    const int64_t total = (rows0 + rows1) * (a.rotary_dim / 2);
+    const bool any_copy = a.copy_through[0] || (a.ntensors > 1 && a.copy_through[1]);
+    const int32_t units_per_row = a.rotary_dim / 2 + (any_copy ? a.D - a.rotary_dim : 0);
+    const int64_t total = (rows0 + rows1) * units_per_row;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
     if (blocks > 152LL * 64)
         blocks = 152LL * 64;                                   // grid-stride beyond this
-    if (layout == 0)
-        rope_scalar_kernel<T, 0><<<(unsigned)blocks, threads, 0, st>>>(a, rows0, total);
-    else
-        rope_scalar_kernel<T, 1><<<(unsigned)blocks, threads, 0, st>>>(a, rows0, total);
-    return cudaGetLastError();
+    auto kernel = layout == 0 ? rope_scalar_kernel<T, 0> : rope_scalar_kernel<T, 1>;
+    return launch_hot(kernel, dim3((unsigned)blocks), dim3(threads), 0, st, a, rows0, total,
+                      units_per_row);
 }
 
 }  // namespace rope

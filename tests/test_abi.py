@@ -167,3 +167,41 @@ def test_force_kernel_variant_rules(lib):
     finally:
         lib.rope_force_kernel_variant(0)
     assert R.rope_status_string(R.ROPE_ERR_KERNEL_TIMEOUT) == "ROPE_ERR_KERNEL_TIMEOUT"
+
+
+def out_args(**over):
+    a = dict(q=A16 * 1, k=A16 * 1000, qo=A16 * 5000, ko=A16 * 6000, cos=A16 * 2000, sin=A16 * 3000,
+             pos=None, stride=0, B=2, Hq=4, Hk=2, S=16, D=64, rd=64, layout=0, sbh=0, bwd=0,
+             dtype=1, rows=16)
+    a.update(over)
+    return (a["q"], a["k"], a["qo"], a["ko"], a["cos"], a["sin"], a["pos"], a["stride"], a["B"],
+            a["Hq"], a["Hk"], a["S"], a["D"], a["rd"], a["layout"], a["sbh"], a["bwd"], a["dtype"],
+            a["rows"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(pos=A16 * 4000, stride=5), R.ROPE_ERR_INVALID_ARG),       # 0 < stride < S
+    (dict(pos=A16 * 4000, stride=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(qo=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(ko=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(qo=A16 * 1 + 64), R.ROPE_ERR_INVALID_ARG),                 # q_out overlaps q, not equal
+    (dict(qo=A16 * 1000), R.ROPE_ERR_INVALID_ARG),                   # q_out over k
+    (dict(ko=A16 * 5000 + 32), R.ROPE_ERR_INVALID_ARG),              # outputs overlap
+    (dict(qo=A16 * 2000), R.ROPE_ERR_INVALID_ARG),                   # output over the table
+    (dict(pos=A16 * 4000, stride=16, qo=A16 * 4000), R.ROPE_ERR_INVALID_ARG),  # output over positions
+    (dict(dtype=9), R.ROPE_ERR_UNSUPPORTED),
+])
+def test_apply_out_rejects_bad_arguments(lib, over, status):
+    assert lib.rope_apply_qk_out(*out_args(**over)) == status
+
+
+def test_bulk_kernel_refuses_out_of_place(lib):
+    try:
+        lib.rope_force_kernel_variant(1)
+        assert lib.rope_apply_qk_out(*out_args()) == R.ROPE_ERR_UNSUPPORTED
+    finally:
+        lib.rope_force_kernel_variant(0)
+
+
+def test_apply_out_empty_is_noop(lib):
+    assert lib.rope_apply_qk_out(*out_args(B=0, qo=None, ko=None)) == R.ROPE_OK

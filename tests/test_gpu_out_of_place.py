@@ -1,0 +1,139 @@
+"""Out-of-place rotation, per-sequence position indices and the autograd
+binding, through the C ABI, against in-place calls and the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_util import (assert_matches, gpu_bits, lib, oracle_apply, oracle_tables, pos_tensor,
+                      require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def case(B, Hq, Hk, S, D, rd, dtype, layout="split_half", sbh=False, rows=None, seed=11):
+    return W.Workload("oop", B, Hq, Hk, S, D, rd, 1e4, dtype, layout, sbh,
+                      rows if rows is not None else S, "none", seed)
+
+
+@pytest.fixture
+def restore_variant():
+    yield
+    lib().rope_force_kernel_variant(0)
+
+
+def _oracle_per_sequence(w, x, H, pos2d, backward, c32, s32):
+    """Oracle on each sequence b with its own position row (pos2d[b, :S])."""
+    xb = W.bits(x)
+    sa = 1 if w.seq_before_head else 2
+    ys, y64s = [], []
+    for b in range(w.B):
+        one = w.with_sizes(B=1)
+        xs = np.ascontiguousarray(xb[b:b + 1])
+        yb, y64 = oracle_apply(one, xs, H, None if pos2d is None else pos2d[b, :w.S], backward,
+                               c32, s32)
+        ys.append(yb)
+        y64s.append(y64)
+    return np.concatenate(ys), np.concatenate(y64s)
+
+
+@pytest.mark.parametrize("variant", [3, 2])
+@pytest.mark.parametrize("cfg", [
+    dict(B=2, Hq=6, Hk=2, S=40, D=128, rd=128, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=3, Hq=4, Hk=4, S=25, D=64, rd=32, dtype="f16", layout="interleaved", sbh=True),
+    dict(B=2, Hq=3, Hk=1, S=19, D=96, rd=64, dtype="f32", layout="split_half", sbh=False),
+])
+def test_out_of_place_matches_in_place_and_passes_through(cfg, variant, restore_variant):
+    require_gpu()
+    R = lib()
+    R.rope_force_kernel_variant(variant)
+    rows = cfg["S"] + 4
+    w = case(cfg["B"], cfg["Hq"], cfg["Hk"], cfg["S"], cfg["D"], cfg["rd"], cfg["dtype"],
+             cfg["layout"], cfg["sbh"], rows=rows)
+    q, k, _ = W.make_inputs(w)
+    c32, s32 = oracle_tables(w.theta, w.rotary_dim, w.table_rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    pos = (np.arange(w.S, dtype=np.int32) + 2) % rows
+    pos[0] = -1
+    pos[3] = rows + 7                                  # out of range: unrotated, flagged
+    pg = pos_tensor(pos)
+    for backward in (False, True):
+        qi, ki = q.cuda(), k.cuda()
+        qin, kin = q.cuda(), k.cuda()
+        qo, ko = torch.full_like(qin, 7.0), torch.full_like(kin, 7.0)
+        R.rope_apply_qk(qi, ki, cg, sg, pg, w.B, w.Hq, w.Hk, w.S, w.D, w.rotary_dim,
+                        W.LAYOUTS[w.layout], int(w.seq_before_head), int(backward),
+                        W.DTYPES[w.dtype], rows)
+        R.rope_apply_qk_out(qin, kin, qo, ko, cg, sg, pg, 0, w.B, w.Hq, w.Hk, w.S, w.D,
+                            w.rotary_dim, W.LAYOUTS[w.layout], int(w.seq_before_head),
+                            int(backward), W.DTYPES[w.dtype], rows)
+        assert R.rope_check_errors() == R.ROPE_ERR_POS_OUT_OF_RANGE
+        # out of place gives every element of the in-place result; inputs untouched
+        assert np.array_equal(gpu_bits(qo), gpu_bits(qi)) and np.array_equal(gpu_bits(ko), gpu_bits(ki))
+        assert np.array_equal(gpu_bits(qin), W.bits(q)) and np.array_equal(gpu_bits(kin), W.bits(k))
+
+
+@pytest.mark.parametrize("stride_pad", [0, 5])
+@pytest.mark.parametrize("cfg", [
+    dict(B=4, Hq=8, Hk=2, S=33, D=128, rd=128, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=3, Hq=4, Hk=4, S=17, D=64, rd=64, dtype="f16", layout="interleaved", sbh=True),
+    dict(B=64, Hq=32, Hk=8, S=1, D=128, rd=128, dtype="bf16", layout="split_half", sbh=False),  # decode
+])
+def test_per_sequence_positions_against_oracle(cfg, stride_pad):
+    require_gpu()
+    R = lib()
+    rows = 4096
+    w = case(cfg["B"], cfg["Hq"], cfg["Hk"], cfg["S"], cfg["D"], cfg["rd"], cfg["dtype"],
+             cfg["layout"], cfg["sbh"], rows=rows)
+    q, k, _ = W.make_inputs(w)
+    c32, s32 = oracle_tables(w.theta, w.rotary_dim, rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    g = np.random.default_rng(w.B * 100 + w.S)
+    stride = w.S + stride_pad
+    pos2d = np.full((w.B, stride), -5, dtype=np.int32)     # padding never read
+    starts = g.integers(0, rows - w.S, w.B)
+    pos2d[:, :w.S] = starts[:, None] + np.arange(w.S)[None, :]   # context shifted per sequence
+    if w.S > 2:
+        pos2d[0, 1] = -1
+    qo, ko = R.rotate_qk(q.cuda(), k.cuda(), cg, sg, pos_idx=torch.from_numpy(pos2d).cuda(),
+                         layout=w.layout, seq_before_head=w.seq_before_head)
+    assert R.rope_check_errors() == R.ROPE_OK
+    for x, got, H in ((q, qo, w.Hq), (k, ko, w.Hk)):
+        yb, y64 = _oracle_per_sequence(w, x, H, pos2d, False, c32, s32)
+        assert_matches(w.dtype, gpu_bits(got), yb, y64)
+    # in place through the same entry point (q_out = q)
+    qi, ki = q.cuda(), k.cuda()
+    R.rotate_qk(qi, ki, cg, sg, pos_idx=torch.from_numpy(pos2d).cuda(), layout=w.layout,
+                seq_before_head=w.seq_before_head, q_out=qi, k_out=ki)
+    assert torch.equal(qi, qo) and torch.equal(ki, ko)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_autograd_forward_and_backward(dtype):
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.autograd import rotary_qk
+
+    w = case(2, 4, 2, 48, 64, 64, dtype, rows=64)
+    q, k, _ = W.make_inputs(w)
+    gq, gk, _ = W.make_inputs(w, seed_offset=50)            # upstream gradients
+    c32, s32 = oracle_tables(w.theta, w.rotary_dim, w.table_rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    qg = q.cuda().requires_grad_(True)
+    kg = k.cuda().requires_grad_(True)
+    qr, kr = rotary_qk(qg, kg, cg, sg)
+    fq, fk = R.rotate_qk(q.cuda(), k.cuda(), cg, sg)
+    assert torch.equal(qr.detach(), fq) and torch.equal(kr.detach(), fk)
+    ((qr * gq.cuda()).sum() + (kr * gk.cuda()).sum()).backward()
+    # d/dx of sum(G * R(t) x) is R(-t) G: the oracle's backward rotation of G
+    for g_in, grad, H in ((gq, qg.grad, w.Hq), (gk, kg.grad, w.Hk)):
+        yb, y64 = oracle_apply(w, W.bits(g_in), H, None, True, c32, s32)
+        assert_matches(dtype, gpu_bits(grad), yb, y64)
+    # a loss that uses only q leaves k's gradient None-free and zero
+    qg2 = q.cuda().requires_grad_(True)
+    kg2 = k.cuda().requires_grad_(True)
+    qr2, _ = rotary_qk(qg2, kg2, cg, sg)
+    (qr2 * gq.cuda()).sum().backward()
+    assert kg2.grad is None or torch.count_nonzero(kg2.grad) == 0
+    yb, y64 = oracle_apply(w, W.bits(gq), w.Hq, None, True, c32, s32)
+    assert_matches(dtype, gpu_bits(qg2.grad), yb, y64)
