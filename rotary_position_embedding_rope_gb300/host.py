@@ -1,0 +1,93 @@
+"""Rotation of Q and K that live in pinned host memory.
+
+The tensors are split along the batch dimension into chunks.  Chunk i is
+copied host->device on one stream, rotated by the CUDA library on a second
+and copied device->host on a third, so the copies in both directions and the
+kernels of neighbouring chunks overlap.  Device staging buffers (two chunks
+per tensor) are allocated once per shape and reused.  Only argument
+marshalling and stream ordering happen here; the rotation is one library call
+per chunk.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _DTYPE_CODE, _LAYOUT_CODE, _shape4, rope_apply_qk_out
+
+
+class HostRotator:
+    def __init__(self, device=None, chunks: int = 4):
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.chunks = chunks
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_run = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
+        self._staging = {}
+        self._free = [None, None]          # event: staging slot's device->host copy done
+
+    def _slots(self, shape_q, shape_k, dtype, rows_q, rows_k):
+        key = (shape_q, shape_k, dtype)
+        if key not in self._staging:
+            self._staging = {key: [(torch.empty((rows_q,) + tuple(shape_q[1:]), dtype=dtype,
+                                                device=self.device),
+                                    None if shape_k is None else
+                                    torch.empty((rows_k,) + tuple(shape_k[1:]), dtype=dtype,
+                                                device=self.device))
+                                   for _ in range(2)]}
+            self._free = [None, None]
+        return self._staging[key]
+
+    def apply_qk(self, q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor,
+                 sin: torch.Tensor, q_out: torch.Tensor, k_out: torch.Tensor | None,
+                 pos_idx: torch.Tensor | None = None, rotary_dim: int | None = None,
+                 layout: str = "split_half", seq_before_head: bool = False,
+                 backward: bool = False, after: torch.cuda.Event | None = None):
+        """Rotate pinned host tensors q, k into pinned host tensors q_out, k_out.
+
+        cos, sin and pos_idx ([S] int32) are device tensors.  Work is ordered
+        after the event `after` (if given).  Returns the event recorded when
+        the last device->host copy is done.
+        """
+        B, Hq, S, D = _shape4(q, seq_before_head)
+        Hk = 0 if k is None else _shape4(k, seq_before_head)[1]
+        for t in (q, k, q_out, k_out):
+            if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
+                raise ValueError("host tensors must be contiguous pinned CPU memory")
+        rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+        n = max(1, min(self.chunks, B))
+        per = (B + n - 1) // n
+        slots = self._slots(q.shape, None if k is None else k.shape, q.dtype, per, per)
+        for s in (self.s_in, self.s_run, self.s_out):
+            if after is not None:
+                s.wait_event(after)
+        done = None
+        for c in range(n):
+            b0, b1 = c * per, min(B, (c + 1) * per)
+            if b0 >= b1:
+                break
+            slot = c % 2
+            dq, dk = slots[slot]
+            dq, dk = dq[: b1 - b0], None if dk is None else dk[: b1 - b0]
+            if self._free[slot] is not None:
+                self.s_in.wait_event(self._free[slot])
+            with torch.cuda.stream(self.s_in):
+                dq.copy_(q[b0:b1], non_blocking=True)
+                if k is not None:
+                    dk.copy_(k[b0:b1], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(self.s_in)
+            self.s_run.wait_event(ready)
+            rope_apply_qk_out(dq, dk, dq, dk, cos, sin, pos_idx, 0, b1 - b0, Hq, Hk, S, D, rd,
+                              _LAYOUT_CODE[layout], int(seq_before_head), int(backward),
+                              _DTYPE_CODE[q.dtype], cos.shape[0], self.s_run)
+            rotated = torch.cuda.Event()
+            rotated.record(self.s_run)
+            self.s_out.wait_event(rotated)
+            with torch.cuda.stream(self.s_out):
+                q_out[b0:b1].copy_(dq, non_blocking=True)
+                if k is not None:
+                    k_out[b0:b1].copy_(dk, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(self.s_out)
+            self._free[slot] = done
+        return done

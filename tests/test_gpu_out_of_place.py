@@ -137,3 +137,26 @@ def test_autograd_forward_and_backward(dtype):
     assert kg2.grad is None or torch.count_nonzero(kg2.grad) == 0
     yb, y64 = oracle_apply(w, W.bits(gq), w.Hq, None, True, c32, s32)
     assert_matches(dtype, gpu_bits(qg2.grad), yb, y64)
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 4])
+def test_host_pipeline_matches_device_call(chunks):
+    """Pinned host tensors rotated through the chunked copy/rotate/copy pipeline
+    give the same bits as the device call."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostRotator
+
+    w = case(5, 4, 2, 64, 128, 128, "bf16", rows=64)
+    q, k, _ = W.make_inputs(w)
+    cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+    rot = HostRotator(chunks=chunks)
+    hq, hk = q.pin_memory(), k.pin_memory()
+    oq, ok_ = torch.empty_like(q).pin_memory(), torch.empty_like(k).pin_memory()
+    for backward in (False, True):
+        done = rot.apply_qk(hq, hk, cos, sin, oq, ok_, backward=backward)
+        done.synchronize()
+        dq, dk = q.cuda(), k.cuda()
+        R.apply_qk(dq, dk, cos, sin, backward=backward)
+        assert torch.equal(oq, dq.cpu()) and torch.equal(ok_, dk.cpu())
+        assert torch.equal(hq, q) and torch.equal(hk, k)
