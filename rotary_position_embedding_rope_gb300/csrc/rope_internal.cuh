@@ -36,9 +36,10 @@ struct ApplyArgs {
     int32_t *range_flag;       // device word set when a position is out of range
 };
 
-// Kernel variants: kBulk stages rows through shared memory with bulk copies
-// (the default for aligned shapes), kVector moves 16-byte vectors through
-// registers, kScalar handles any shape one pair at a time.
+// Kernel variants: kVector moves 16-byte vectors through registers (the
+// automatic choice for aligned shapes), kBulk stages rows through shared
+// memory with bulk copies (in place only, chosen only when forced), kScalar
+// handles any shape one pair at a time.
 enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
 
 // Threads per CTA of the vectorised kernel and heads in flight per thread.
@@ -52,15 +53,10 @@ enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
 #ifndef ROPE_VEC_MIN_BLOCKS
 #define ROPE_VEC_MIN_BLOCKS 4
 #endif
-// 0: one token per thread row (grid = ceil(B*S / tokens per CTA));
-// 1: persistent grid of SMs x resident CTAs, each with a balanced token range.
-#ifndef ROPE_VEC_PERSISTENT
-#define ROPE_VEC_PERSISTENT 0
-#endif
 // Threads the register kernel aims to run at once; below that, a token's
 // heads are split into groups handled by separate thread rows.
 #ifndef ROPE_VEC_TARGET_THREADS
-#define ROPE_VEC_TARGET_THREADS (152 * 32)
+#define ROPE_VEC_TARGET_THREADS (152 * 128)
 #endif
 // Launch the hot kernels with programmatic dependent launch.
 #ifndef ROPE_PDL
@@ -82,7 +78,6 @@ constexpr bool kPdl = ROPE_PDL != 0;
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
 constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;
-constexpr bool kVecPersistent = ROPE_VEC_PERSISTENT != 0;
 // NJ (16-byte vectors per half span) must fit in one CTA row: the register
 // and bulk kernels take rotary spans of up to 32 * kVecThreads bytes.
 constexpr int kMaxVectorsPerHalf = kVecThreads;

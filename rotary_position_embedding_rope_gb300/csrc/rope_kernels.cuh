@@ -175,8 +175,13 @@ cudaError_t launch_hot(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 //   1: ld.global.L1::no_allocate.L2::256B (fetch the whole 256-byte segment
 //      into L2, so the second-half load of a row hits L2) / st.global.cs
 //   2: ld.global.cs.L2::256B / st.global.cs
-__device__ __forceinline__ uint4 load_stream(const uint4 *p)
+// The 256-byte fetch is used only when `whole` says the rotary spans tile
+// whole 256-byte segments; otherwise it would pull in bytes (the tail past
+// rotary_dim, neighbouring rows) the kernel never touches.
+__device__ __forceinline__ uint4 load_stream(const uint4 *p, bool whole = false)
 {
+    if (!whole)
+        return __ldcs(p);
     if constexpr (kVecLoadMode == 1) {
         uint4 v;
         asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -226,7 +231,7 @@ __device__ __forceinline__ void rotate_vectors(uint4 &va, uint4 &vb, const float
 template <typename T, int LAYOUT, int U>
 __device__ __forceinline__ void rotate_heads(const T *in0, T *out0, int64_t stride_h, int32_t lo,
                                              int32_t hi, int j, int NJ, const float *c,
-                                             const float *sn)
+                                             const float *sn, bool whole)
 {
     if constexpr (!kVecPipeline) {
         for (int32_t h0 = lo; h0 < hi; h0 += U) {
@@ -235,8 +240,8 @@ __device__ __forceinline__ void rotate_heads(const T *in0, T *out0, int64_t stri
             for (int u = 0; u < U; ++u) {
                 if (h0 + u < hi) {
                     const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(h0 + u) * stride_h);
-                    va[u] = load_stream(ptr + j);
-                    vb[u] = load_stream(ptr + j + NJ);
+                    va[u] = load_stream(ptr + j, whole);
+                    vb[u] = load_stream(ptr + j + NJ, whole);
                 }
             }
 #pragma unroll
@@ -255,8 +260,8 @@ __device__ __forceinline__ void rotate_heads(const T *in0, T *out0, int64_t stri
         for (int u = 0; u < U; ++u) {
             if (lo + u < hi) {
                 const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(lo + u) * stride_h);
-                ca[u] = load_stream(ptr + j);
-                cb[u] = load_stream(ptr + j + NJ);
+                ca[u] = load_stream(ptr + j, whole);
+                cb[u] = load_stream(ptr + j + NJ, whole);
             }
         }
         for (int32_t h0 = lo; h0 < hi; h0 += U) {
@@ -265,8 +270,8 @@ __device__ __forceinline__ void rotate_heads(const T *in0, T *out0, int64_t stri
             for (int u = 0; u < U; ++u) {
                 if (h1 + u < hi) {
                     const uint4 *ptr = reinterpret_cast<const uint4 *>(in0 + (int64_t)(h1 + u) * stride_h);
-                    na[u] = load_stream(ptr + j);
-                    nb[u] = load_stream(ptr + j + NJ);
+                    na[u] = load_stream(ptr + j, whole);
+                    nb[u] = load_stream(ptr + j + NJ, whole);
                 }
             }
 #pragma unroll
@@ -319,7 +324,8 @@ __device__ __forceinline__ void copy_heads(const T *in0, T *out0, int64_t stride
 // ---------------------------------------------------------------------------
 template <typename T, int LAYOUT, int U>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
-rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t heads_per_group)
+rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t heads_per_group,
+                int32_t TT)
 {
     constexpr int V = Elt<T>::V;
     const int NJ = blockDim.x;
@@ -327,7 +333,10 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
     const int32_t P = p.t[0].heads + (p.ntensors > 1 ? p.t[1].heads : 0);
+    // rotary spans that are whole rows of a multiple of 256 bytes
+    const bool whole = p.rotary_dim == p.D && (p.D * (int32_t)sizeof(T)) % 256 == 0;
 
+    const int64_t total_tokens = p.B * p.S;
     const int64_t G = gridDim.x;
     const int64_t c = blockIdx.x;
     const int64_t share = total_items / G;
@@ -339,8 +348,19 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
     pdl_trigger();
 
     for (int64_t item = i0 + threadIdx.y; item < i1; item += TS) {
-        const int64_t tok = groups == 1 ? item : item / groups;
-        const int32_t g = static_cast<int32_t>(item - tok * groups);
+        // items run (tile of TT tokens, group, token in tile), so the rows of a
+        // warp hold consecutive tokens of one head group
+        int64_t tok = item;
+        int32_t g = 0;
+        if (groups > 1) {
+            const int64_t per_tile = (int64_t)groups * TT;
+            const int64_t tile = item / per_tile;
+            const int64_t rem = item - tile * per_tile;
+            g = static_cast<int32_t>(rem / TT);
+            tok = tile * TT + (rem - (int64_t)g * TT);
+        }
+        if (tok >= total_tokens)
+            continue;
         const int64_t b = tok / p.S;
         const int64_t s = tok - b * p.S;
 
@@ -429,7 +449,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
             const int64_t o = b * t.stride_b + s * t.stride_s;
             const T *in0 = static_cast<const T *>(t.base) + o;
             T *out0 = static_cast<T *>(p.out[ti]) + o;
-            rotate_heads<T, LAYOUT, U>(in0, out0, t.stride_h, lo, hi, j, NJ, c, sn);
+            rotate_heads<T, LAYOUT, U>(in0, out0, t.stride_h, lo, hi, j, NJ, c, sn, whole);
             if (p.copy_through[ti] && p.rotary_dim < p.D)  // pass the tail through
                 copy_heads<T>(in0, out0, t.stride_h, lo, hi, j, NJ,
                               (p.rotary_dim * (int32_t)sizeof(T)) / 16,
@@ -509,20 +529,6 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
 // ---------------------------------------------------------------------------
 // Host-side launcher for one element type.
 // ---------------------------------------------------------------------------
-// CTAs of `kernel` (with `threads` threads, no dynamic shared memory) that
-// the current device holds at once: SM count x resident CTAs per SM.
-inline cudaError_t resident_grid(const void *kernel, int threads, int *out)
-{
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
-    *out = sms * (per_sm > 0 ? per_sm : 1);
-    return e;
-}
-
 template <typename T>
 cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st)
 {
@@ -539,21 +545,17 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         const int32_t max_groups = (P + kVecUnroll - 1) / kVecUnroll;
         const int32_t groups = (int32_t)(want < 1 ? 1 : (want > max_groups ? max_groups : want));
         const int32_t hpg = (P + groups - 1) / groups;
-        const int64_t items = a.B * a.S * groups;
+        // tokens per warp row group: a warp covers TT consecutive tokens
+        const int32_t TT = NJ >= 32 ? 1 : 32 / NJ;
+        const int64_t tiles = (a.B * a.S + TT - 1) / TT;
+        const int64_t items = groups == 1 ? a.B * a.S : tiles * TT * groups;
         int64_t grid = (items + TS - 1) / TS;                  // one item per thread row
         if (grid > 0x7fffffffLL)
             grid = 0x7fffffffLL;
         auto kernel = layout == 0 ? rope_vec_kernel<T, 0, kVecUnroll>
                                   : rope_vec_kernel<T, 1, kVecUnroll>;
-        if (kVecPersistent) {
-            int resident = 0;
-            cudaError_t e = resident_grid(reinterpret_cast<const void *>(kernel), NJ * TS, &resident);
-            if (e != cudaSuccess)
-                return e;
-            if (grid > resident)
-                grid = resident;
-        }
-        return launch_hot(kernel, dim3((unsigned)grid), dim3(NJ, TS), 0, st, a, items, groups, hpg);
+        return launch_hot(kernel, dim3((unsigned)grid), dim3(NJ, TS), 0, st, a, items, groups, hpg,
+                          TT);
     }
     const int64_t rows0 = a.B * a.S * a.t[0].heads;
     const int64_t rows1 = a.ntensors > 1 ? a.B * a.S * a.t[1].heads : 0;
