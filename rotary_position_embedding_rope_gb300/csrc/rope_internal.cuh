@@ -75,6 +75,12 @@ constexpr bool kVecPipeline = ROPE_VEC_PIPELINE != 0;
 constexpr int kVecLoadMode = ROPE_VEC_LOAD_MODE;
 constexpr int64_t kVecTargetThreads = ROPE_VEC_TARGET_THREADS;
 constexpr bool kPdl = ROPE_PDL != 0;
+// Head rows of its first item each thread row prefetches into L2 before
+// waiting for the previous grid (0: none; default: the first batch of heads).
+#ifndef ROPE_VEC_PREFETCH_HEADS
+#define ROPE_VEC_PREFETCH_HEADS ROPE_VEC_UNROLL
+#endif
+constexpr int kVecPrefetchHeads = ROPE_VEC_PREFETCH_HEADS;
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
 constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;

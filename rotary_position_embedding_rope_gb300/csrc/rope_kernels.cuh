@@ -344,6 +344,49 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
     const int64_t i0 = c * share + (c < extra ? c : extra);
     const int64_t i1 = i0 + share + (c < extra ? 1 : 0);
 
+    if constexpr (kVecPrefetchHeads > 0) {
+        // Before waiting for the previous grid: pull this row's first item's
+        // head rows into L2.  A prefetch only fills L2, the coherence point
+        // that the previous grid's writes also reach, so it cannot make a
+        // later load see stale data; it overlaps DRAM latency with the
+        // previous launch's tail.
+        const int64_t item = i0 + threadIdx.y;
+        if (item < i1) {
+            int64_t tok = item;
+            int32_t g = 0;
+            if (groups > 1) {
+                const int64_t per_tile = (int64_t)groups * TT;
+                const int64_t tile = item / per_tile;
+                const int64_t rem = item - tile * per_tile;
+                g = static_cast<int32_t>(rem / TT);
+                tok = tile * TT + (rem - (int64_t)g * TT);
+            }
+            if (tok < total_tokens) {
+                const int64_t b = tok / p.S;
+                const int64_t s = tok - b * p.S;
+                const int32_t hb = g * heads_per_group;
+                int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
+                if (he > hb + kVecPrefetchHeads)
+                    he = hb + kVecPrefetchHeads;
+#pragma unroll
+                for (int ti = 0; ti < 2; ++ti) {
+                    if (ti >= p.ntensors)
+                        break;
+                    const TensorRef t = p.t[ti];
+                    const int32_t off = ti ? p.t[0].heads : 0;
+                    const int32_t lo = (hb > off ? hb : off) - off;
+                    const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
+                    const T *in0 = static_cast<const T *>(t.base) + b * t.stride_b + s * t.stride_s;
+                    for (int32_t hd = lo; hd < hi; ++hd) {
+                        const uint4 *row = reinterpret_cast<const uint4 *>(in0 + (int64_t)hd * t.stride_h);
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j + NJ));
+                    }
+                }
+            }
+        }
+    }
+
     pdl_wait();
     pdl_trigger();
 
