@@ -363,3 +363,38 @@ def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
         assert_matches(w.dtype, np.ascontiguousarray(np.take(got, idx, axis=sa)), yb, y64)
         bad = np.flatnonzero(~good)
         assert np.array_equal(np.take(got, bad, axis=sa), np.take(W.bits(x), bad, axis=sa))
+
+
+def test_calls_replay_in_a_cuda_graph():
+    """Forward/backward calls captured in a CUDA graph (programmatic launches
+    become graph edges) and replayed give the eager results."""
+    require_gpu()
+    R = lib()
+    w = case(2, 8, 2, 96, 128, 128, "bf16")
+    q, k, _ = W.make_inputs(w)
+    dq, dk, _ = W.make_inputs(w, seed_offset=3)
+    cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+    # eager
+    eq, ek, edq, edk = q.cuda(), k.cuda(), dq.cuda(), dk.cuda()
+    for _ in range(3):
+        R.apply_qk(eq, ek, cos, sin)
+        R.apply_qk(edq, edk, cos, sin, backward=True)
+    # captured
+    gq, gk, gdq, gdk = q.cuda(), k.cuda(), dq.cuda(), dk.cuda()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            R.apply_qk(gq, gk, cos, sin, stream=s)
+            R.apply_qk(gdq, gdk, cos, sin, backward=True, stream=s)
+    torch.cuda.synchronize()
+    # capture does not execute: replay three times
+    gq.copy_(q.cuda()); gk.copy_(k.cuda()); gdq.copy_(dq.cuda()); gdk.copy_(dk.cuda())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(gq, eq) and torch.equal(gk, ek)
+    assert torch.equal(gdq, edq) and torch.equal(gdk, edk)
