@@ -159,6 +159,42 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
                          int64_t table_rows, void *stream);
 
 /*
+ * rope_attention_fwd -- attention forward with the rotation fused into the
+ * loads of Q and K ("rotary-embedding-torch", flash_attn_with_rotary: the
+ * rotary transformation is applied to the loaded Q and K blocks inside the
+ * attention kernel, so rotated Q and K are never written to global memory).
+ *
+ *   o = softmax(scale * rot(q) rot(k)^T + mask) v
+ *
+ * q: device [B, Hq, Sq, D]; k, v: device [B, Hk, Sk, D]; o: device
+ *    [B, Hq, Sq, D], written; all of `dtype` (ROPE_BF16 or ROPE_F16), dense.
+ *    Hq must be a multiple of Hk (GQA/MQA: query head h uses key/value head
+ *    h / (Hq/Hk)).
+ * cos, sin: the rotation table (rope_tables_build), [table_rows, rotary_dim/2].
+ * pos_q, pos_k: device int32 [Sq], [Sk] or NULL (row = index); -1 leaves a
+ *    token unrotated (pos_mask); other out-of-range values are not rotated and
+ *    raise the flag that rope_check_errors reports.
+ * rotary_dim: multiple of 16, 16 <= rotary_dim <= D; D is 64 or 128.
+ * layout: pair layout of the rotation.  causal: 0 or 1; the mask is aligned
+ *    to the bottom right (query i sees key j when j <= i + Sk - Sq); a query
+ *    row that sees no key gets zeros.
+ * softmax_scale: > 0, or <= 0 for 1/sqrt(D).
+ * Arithmetic: the rotated q and k rows are rounded to `dtype`, S = q k^T is
+ *    accumulated in fp32 in tensor memory, P is rounded to `dtype` for the
+ *    P v product (fp32 accumulation), o is rounded once.
+ * Errors: ROPE_ERR_UNSUPPORTED for other dtypes, D, rotary_dim, layouts or
+ *    pointers not 16-byte aligned; ROPE_ERR_INVALID_ARG for bad sizes, null
+ *    pointers, o overlapping an input; ROPE_ERR_CUDA if the launch fails.
+ *    B, Hq or Sq zero: nothing to do, ROPE_OK.  Asynchronous on `stream`.
+ */
+rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void *o,
+                               const float *cos, const float *sin, const int32_t *pos_q,
+                               const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
+                               int64_t Sk, int32_t D, int32_t rotary_dim, int32_t layout,
+                               int32_t causal, float softmax_scale, int32_t dtype,
+                               int64_t table_rows, void *stream);
+
+/*
  * rope_check_errors -- synchronise `stream`, then report and clear the
  * current device's error flag.
  * Returns ROPE_ERR_CUDA if the stream reports an error, else

@@ -28,7 +28,8 @@ __all__ = [
     "VARIANT_VECTOR", "rope_force_kernel_variant", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
-    "library_path", "load_library", "rope_apply_qk_out", "rotate_qk",
+    "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
+    "attention",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
@@ -88,6 +89,10 @@ def load_library() -> ctypes.CDLL:
                                       c.c_int32, c.c_int64, c.c_int32, c.c_int32, c.c_int32,
                                       c.c_int32, c.c_int32, c.c_int32, c.c_int64, P]
     lib.rope_apply_qk_out.restype = c.c_int
+    lib.rope_attention_fwd.argtypes = [P, P, P, P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32,
+                                       c.c_int64, c.c_int64, c.c_int32, c.c_int32, c.c_int32,
+                                       c.c_int32, c.c_float, c.c_int32, c.c_int64, P]
+    lib.rope_attention_fwd.restype = c.c_int
     lib.rope_force_kernel_variant.argtypes = [c.c_int32]
     lib.rope_force_kernel_variant.restype = c.c_int
     _lib = lib
@@ -320,3 +325,32 @@ def rotate_qk(q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor, sin: t
                       Hk, S, D, rd, _LAYOUT_CODE[layout], int(seq_before_head), int(backward),
                       _DTYPE_CODE[q.dtype], cos.shape[0], stream)
     return q_out, k_out
+
+
+def rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim,
+                       layout, causal, softmax_scale, dtype, table_rows, stream=None):
+    lib = load_library()
+    st = lib.rope_attention_fwd(_addr(q, "q"), _addr(k, "k"), _addr(v, "v"), _addr(o, "o"),
+                                _addr(cos, "cos"), _addr(sin, "sin"), _addr(pos_q, "pos_q"),
+                                _addr(pos_k, "pos_k"), int(B), int(Hq), int(Hk), int(Sq), int(Sk),
+                                int(D), int(rotary_dim), int(layout), int(causal),
+                                float(softmax_scale), int(dtype), int(table_rows), _stream(stream))
+    _check(st, "rope_attention_fwd")
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor,
+              sin: torch.Tensor, pos_q: torch.Tensor | None = None,
+              pos_k: torch.Tensor | None = None, rotary_dim: int | None = None,
+              layout: str = "split_half", causal: bool = False, scale: float | None = None,
+              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """softmax(scale * rot(q) rot(k)^T + mask) v with q [B,Hq,Sq,D], k/v [B,Hk,Sk,D]."""
+    B, Hq, Sq, D = q.shape
+    _, Hk, Sk, _ = k.shape
+    if v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must have the same shape, and q, k, v the same dtype")
+    rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+    o = torch.empty_like(q) if out is None else out
+    rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rd,
+                       _LAYOUT_CODE[layout], int(causal), -1.0 if scale is None else scale,
+                       _DTYPE_CODE[q.dtype], cos.shape[0], stream)
+    return o

@@ -339,6 +339,63 @@ int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, c
     return plan_apply(c, &plan) == ROPE_OK ? (int32_t)plan.variant : 0;
 }
 
+rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void *o,
+                               const float *cos, const float *sin, const int32_t *pos_q,
+                               const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
+                               int64_t Sk, int32_t D, int32_t rotary_dim, int32_t layout,
+                               int32_t causal, float softmax_scale, int32_t dtype,
+                               int64_t table_rows, void *stream)
+{
+    if (dtype != ROPE_BF16 && dtype != ROPE_F16)
+        return ROPE_ERR_UNSUPPORTED;
+    if (layout != ROPE_SPLIT_HALF && layout != ROPE_INTERLEAVED)
+        return ROPE_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128)
+        return ROPE_ERR_UNSUPPORTED;
+    if (rotary_dim < 16 || rotary_dim > D || (rotary_dim % 16) != 0)
+        return ROPE_ERR_UNSUPPORTED;
+    if ((causal != 0 && causal != 1) || B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hk < 0 ||
+        table_rows < 0 || !(softmax_scale == softmax_scale))
+        return ROPE_ERR_INVALID_ARG;
+    if (Hq > 0 && (Hk == 0 || Hq % Hk != 0))
+        return ROPE_ERR_INVALID_ARG;
+    int64_t nq = 0, nk = 0, qb = 0, kb = 0, tab = 0, tabb = 0;
+    if (!mul_ok(B * (int64_t)Hq, Sq, &nq) || !mul_ok(nq, (int64_t)D * 2, &qb) ||
+        !mul_ok(B * (int64_t)Hk, Sk, &nk) || !mul_ok(nk, (int64_t)D * 2, &kb) ||
+        !mul_ok(table_rows, rotary_dim / 2, &tab) || !mul_ok(tab, 4, &tabb))
+        return ROPE_ERR_INVALID_ARG;
+    if (B == 0 || Hq == 0 || Sq == 0)
+        return ROPE_OK;                                  // no output rows
+    if (!q || !o || !cos || !sin || (Sk > 0 && (!k || !v)))
+        return ROPE_ERR_INVALID_ARG;
+    if (table_rows < 1 || (!pos_q && Sq > table_rows) || (!pos_k && Sk > table_rows))
+        return ROPE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(cos) ||
+        !aligned16(sin))
+        return ROPE_ERR_UNSUPPORTED;
+    if (ranges_overlap(o, qb, q, qb) || ranges_overlap(o, qb, k, kb) ||
+        ranges_overlap(o, qb, v, kb) || ranges_overlap(o, qb, cos, tabb) ||
+        ranges_overlap(o, qb, sin, tabb) || ranges_overlap(o, qb, pos_q, Sq * 4) ||
+        ranges_overlap(o, qb, pos_k, Sk * 4))
+        return ROPE_ERR_INVALID_ARG;
+    AttnArgs a;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.cos = cos; a.sin = sin;
+    a.pos_q = pos_q; a.pos_k = pos_k;
+    a.B = B; a.Hq = Hq; a.Hk = Hk; a.Sq = Sq; a.Sk = Sk;
+    a.rotary_dim = rotary_dim;
+    a.table_rows = table_rows;
+    const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt((double)D);
+    a.scale_log2 = (float)(scale * 1.4426950408889634);
+    a.causal = causal;
+    int32_t *taken = nullptr;
+    if (flag_addresses(&a.flag, &taken) != cudaSuccess)
+        return ROPE_ERR_CUDA;
+    return launch_attention(a, D, layout, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ROPE_OK
+               : ROPE_ERR_CUDA;
+}
+
 rope_status rope_check_errors(void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

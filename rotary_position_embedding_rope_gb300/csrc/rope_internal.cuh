@@ -88,6 +88,24 @@ constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;
 // and bulk kernels take rotary spans of up to 32 * kVecThreads bytes.
 constexpr int kMaxVectorsPerHalf = kVecThreads;
 
+// Attention with rotary Q/K (rope_attention.cu).
+struct AttnArgs {
+    const void *q, *k, *v;
+    void *o;
+    const float *cos, *sin;
+    const int32_t *pos_q, *pos_k;    // [Sq], [Sk] or nullptr (-1 = not rotated)
+    int64_t B;
+    int32_t Hq, Hk;
+    int64_t Sq, Sk;
+    int32_t rotary_dim;
+    int64_t table_rows;
+    float scale_log2;                // softmax scale * log2(e)
+    int32_t causal;
+    int32_t *flag;
+};
+cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
+                             cudaStream_t st);
+
 // Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).
 cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);
 cudaError_t launch_apply_bf16(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);

@@ -205,3 +205,38 @@ def test_bulk_kernel_refuses_out_of_place(lib):
 
 def test_apply_out_empty_is_noop(lib):
     assert lib.rope_apply_qk_out(*out_args(B=0, qo=None, ko=None)) == R.ROPE_OK
+
+
+def attn_args(**over):
+    a = dict(q=A16 * 1, k=A16 * 100, v=A16 * 200, o=A16 * 300, cos=A16 * 400, sin=A16 * 500,
+             pq=None, pk=None, B=1, Hq=4, Hk=2, Sq=64, Sk=64, D=128, rd=128, layout=0, causal=1,
+             scale=-1.0, dtype=1, rows=64)
+    a.update(over)
+    return (a["q"], a["k"], a["v"], a["o"], a["cos"], a["sin"], a["pq"], a["pk"], a["B"], a["Hq"],
+            a["Hk"], a["Sq"], a["Sk"], a["D"], a["rd"], a["layout"], a["causal"], a["scale"],
+            a["dtype"], a["rows"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(dtype=0), R.ROPE_ERR_UNSUPPORTED),          # fp32 attention not offered
+    (dict(D=96, rd=96), R.ROPE_ERR_UNSUPPORTED),
+    (dict(rd=8), R.ROPE_ERR_UNSUPPORTED),
+    (dict(rd=40), R.ROPE_ERR_UNSUPPORTED),
+    (dict(layout=2), R.ROPE_ERR_UNSUPPORTED),
+    (dict(Hq=3), R.ROPE_ERR_INVALID_ARG),              # not a multiple of Hk
+    (dict(Hk=0), R.ROPE_ERR_INVALID_ARG),
+    (dict(causal=2), R.ROPE_ERR_INVALID_ARG),
+    (dict(o=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(o=A16 * 1), R.ROPE_ERR_INVALID_ARG),          # o over q
+    (dict(o=A16 * 200 + 64), R.ROPE_ERR_INVALID_ARG),   # o over v
+    (dict(rows=32), R.ROPE_ERR_INVALID_ARG),            # positions past the table
+    (dict(q=A16 + 8), R.ROPE_ERR_UNSUPPORTED),          # not 16-byte aligned
+    (dict(scale=float("nan")), R.ROPE_ERR_INVALID_ARG),
+])
+def test_attention_rejects_bad_arguments(lib, over, status):
+    assert lib.rope_attention_fwd(*attn_args(**over)) == status
+
+
+def test_attention_empty_is_noop(lib):
+    assert lib.rope_attention_fwd(*attn_args(Sq=0, q=None, o=None)) == R.ROPE_OK
+    assert lib.rope_attention_fwd(*attn_args(B=0)) == R.ROPE_OK

@@ -1,0 +1,102 @@
+"""Attention with the rotation fused into the Q/K tile loads (tcgen05) against
+the fp64 rotary-attention oracle.
+
+Tolerance: the kernel rounds P to the element type before the P.V product and
+rounds O once; each is within half a unit in the last place, so per element
+|o - o_ref| <= u * (max|v| + |o_ref|) with u = 2^-8 (bf16) or 2^-10 (fp16),
+a bound twice the two roundings' sum.  Everything else (fp32 accumulation,
+exp2) is far below it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from gpu_util import lib, oracle_tables, require_gpu
+from oracle import attention as OA
+
+pytestmark = pytest.mark.gpu
+U = {"bf16": 2.0 ** -8, "f16": 2.0 ** -10}
+CODE = {"bf16": O.BF16, "f16": O.F16}
+
+
+def _inputs(B, Hq, Hk, Sq, Sk, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = W.draw((B, Hq, Sq, D), dtype, g)
+    k = W.draw((B, Hk, Sk, D), dtype, g)
+    v = W.draw((B, Hk, Sk, D), dtype, g)
+    return q, k, v
+
+
+def _check(got, q, k, v, dtype, rd, layout, c32, s32, pq, pk, causal, what=""):
+    ref = OA.attention(W.bits(q), W.bits(k), W.bits(v), CODE[dtype], rd, layout, c32, s32,
+                       pq, pk, causal)
+    g = got.float().cpu().numpy().astype(np.float64)
+    vmax = float(v.float().abs().max()) if v.numel() else 0.0
+    tol = U[dtype] * (vmax + np.abs(ref))
+    err = np.abs(g - ref)
+    assert np.all(np.isfinite(g)), what
+    assert np.all(err <= tol), "%s: %d of %d beyond tolerance, max err %.3g" % (
+        what, np.count_nonzero(err > tol), err.size, err.max())
+
+
+CASES = [
+    dict(B=1, Hq=4, Hk=2, Sq=200, Sk=200, D=128, rd=128, dtype="bf16", layout="split_half", causal=True),
+    dict(B=2, Hq=2, Hk=2, Sq=130, Sk=257, D=128, rd=64, dtype="bf16", layout="split_half", causal=False),
+    dict(B=1, Hq=8, Hk=1, Sq=129, Sk=129, D=64, rd=32, dtype="f16", layout="interleaved", causal=True),
+    dict(B=1, Hq=2, Hk=1, Sq=64, Sk=300, D=64, rd=64, dtype="bf16", layout="interleaved", causal=False),
+    dict(B=1, Hq=2, Hk=2, Sq=1, Sk=300, D=128, rd=128, dtype="bf16", layout="split_half", causal=True),
+    dict(B=1, Hq=2, Hk=2, Sq=300, Sk=100, D=128, rd=128, dtype="f16", layout="split_half", causal=True),
+]
+
+
+@pytest.mark.parametrize("c", CASES, ids=lambda c: "Sq%d_Sk%d_D%d_rd%d_%s_%s_c%d" % (
+    c["Sq"], c["Sk"], c["D"], c["rd"], c["dtype"], c["layout"], c["causal"]))
+def test_attention_against_oracle(c):
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], 31)
+    rows = max(c["Sq"], c["Sk"]) + 8
+    c32, s32 = oracle_tables(1e4, c["rd"], rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, rotary_dim=c["rd"], layout=c["layout"],
+                    causal=c["causal"])
+    assert R.rope_check_errors() == R.ROPE_OK
+    _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, None, None,
+           c["causal"], str(c))
+
+
+def test_pages_example_cls_tokens_unrotated():
+    """q, k, v [1, 8, 1024 + 2, 64], rotary dim 32, the first 2 tokens not
+    rotated and the rest at positions 0..1023 ("rotary-embedding-torch",
+    flash_attn_with_rotary example), causal."""
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(1, 8, 8, 1026, 1026, 64, "bf16", 7)
+    pos = np.arange(-2, 1024, dtype=np.int32)
+    pos[:2] = -1
+    c32, s32 = oracle_tables(1e4, 32, 1024)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    pg = torch.from_numpy(pos).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=pg, pos_k=pg, rotary_dim=32,
+                    causal=True)
+    assert R.rope_check_errors() == R.ROPE_OK
+    _check(o, q, k, v, "bf16", 32, O.SPLIT_HALF, c32, s32, pos, pos, True, "pages example")
+
+
+def test_attention_with_no_keys_is_zero_and_shift_invariant():
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(1, 2, 2, 100, 0, 128, "bf16", 3)
+    c32, s32 = oracle_tables(1e4, 128, 512)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, causal=False)
+    assert torch.count_nonzero(o) == 0
+    # a common shift of every position changes only rounding
+    q, k, v = _inputs(1, 2, 2, 160, 160, 128, "bf16", 4)
+    p0 = torch.arange(160, dtype=torch.int32).cuda()
+    a = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=p0, pos_k=p0, causal=True)
+    b = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=p0 + 300, pos_k=p0 + 300,
+                    causal=True)
+    assert float((a.float() - b.float()).abs().max()) < 0.05
