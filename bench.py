@@ -316,6 +316,151 @@ def config_of(w):
 
 
 # --------------------------------------------------------------------------
+# attention with fused rotation (--op attention)
+# --------------------------------------------------------------------------
+ATTN_WORKLOAD = dict(name="llama3_8b_prefill_attention_bf16", B=4, Hq=32, Hk=8, S=4096, D=128,
+                     rotary_dim=128, theta=5e5, causal=True, dtype="bf16")
+
+
+def attention_flops(B, Hq, Sq, Sk, D, causal):
+    """Multiply-adds of S = Q K^T and O = P V over the visible (query, key)
+    pairs, times 2: the work a causal kernel must do."""
+    if causal:
+        shift = Sk - Sq
+        pairs = sum(max(0, min(Sk, i + shift + 1)) for i in range(Sq))
+    else:
+        pairs = Sq * Sk
+    return 4.0 * B * Hq * D * pairs
+
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def attention_arm(args):
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from rotary_position_embedding_rope_gb300 import _build
+    if local == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    import rotary_position_embedding_rope_gb300 as R
+
+    a = ATTN_WORKLOAD
+    g = torch.Generator().manual_seed(6)
+    q = W.draw((a["B"], a["Hq"], a["S"], a["D"]), a["dtype"], g).to(device)
+    k = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g).to(device)
+    v = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g).to(device)
+    cos, sin = R.build_tables(a["theta"], a["rotary_dim"], a["S"], device=device)
+    stream = torch.cuda.current_stream(device)
+    o = torch.empty_like(q)
+    warmup = max(3, args.warmup)
+    steps = max(1, min(args.steps, 200))
+
+    def step():
+        R.attention(q, k, v, cos, sin, rotary_dim=a["rotary_dim"], causal=a["causal"], out=o,
+                    stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / steps
+    flops = attention_flops(a["B"], a["Hq"], a["S"], a["S"], a["D"], a["causal"])
+    max_ms, all_flops = aggregate(dist, device, ms * steps, flops * steps)
+    tflops = all_flops / (max_ms * 1e-3) / 1e12
+
+    # context: the same result from the unfused path (rotation kernel, then
+    # torch's scaled_dot_product_attention on the rotated tensors)
+    unfused = None
+    try:
+        import torch.nn.functional as F
+
+        qr, kr = q.clone(), k.clone()
+
+        def unfused_step():
+            qr.copy_(q)
+            kr.copy_(k)
+            R.apply_qk(qr, kr, cos, sin, stream=stream)
+            return F.scaled_dot_product_attention(qr, kr, v, is_causal=True, enable_gqa=True)
+
+        for _ in range(warmup):
+            unfused_step()
+        torch.cuda.synchronize(device)
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(steps):
+            unfused_step()
+        u1.record(stream)
+        torch.cuda.synchronize(device)
+        ums = u0.elapsed_time(u1) / steps
+        unfused = {"ms": round(ums, 4), "tflops": round(flops / (ums * 1e-3) / 1e12, 1),
+                   "what": "copy Q,K; rope_apply_qk; torch scaled_dot_product_attention"}
+    except Exception as exc:  # noqa: BLE001 - context only
+        unfused = {"unavailable": str(exc)[:200]}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        from oracle import attention as OA
+        import oracle as O
+
+        c32, s32 = O.load().tables(a["theta"], a["rotary_dim"], a["S"], 1.0, "f32")
+        nq = 64
+        t0 = time.perf_counter()
+        OA.attention(W.bits(q[:1, :1, :nq].cpu()), W.bits(k[:1, :1].cpu()), W.bits(v[:1, :1].cpu()),
+                     O.BF16, a["rotary_dim"], O.SPLIT_HALF, c32, s32, causal=True)
+        el = time.perf_counter() - t0
+        sf = attention_flops(1, 1, nq, a["S"], a["D"], True)
+        cpu = {"value": round(sf / el / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count() or 0,
+               "kind": "oracle", "sample": "1 head, the last %d of %d query rows against all keys "
+               "(numpy fp64; threads as numpy uses them)" % (nq, a["S"])}
+
+    peak, peak_kind = tensor_peak()
+    if rank == 0:
+        line = {
+            "metric": "fused rotary attention forward TFLOP/s", "op": "attention",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(max_ms / steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": a["dtype"], "data": "synthetic",
+            "config": {"workload": a["name"], "q_shape": [a["B"], a["Hq"], a["S"], a["D"]],
+                       "kv_shape": [a["B"], a["Hk"], a["S"], a["D"]], "causal": a["causal"],
+                       "rotary_dim": a["rotary_dim"], "flops_per_call": flops},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "peak_source": "%s bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
+                         "traffic": None, "kernel": "rope_attn_kernel"},
+            "unfused_context": unfused,
+            "gpu_launches": steps,
+            "clocks": sampler.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+# --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
 def main():
@@ -327,7 +472,16 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", choices=["rope", "attention"], default="rope",
+                    help="rope: the fused Q+K rotation (default); attention: attention with the "
+                         "rotation fused into the Q/K tile loads")
     args = ap.parse_args()
+    if args.op == "attention":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "attention",
+                              "unavailable": "the reference arm times the rotation only"}))
+            return 0
+        return attention_arm(args)
     w = W.BY_NAME[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)

@@ -154,7 +154,7 @@ __device__ __forceinline__ uint32_t kmajor128(int r, int k)
 
 // Table row of a token: its index, or its position; -1 when not rotated.
 __device__ __forceinline__ int64_t attn_row(const int32_t *pos, int64_t s, int64_t table_rows,
-                                            int32_t *flag)
+                                            int32_t *flag, bool report = true)
 {
     if (pos == nullptr)
         return s;
@@ -162,89 +162,147 @@ __device__ __forceinline__ int64_t attn_row(const int32_t *pos, int64_t s, int64
     if (r == -1)
         return -1;
     if (r < 0 || r >= table_rows) {
-        atomicOr(flag, 1);
+        if (report)
+            atomicOr(flag, 1);
         return -1;
     }
     return r;
 }
 
-// Load one head row (D elements of T) from global memory, rotate its first
-// rotary_dim features when trow >= 0, and store it to a K-major 128-row tile
-// at row r.  src == nullptr stores zeros.
-template <typename T, int LAYOUT, int D>
-__device__ __forceinline__ void load_rotate_store(const T *src, int64_t trow, const AttnArgs &a,
-                                                  uint8_t *tile, int r)
+// Warp-cooperative load of the 32 tile rows [32 * warp, 32 * warp + 32):
+// every load instruction covers RPI = 32 / CPR whole rows (CPR = D / 8
+// chunks of 16 bytes per row), so global reads are fully coalesced.  Lane l
+// holds chunk l % CPR of row l / CPR of each group.  Rows whose token index
+// (tok0 + row) is not below n_tok are stored as zeros.
+//   ROT: the first rotary_dim features are rotated with the row's table row
+//        (its position; -1 = not rotated).  Split-half: the partner chunk of a
+//        first-half chunk c is chunk c + rd/16 of the same row, fetched from
+//        that lane with a shuffle; each lane computes the pair and keeps its
+//        own element (the same arithmetic as the row-wise kernels).
+//   VTILE: store to the MN-major value tile instead of a K-major tile.
+template <typename T, int LAYOUT, int D, bool ROT, bool VTILE>
+__device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int64_t n_tok,
+                                               const int32_t *pos, const AttnArgs &a, uint8_t *tile,
+                                               int warp, int lane)
 {
-    constexpr int V = 8;                           // elements per 16-byte chunk
-    const int rd = a.rotary_dim, h = rd >> 1;
-    if (src == nullptr) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
+    constexpr int CPR = D / 8;
+    constexpr int RPI = 32 / CPR;
+    constexpr int ITERS = 32 / RPI;
+    constexpr int BATCH = ITERS;                   // every load of the warp in flight at once
+    const int c = lane % CPR;
+    const int rsub = lane / CPR;
+    const int rd = a.rotary_dim;
+    const int h8 = rd / 16;                        // chunks per half span (split-half)
+#pragma unroll 1
+    for (int i0 = 0; i0 < ITERS; i0 += BATCH) {
+        uint4 x[BATCH];
 #pragma unroll
-        for (int c = 0; c < D / V; ++c)
-            *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V)) = z;
-        return;
-    }
-    const uint4 *row = reinterpret_cast<const uint4 *>(src);
-    if (trow < 0) {
+        for (int u = 0; u < BATCH; ++u) {
+            const int r = warp * 32 + (i0 + u) * RPI + rsub;
+            const bool valid = tok0 + r < n_tok;
+            x[u] = valid ? __ldg(reinterpret_cast<const uint4 *>(rows + (int64_t)r * D) + c)
+                         : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int c = 0; c < D / V; ++c)
-            *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V)) = __ldg(row + c);
-        return;
-    }
-    const float *crow = a.cos + trow * h;
-    const float *srow = a.sin + trow * h;
-    if constexpr (LAYOUT == 0) {
-        // split-half: chunk c of the first half pairs with chunk c + h/8
-        for (int c = 0; c < h / V; ++c) {
-            float fa[V], fb[V], cc[V], ss[V];
-            Elt<T>::unpack(__ldg(row + c), fa);
-            Elt<T>::unpack(__ldg(row + c + h / V), fb);
+        for (int u = 0; u < BATCH; ++u) {
+            const int r = warp * 32 + (i0 + u) * RPI + rsub;
+            uint4 y = x[u];
+            if constexpr (ROT) {
+                const int64_t tok = tok0 + r;
+                const int64_t trow =
+                    tok < n_tok ? attn_row(pos, tok, a.table_rows, a.flag, c == 0) : -1;
+                if constexpr (LAYOUT == 0) {
+                    const int src = c < h8 ? lane + h8 : (c < 2 * h8 ? lane - h8 : lane);
+                    uint4 partner;
+                    partner.x = __shfl_sync(0xffffffffu, x[u].x, src);
+                    partner.y = __shfl_sync(0xffffffffu, x[u].y, src);
+                    partner.z = __shfl_sync(0xffffffffu, x[u].z, src);
+                    partner.w = __shfl_sync(0xffffffffu, x[u].w, src);
+                    if (trow >= 0 && c < 2 * h8) {
+                        const bool first = c < h8;
+                        const int pi = (first ? c : c - h8) * 8;    // pair index of element 0
+                        const float *crow = a.cos + trow * (rd >> 1) + pi;
+                        const float *srow = a.sin + trow * (rd >> 1) + pi;
+                        float f1[8], f2[8], cc[8], ss[8];
+                        Elt<T>::unpack(first ? x[u] : partner, f1);
+                        Elt<T>::unpack(first ? partner : x[u], f2);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float4 cv = __ldg(reinterpret_cast<const float4 *>(crow + c * V) + q);
-                const float4 sv = __ldg(reinterpret_cast<const float4 *>(srow + c * V) + q);
-                cc[4 * q] = cv.x; cc[4 * q + 1] = cv.y; cc[4 * q + 2] = cv.z; cc[4 * q + 3] = cv.w;
-                ss[4 * q] = sv.x; ss[4 * q + 1] = sv.y; ss[4 * q + 2] = sv.z; ss[4 * q + 3] = sv.w;
+                        for (int q = 0; q < 2; ++q) {
+                            const float4 cv = __ldg(reinterpret_cast<const float4 *>(crow) + q);
+                            const float4 sv = __ldg(reinterpret_cast<const float4 *>(srow) + q);
+                            cc[4 * q] = cv.x; cc[4 * q + 1] = cv.y; cc[4 * q + 2] = cv.z; cc[4 * q + 3] = cv.w;
+                            ss[4 * q] = sv.x; ss[4 * q + 1] = sv.y; ss[4 * q + 2] = sv.z; ss[4 * q + 3] = sv.w;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            rotate_pair(f1[e], f2[e], cc[e], ss[e]);
+                        y = Elt<T>::pack(first ? f1 : f2);
+                    }
+                } else {
+                    if (trow >= 0 && c < rd / 8) {
+                        const float4 cv = __ldg(reinterpret_cast<const float4 *>(a.cos + trow * (rd >> 1) + c * 4));
+                        const float4 sv = __ldg(reinterpret_cast<const float4 *>(a.sin + trow * (rd >> 1) + c * 4));
+                        float f[8];
+                        Elt<T>::unpack(x[u], f);
+                        rotate_pair(f[0], f[1], cv.x, sv.x);
+                        rotate_pair(f[2], f[3], cv.y, sv.y);
+                        rotate_pair(f[4], f[5], cv.z, sv.z);
+                        rotate_pair(f[6], f[7], cv.w, sv.w);
+                        y = Elt<T>::pack(f);
+                    }
+                }
             }
-#pragma unroll
-            for (int e = 0; e < V; ++e)
-                rotate_pair(fa[e], fb[e], cc[e], ss[e]);
-            *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V)) = Elt<T>::pack(fa);
-            *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V + h)) = Elt<T>::pack(fb);
-        }
-    } else {
-        // interleaved: chunk c holds pairs 4c .. 4c+3
-        for (int c = 0; c < rd / V; ++c) {
-            float f[V];
-            Elt<T>::unpack(__ldg(row + c), f);
-            const float4 cv = __ldg(reinterpret_cast<const float4 *>(crow + c * 4));
-            const float4 sv = __ldg(reinterpret_cast<const float4 *>(srow + c * 4));
-            rotate_pair(f[0], f[1], cv.x, sv.x);
-            rotate_pair(f[2], f[3], cv.y, sv.y);
-            rotate_pair(f[4], f[5], cv.z, sv.z);
-            rotate_pair(f[6], f[7], cv.w, sv.w);
-            *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V)) = Elt<T>::pack(f);
+            if constexpr (VTILE)
+                *reinterpret_cast<uint4 *>(tile + (uint32_t)(r >> 3) * CPR * 128u + (uint32_t)c * 128u +
+                                           (uint32_t)(r & 7) * 16u) = y;
+            else
+                *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * 8)) = y;
         }
     }
-    for (int c = rd / V; c < D / V; ++c)           // features past rotary_dim: as they are
-        *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * V)) = __ldg(row + c);
+}
+
+// Value tile rows [32 * warp, 32 * warp + 32) straight into the MN-major
+// tile with cp.async (16-byte global -> shared copies, no registers; rows past
+// n_tok are zero-filled).  Completion: cp.async.wait_group by the caller.
+template <int D>
+__device__ __forceinline__ void warp_copy_vtile(const void *rows, int64_t tok0, int64_t n_tok,
+                                                uint8_t *tile, int warp, int lane)
+{
+    constexpr int CPR = D / 8;
+    constexpr int RPI = 32 / CPR;
+    const int c = lane % CPR;
+    const int rsub = lane / CPR;
+#pragma unroll
+    for (int it = 0; it < 32 / RPI; ++it) {
+        const int r = warp * 32 + it * RPI + rsub;
+        const bool valid = tok0 + r < n_tok;
+        const uint8_t *src = static_cast<const uint8_t *>(rows) +
+                             (valid ? ((int64_t)r * D * 2 + c * 16) : 0);
+        const uint32_t dst = attn_smem_u32(tile + (uint32_t)(r >> 3) * CPR * 128u +
+                                           (uint32_t)c * 128u + (uint32_t)(r & 7) * 16u);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                     "r"(valid ? 16 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <typename T, int LAYOUT, int D>
-__global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs a)
 {
-    constexpr int V = 8;
     constexpr uint32_t kTile = kAttnRows * D * 2;  // bytes of a 128 x D tile
     constexpr uint32_t ab_format = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *sQ = smem;
     uint8_t *sK = sQ + kTile;
     uint8_t *sV = sK + kTile;
-    uint8_t *sP = sV + kTile;                      // 128 x 128
+    // P (128 x 128) reuses the K tile once S = Q K^T has been read out of it
+    // (the K tile is exactly P's size when D = 128)
+    uint8_t *sP = D == kAttnKeys ? sK : sV + kTile;
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tmem_base;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.y;
     const int64_t b = bh / a.Hq;
     const int32_t hq = static_cast<int32_t>(bh - b * a.Hq);
@@ -267,9 +325,8 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
 
-    // this thread's query row, rotated, into the Q tile
-    const int64_t q_trow = qi < a.Sq ? attn_row(a.pos_q, qi, a.table_rows, a.flag) : -1;
-    load_rotate_store<T, LAYOUT, D>(qi < a.Sq ? Q + qi * D : nullptr, q_trow, a, sQ, tid);
+    // the query tile, rotated
+    warp_load_tile<T, LAYOUT, D, true, false>(Q + q0 * D, q0, a.Sq, a.pos_q, a, sQ, warp, lane);
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -289,28 +346,15 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
             n_tiles = t;
     }
 
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_ref = -INFINITY, l_run = 0.0f;         // reference max (log2 domain), sum
     uint32_t phase = 0;
     bool ok = true;                                // CTA-uniform
     for (int64_t kt = 0; kt < n_tiles; ++kt) {
-        // 1. key row (rotated) and value row of this thread into the tiles
-        const int64_t kj = kt * kAttnKeys + tid;
-        const int64_t k_trow = kj < a.Sk ? attn_row(a.pos_k, kj, a.table_rows, a.flag) : -1;
-        load_rotate_store<T, LAYOUT, D>(kj < a.Sk ? K + kj * D : nullptr, k_trow, a, sK, tid);
-        {
-            // MN-major value tile: core matrix = 8 keys x 8 features (16 bytes each)
-            const uint32_t base = (uint32_t)(tid >> 3) * (D / 8) * 128u + (uint32_t)(tid & 7) * 16u;
-            if (kj < a.Sk) {
-                const uint4 *vr = reinterpret_cast<const uint4 *>(Vg + kj * D);
-#pragma unroll
-                for (int c = 0; c < D / V; ++c)
-                    *reinterpret_cast<uint4 *>(sV + base + c * 128u) = __ldg(vr + c);
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / V; ++c)
-                    *reinterpret_cast<uint4 *>(sV + base + c * 128u) = make_uint4(0, 0, 0, 0);
-            }
-        }
+        // 1. key tile (rotated) and value tile, loaded warp-cooperatively
+        const int64_t k0 = kt * kAttnKeys;
+        warp_copy_vtile<D>(Vg + k0 * D, k0, a.Sk, sV, warp, lane);
+        warp_load_tile<T, LAYOUT, D, true, false>(K + k0 * D, k0, a.Sk, a.pos_k, a, sK, warp, lane);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncthreads();
@@ -324,6 +368,17 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
                      umma_desc(attn_smem_u32(sK) + kk * 4096u, 2048u, 128u), idesc_s, kk > 0);
             umma_commit(&bar);
         }
+        // while the MMAs run: pull the next tile's key and value rows into L2
+        if (kt + 1 < n_tiles) {
+            const int64_t nk = (kt + 1) * kAttnKeys + tid;
+            if (nk < a.Sk) {
+#pragma unroll
+                for (int off = 0; off < D; off += 64) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(K + nk * D + off));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(Vg + nk * D + off));
+                }
+            }
+        }
         ok = __syncthreads_and(attn_wait(&bar, phase));
         if (!ok)
             break;
@@ -333,7 +388,7 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
         // 3. online softmax of this thread's row (TMEM loads are warp-wide)
         const int64_t lim = a.causal ? qi + shift : INT64_MAX;
         float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
             float sv[32];
             tmem_ld32(lane_base + c0, sv);
@@ -344,10 +399,17 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
                     mx = fmaxf(mx, sv[i] * a.scale_log2);
             }
         }
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
+        // The exponentials use a reference max m_ref that only moves when the
+        // row max exceeds it by more than 8 (factor 256): P stays <= 256,
+        // exact in fp32 and bf16/fp16 range, and O is rescaled only then.
+        float alpha = 1.0f;
+        if (mx > m_ref + 8.0f) {
+            alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
+            m_ref = mx;
+        }
+        const float m_new = m_ref;
         float sum = 0.0f;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
             float sv[32];
             tmem_ld32(lane_base + c0, sv);
@@ -368,9 +430,8 @@ __global__ void __launch_bounds__(kAttnRows, 1) rope_attn_kernel(const AttnArgs 
             }
         }
         l_run = l_run * alpha + sum;
-        m_run = m_new;
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float ov[32];
                 tmem_ld32(lane_base + kAttnKeys + c0, ov);
@@ -448,7 +509,8 @@ static cudaError_t launch_attn_t(const AttnArgs &a, int32_t D, int32_t layout, c
 {
     const dim3 grid((unsigned)((a.Sq + kAttnRows - 1) / kAttnRows), (unsigned)(a.B * a.Hq));
     auto go = [&](auto kernel, int d) -> cudaError_t {
-        const size_t smem = (size_t)3 * kAttnRows * d * 2 + (size_t)kAttnRows * kAttnKeys * 2;
+        const size_t smem = (size_t)3 * kAttnRows * d * 2 +
+                            (d == kAttnKeys ? 0 : (size_t)kAttnRows * kAttnKeys * 2);
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess)
