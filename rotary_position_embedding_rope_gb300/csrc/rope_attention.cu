@@ -145,6 +145,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32])
                  : "memory");
 }
 
+// 2^x with the SFU's approximate exponential (relative error ~2^-22, far
+// below the bf16/fp16 rounding of P that follows).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Byte offset of element (r, k) in a K-major no-swizzle tile of 128 rows.
 __device__ __forceinline__ uint32_t kmajor128(int r, int k)
 {
@@ -169,95 +178,116 @@ __device__ __forceinline__ int64_t attn_row(const int32_t *pos, int64_t s, int64
     return r;
 }
 
-// Warp-cooperative load of the 32 tile rows [32 * warp, 32 * warp + 32):
-// every load instruction covers RPI = 32 / CPR whole rows (CPR = D / 8
-// chunks of 16 bytes per row), so global reads are fully coalesced.  Lane l
-// holds chunk l % CPR of row l / CPR of each group.  Rows whose token index
-// (tok0 + row) is not below n_tok are stored as zeros.
+// Warp-cooperative load of the 32 tile rows [32 * warp, 32 * warp + 32).
+// Lane l takes row (l & 7) of an 8-row group and chunk (l >> 3) of a group of
+// four 16-byte chunks, so every shared-memory store instruction writes four
+// runs of 128 contiguous bytes (8 rows of one chunk): the minimum number of
+// wavefronts, no bank conflicts, in both canonical layouts.  Global reads are
+// 64-byte runs per row.  Rows whose token index (tok0 + row) is not below
+// n_tok are stored as zeros.
 //   ROT: the first rotary_dim features are rotated with the row's table row
-//        (its position; -1 = not rotated).  Split-half: the partner chunk of a
-//        first-half chunk c is chunk c + rd/16 of the same row, fetched from
-//        that lane with a shuffle; each lane computes the pair and keeps its
-//        own element (the same arithmetic as the row-wise kernels).
-//   VTILE: store to the MN-major value tile instead of a K-major tile.
-template <typename T, int LAYOUT, int D, bool ROT, bool VTILE>
+//        (its position; -1 = not rotated).  Split-half: the lane loads the
+//        first-half chunk and its partner chunk (+ rd/16) and rotates both
+//        (the same arithmetic as the row-wise kernels); interleaved: pairs
+//        sit inside one chunk.  Features past rotary_dim are copied.
+template <typename T, int LAYOUT, int D, bool ROT>
 __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int64_t n_tok,
                                                const int32_t *pos, const AttnArgs &a, uint8_t *tile,
                                                int warp, int lane)
 {
-    constexpr int CPR = D / 8;
-    constexpr int RPI = 32 / CPR;
-    constexpr int ITERS = 32 / RPI;
-    constexpr int BATCH = ITERS;                   // every load of the warp in flight at once
-    const int c = lane % CPR;
-    const int rsub = lane / CPR;
+    constexpr int CPR = D / 8;                     // 16-byte chunks per row
+    constexpr int G = 4;                           // 8-row groups per warp
+    const int rr = lane & 7, cc = lane >> 3;
     const int rd = a.rotary_dim;
-    const int h8 = rd / 16;                        // chunks per half span (split-half)
+    const int h = rd >> 1;
+    const int h8 = rd / 16;                        // chunks per half span
+    int r[G];
+    bool valid[G];
+    int64_t trow[G];
+    const uint4 *src[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        r[g] = warp * 32 + g * 8 + rr;
+        valid[g] = tok0 + r[g] < n_tok;
+        src[g] = reinterpret_cast<const uint4 *>(rows + (int64_t)r[g] * D);
+        trow[g] = (ROT && valid[g]) ? attn_row(pos, tok0 + r[g], a.table_rows, a.flag, cc == 0) : -1;
+    }
+    // rotated chunks: each pass issues the loads of all four rows of the lane
+    // (data and table) before any arithmetic, so a pass costs one round trip
+    const int rot_chunks = ROT ? (LAYOUT == 0 ? h8 : rd / 8) : 0;
 #pragma unroll 1
-    for (int i0 = 0; i0 < ITERS; i0 += BATCH) {
-        uint4 x[BATCH];
+    for (int c = cc; c < rot_chunks; c += 4) {
+        if constexpr (LAYOUT == 0) {
+            uint4 x1[G], x2[G];
+            float4 cv[G][2], sv[G][2];
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int r = warp * 32 + (i0 + u) * RPI + rsub;
-            const bool valid = tok0 + r < n_tok;
-            x[u] = valid ? __ldg(reinterpret_cast<const uint4 *>(rows + (int64_t)r * D) + c)
-                         : make_uint4(0, 0, 0, 0);
-        }
+            for (int g = 0; g < G; ++g) {
+                x1[g] = valid[g] ? __ldg(src[g] + c) : make_uint4(0, 0, 0, 0);
+                x2[g] = valid[g] ? __ldg(src[g] + c + h8) : make_uint4(0, 0, 0, 0);
+                const int64_t tr = trow[g] < 0 ? 0 : trow[g];
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int r = warp * 32 + (i0 + u) * RPI + rsub;
-            uint4 y = x[u];
-            if constexpr (ROT) {
-                const int64_t tok = tok0 + r;
-                const int64_t trow =
-                    tok < n_tok ? attn_row(pos, tok, a.table_rows, a.flag, c == 0) : -1;
-                if constexpr (LAYOUT == 0) {
-                    const int src = c < h8 ? lane + h8 : (c < 2 * h8 ? lane - h8 : lane);
-                    uint4 partner;
-                    partner.x = __shfl_sync(0xffffffffu, x[u].x, src);
-                    partner.y = __shfl_sync(0xffffffffu, x[u].y, src);
-                    partner.z = __shfl_sync(0xffffffffu, x[u].z, src);
-                    partner.w = __shfl_sync(0xffffffffu, x[u].w, src);
-                    if (trow >= 0 && c < 2 * h8) {
-                        const bool first = c < h8;
-                        const int pi = (first ? c : c - h8) * 8;    // pair index of element 0
-                        const float *crow = a.cos + trow * (rd >> 1) + pi;
-                        const float *srow = a.sin + trow * (rd >> 1) + pi;
-                        float f1[8], f2[8], cc[8], ss[8];
-                        Elt<T>::unpack(first ? x[u] : partner, f1);
-                        Elt<T>::unpack(first ? partner : x[u], f2);
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const float4 cv = __ldg(reinterpret_cast<const float4 *>(crow) + q);
-                            const float4 sv = __ldg(reinterpret_cast<const float4 *>(srow) + q);
-                            cc[4 * q] = cv.x; cc[4 * q + 1] = cv.y; cc[4 * q + 2] = cv.z; cc[4 * q + 3] = cv.w;
-                            ss[4 * q] = sv.x; ss[4 * q + 1] = sv.y; ss[4 * q + 2] = sv.z; ss[4 * q + 3] = sv.w;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            rotate_pair(f1[e], f2[e], cc[e], ss[e]);
-                        y = Elt<T>::pack(first ? f1 : f2);
-                    }
-                } else {
-                    if (trow >= 0 && c < rd / 8) {
-                        const float4 cv = __ldg(reinterpret_cast<const float4 *>(a.cos + trow * (rd >> 1) + c * 4));
-                        const float4 sv = __ldg(reinterpret_cast<const float4 *>(a.sin + trow * (rd >> 1) + c * 4));
-                        float f[8];
-                        Elt<T>::unpack(x[u], f);
-                        rotate_pair(f[0], f[1], cv.x, sv.x);
-                        rotate_pair(f[2], f[3], cv.y, sv.y);
-                        rotate_pair(f[4], f[5], cv.z, sv.z);
-                        rotate_pair(f[6], f[7], cv.w, sv.w);
-                        y = Elt<T>::pack(f);
-                    }
+                for (int q = 0; q < 2; ++q) {
+                    cv[g][q] = __ldg(reinterpret_cast<const float4 *>(a.cos + tr * h + c * 8) + q);
+                    sv[g][q] = __ldg(reinterpret_cast<const float4 *>(a.sin + tr * h + c * 8) + q);
                 }
             }
-            if constexpr (VTILE)
-                *reinterpret_cast<uint4 *>(tile + (uint32_t)(r >> 3) * CPR * 128u + (uint32_t)c * 128u +
-                                           (uint32_t)(r & 7) * 16u) = y;
-            else
-                *reinterpret_cast<uint4 *>(tile + kmajor128(r, c * 8)) = y;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                uint4 y1 = x1[g], y2 = x2[g];
+                if (trow[g] >= 0) {
+                    float f1[8], f2[8];
+                    const float cs[8] = {cv[g][0].x, cv[g][0].y, cv[g][0].z, cv[g][0].w,
+                                         cv[g][1].x, cv[g][1].y, cv[g][1].z, cv[g][1].w};
+                    const float sn[8] = {sv[g][0].x, sv[g][0].y, sv[g][0].z, sv[g][0].w,
+                                         sv[g][1].x, sv[g][1].y, sv[g][1].z, sv[g][1].w};
+                    Elt<T>::unpack(x1[g], f1);
+                    Elt<T>::unpack(x2[g], f2);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        rotate_pair(f1[e], f2[e], cs[e], sn[e]);
+                    y1 = Elt<T>::pack(f1);
+                    y2 = Elt<T>::pack(f2);
+                }
+                *reinterpret_cast<uint4 *>(tile + kmajor128(r[g], c * 8)) = y1;
+                *reinterpret_cast<uint4 *>(tile + kmajor128(r[g], (c + h8) * 8)) = y2;
+            }
+        } else {
+            uint4 x[G];
+            float4 cv[G], sv[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                x[g] = valid[g] ? __ldg(src[g] + c) : make_uint4(0, 0, 0, 0);
+                const int64_t tr = trow[g] < 0 ? 0 : trow[g];
+                cv[g] = __ldg(reinterpret_cast<const float4 *>(a.cos + tr * h + c * 4));
+                sv[g] = __ldg(reinterpret_cast<const float4 *>(a.sin + tr * h + c * 4));
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                uint4 y = x[g];
+                if (trow[g] >= 0) {
+                    float f[8];
+                    Elt<T>::unpack(x[g], f);
+                    rotate_pair(f[0], f[1], cv[g].x, sv[g].x);
+                    rotate_pair(f[2], f[3], cv[g].y, sv[g].y);
+                    rotate_pair(f[4], f[5], cv[g].z, sv[g].z);
+                    rotate_pair(f[6], f[7], cv[g].w, sv[g].w);
+                    y = Elt<T>::pack(f);
+                }
+                *reinterpret_cast<uint4 *>(tile + kmajor128(r[g], c * 8)) = y;
+            }
         }
+    }
+    // chunks copied unchanged: past the rotary span (or all, without ROT)
+    const int first_copy = ROT ? rd / 8 : 0;
+#pragma unroll 1
+    for (int c = first_copy + cc; c < CPR; c += 4) {
+        uint4 x[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            x[g] = valid[g] ? __ldg(src[g] + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            *reinterpret_cast<uint4 *>(tile + kmajor128(r[g], c * 8)) = x[g];
     }
 }
 
@@ -269,20 +299,21 @@ __device__ __forceinline__ void warp_copy_vtile(const void *rows, int64_t tok0, 
                                                 uint8_t *tile, int warp, int lane)
 {
     constexpr int CPR = D / 8;
-    constexpr int RPI = 32 / CPR;
-    const int c = lane % CPR;
-    const int rsub = lane / CPR;
+    const int rr = lane & 7, cc = lane >> 3;       // 8 rows x 4 chunks: 512 contiguous bytes
 #pragma unroll
-    for (int it = 0; it < 32 / RPI; ++it) {
-        const int r = warp * 32 + it * RPI + rsub;
+    for (int g = 0; g < 4; ++g) {
+        const int r = warp * 32 + g * 8 + rr;
         const bool valid = tok0 + r < n_tok;
-        const uint8_t *src = static_cast<const uint8_t *>(rows) +
-                             (valid ? ((int64_t)r * D * 2 + c * 16) : 0);
-        const uint32_t dst = attn_smem_u32(tile + (uint32_t)(r >> 3) * CPR * 128u +
-                                           (uint32_t)c * 128u + (uint32_t)(r & 7) * 16u);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                     "r"(valid ? 16 : 0)
-                     : "memory");
+#pragma unroll
+        for (int c = cc; c < CPR; c += 4) {
+            const uint8_t *src = static_cast<const uint8_t *>(rows) +
+                                 (valid ? ((int64_t)r * D * 2 + c * 16) : 0);
+            const uint32_t dst = attn_smem_u32(tile + (uint32_t)(r >> 3) * CPR * 128u +
+                                               (uint32_t)c * 128u + (uint32_t)(r & 7) * 16u);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                         "r"(valid ? 16 : 0)
+                         : "memory");
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -326,7 +357,7 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
     }
 
     // the query tile, rotated
-    warp_load_tile<T, LAYOUT, D, true, false>(Q + q0 * D, q0, a.Sq, a.pos_q, a, sQ, warp, lane);
+    warp_load_tile<T, LAYOUT, D, true>(Q + q0 * D, q0, a.Sq, a.pos_q, a, sQ, warp, lane);
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -353,7 +384,7 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
         // 1. key tile (rotated) and value tile, loaded warp-cooperatively
         const int64_t k0 = kt * kAttnKeys;
         warp_copy_vtile<D>(Vg + k0 * D, k0, a.Sk, sV, warp, lane);
-        warp_load_tile<T, LAYOUT, D, true, false>(K + k0 * D, k0, a.Sk, a.pos_k, a, sK, warp, lane);
+        warp_load_tile<T, LAYOUT, D, true>(K + k0 * D, k0, a.Sk, a.pos_k, a, sK, warp, lane);
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -386,25 +417,36 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
         // 3. online softmax of this thread's row (TMEM loads are warp-wide)
-        const int64_t lim = a.causal ? qi + shift : INT64_MAX;
+        // columns of this tile visible to this row: [0, nvis)
+        int64_t vis_end = a.Sk;                    // first invisible key
+        if (a.causal && qi + shift + 1 < vis_end)
+            vis_end = qi + shift + 1;
+        const int64_t nv = vis_end - kt * kAttnKeys;
+        const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
         float mx = -INFINITY;
+        const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
 #pragma unroll 1
         for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
             float sv[32];
             tmem_ld32(lane_base + c0, sv);
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int64_t key = kt * kAttnKeys + c0 + i;
-                if (key < a.Sk && key <= lim)
-                    mx = fmaxf(mx, sv[i] * a.scale_log2);
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, sv[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c0 + i < nvis)
+                        mx = fmaxf(mx, sv[i]);
             }
         }
+        mx *= a.scale_log2;                        // scale > 0: max commutes with it
         // The exponentials use a reference max m_ref that only moves when the
         // row max exceeds it by more than 8 (factor 256): P stays <= 256,
         // exact in fp32 and bf16/fp16 range, and O is rescaled only then.
         float alpha = 1.0f;
         if (mx > m_ref + 8.0f) {
-            alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
+            alpha = m_ref == -INFINITY ? 0.0f : fast_exp2(m_ref - mx);
             m_ref = mx;
         }
         const float m_new = m_ref;
@@ -414,11 +456,18 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
             float sv[32];
             tmem_ld32(lane_base + c0, sv);
             float pv[32];
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int64_t key = kt * kAttnKeys + c0 + i;
-                pv[i] = (key < a.Sk && key <= lim) ? exp2f(sv[i] * a.scale_log2 - m_new) : 0.0f;
-                sum += pv[i];
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
+                    sum += pv[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
+                    sum += pv[i];
+                }
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
