@@ -1,5 +1,5 @@
 // rope_attention.cu -- attention forward with the rotation fused into the
-// loads of the Q and K tiles, on the sm_103a tensor cores (tcgen05, TMEM).
+// loads of the Q and K tiles, on the sm_103a tensor cores (tcgen05, TMEM, TMA).
 //
 // "rotary-embedding-torch", flash_attn_with_rotary: the rotary transformation
 // is applied to the loaded blocks of Q and K inside the attention kernel, so
@@ -9,25 +9,39 @@
 //
 //   O = softmax(scale * rot(Q) rot(K)^T + mask) V
 //
-// One CTA = 128 query rows of one (batch, query head); thread t owns query
-// row t, which is also TMEM lane t of the accumulators.  Per key tile of 128:
-//   1. every thread loads one key row and one value row, rotates the key row
-//      in fp32 (rotate_pair: Kahan-compensated, one rounding) and stores both
-//      to shared memory in the canonical no-swizzle layouts (K: K-major,
-//      V: MN-major, so V rows are stored as they are read);
-//   2. thread 0 issues S = Q K^T (tcgen05.mma, M = N = 128, K = 16 steps,
-//      fp32 in TMEM columns [0, 128)) and commits to an mbarrier;
-//   3. each thread reads its S row back (tcgen05.ld), applies the mask and
-//      the online softmax in the exp2 domain, writes P as bf16/fp16 to shared
-//      memory and rescales its O row in TMEM when the running max moved;
-//   4. thread 0 issues O += P V (M = 128, N = D, K = 16 steps, TMEM columns
-//      [128, 128 + D)) and commits.
+// One CTA = two row blocks of 128 query rows that read the same key/value
+// head: two query heads of one GQA group (same rows), or, when the group
+// size is odd, two consecutive query tiles of one head.  256 threads; warps
+// 4j .. 4j+3 own row block j, thread t row t mod 128, which is also TMEM lane
+// t mod 128 of block j's accumulators (S: columns [256j, 256j+128), O:
+// [256j+128, 256j+128+D)).
+//
+// Key tile kt, in shared memory:
+//   * K rows arrive by TMA (cp.async.bulk.tensor, boxes of 64 elements x 128
+//     rows, 128-byte swizzle: the K-major SW128 operand layout); the table
+//     rows of the keys arrive the same way (boxes of 32 fp32 values), when
+//     the keys sit at their own indices and rotary_dim is a multiple of 64.
+//     Both are requested one tile ahead, so their latency hides behind the
+//     previous tile's softmax.
+//   * Every thread rotates its (row, chunk pair) items of the key tile in
+//     place (rotate_pair: Kahan-compensated, one rounding to the element type).
+//   * Thread 0 issues S = Q K^T for both row blocks (tcgen05.mma, fp32 in TMEM).
+//   * Each thread reads its S row (tcgen05.ld), applies the mask and the
+//     online softmax in the exp2 domain and writes P as bf16/fp16 back into
+//     the first 64 columns of its S row (tcgen05.st); O is rescaled in TMEM
+//     when the reference max moved.
+//   * Thread 0 issues O += P V with P read from TMEM and V (TMA, two buffers,
+//     MN-major SW128) from shared memory.  That product overlaps the next
+//     tile's rotation.
 // The epilogue divides by the softmax sum and writes O.  Causal tiles past
 // the diagonal are skipped.  Every mbarrier wait is bounded (~2 s of clock):
-// on expiry the CTA raises the timeout flag, waits (bounded) for its MMAs,
-// frees its TMEM and returns.
+// on expiry the CTA raises the timeout flag, waits (bounded) for its copies
+// and MMAs in flight, frees its TMEM and returns.
+#include <atomic>
+#include <cstring>
 #include <type_traits>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -38,25 +52,51 @@ namespace rope {
 
 constexpr int kAttnRows = 128;
 constexpr int kAttnKeys = 128;
-constexpr uint32_t kTmemCols = 256;        // S: 128 columns, O: up to 128
+constexpr int kAttnBlocks = 2;                 // row blocks per CTA
+constexpr int kAttnThreads = kAttnRows * kAttnBlocks;
+constexpr uint32_t kBlockCols = 256;           // TMEM columns of one row block (S + O)
+constexpr uint32_t kTmemCols = kBlockCols * kAttnBlocks;
+constexpr uint32_t kChunkBytes = kAttnKeys * 16;   // one 16-byte column of a 128-row tile
+constexpr uint32_t kBoxBytes = kAttnKeys * 128;    // one 128-byte-wide swizzled box of 128 rows
+constexpr uint32_t kSwizzle128 = 2;                // descriptor layout type: 128-byte swizzle
 constexpr long long kAttnWaitCycles = 4000000000LL;
+
+// Tensor maps of one call, all with 128-byte swizzle: K and V as
+// [B * Hk][Sk][D] (box: 64 elements x 128 rows), the cos and sin tables as
+// [table_rows][rotary_dim / 2] fp32 (box: 32 values x 128 rows).  A box lands
+// as 128 rows of 128 bytes, the 16-byte chunk c of row r at chunk c ^ (r & 7).
+struct AttnMaps {
+    CUtensorMap k, v, cos, sin;
+};
 
 __device__ __forceinline__ uint32_t attn_smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Shared-memory matrix descriptor, canonical layout without swizzle: core
-// matrices of 8 rows x 16 bytes; lbo = bytes between core matrices along K,
-// sbo = bytes between core matrices along M/N.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+// Shared-memory matrix descriptor.  Without swizzle (layout 0): core
+// matrices of 8 rows x 16 bytes, K-major lbo = bytes between core matrices
+// along K, sbo = along M/N.  128-byte swizzle (layout 2): K-major sbo = bytes
+// between 8-row groups (lbo unused), the start moving 32 bytes per 16-element
+// step inside a 64-element row; MN-major lbo = bytes between 64-element
+// atoms along N, sbo = bytes between 8-row groups along K.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout = 0)
 {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFF);
     d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;                        // descriptor version for tcgen05
+    d |= (uint64_t)layout << 61;
     return d;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-row tile of swizzled
+// 128-byte-wide boxes (eight chunks per box row).
+__device__ __forceinline__ uint32_t sw128(int r, int c)
+{
+    return (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)r * 128u + (uint32_t)((c ^ r) & 7) * 16u;
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B of the same
@@ -67,8 +107,9 @@ __device__ __forceinline__ uint32_t umma_idesc(int M, int N, uint32_t ab_format,
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate)
+// D (TMEM) (+)= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
@@ -76,10 +117,53 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
                  : "memory");
 }
 
+// D (TMEM) (+)= A (TMEM: lane = row, two 16-bit elements per column, the
+// even one in the low half) * B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(attn_smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(attn_smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(attn_smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                 ::"r"(attn_smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z),
+                   "r"(attn_smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(attn_smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(attn_smem_u32(bar))
                  : "memory");
 }
 
@@ -145,6 +229,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32])
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                   "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),
+                   "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
 // 2^x with the SFU's approximate exponential (relative error ~2^-22, far
 // below the bf16/fp16 rounding of P that follows).
 __device__ __forceinline__ float fast_exp2(float x)
@@ -157,7 +251,7 @@ __device__ __forceinline__ float fast_exp2(float x)
 // Byte offset of element (r, k) in a K-major no-swizzle tile of 128 rows.
 __device__ __forceinline__ uint32_t kmajor128(int r, int k)
 {
-    return (uint32_t)(k >> 3) * 2048u + (uint32_t)(r >> 3) * 128u + (uint32_t)(r & 7) * 16u +
+    return (uint32_t)(k >> 3) * kChunkBytes + (uint32_t)(r >> 3) * 128u + (uint32_t)(r & 7) * 16u +
            (uint32_t)(k & 7) * 2u;
 }
 
@@ -178,19 +272,17 @@ __device__ __forceinline__ int64_t attn_row(const int32_t *pos, int64_t s, int64
     return r;
 }
 
-// Warp-cooperative load of the 32 tile rows [32 * warp, 32 * warp + 32).
-// Lane l takes row (l & 7) of an 8-row group and chunk (l >> 3) of a group of
-// four 16-byte chunks, so every shared-memory store instruction writes four
-// runs of 128 contiguous bytes (8 rows of one chunk): the minimum number of
-// wavefronts, no bank conflicts, in both canonical layouts.  Global reads are
-// 64-byte runs per row.  Rows whose token index (tok0 + row) is not below
-// n_tok are stored as zeros.
-//   ROT: the first rotary_dim features are rotated with the row's table row
-//        (its position; -1 = not rotated).  Split-half: the lane loads the
-//        first-half chunk and its partner chunk (+ rd/16) and rotates both
-//        (the same arithmetic as the row-wise kernels); interleaved: pairs
-//        sit inside one chunk.  Features past rotary_dim are copied.
-template <typename T, int LAYOUT, int D, bool ROT>
+// Warp-cooperative load of the 32 query-tile rows [32 * warp, 32 * warp + 32)
+// from global memory, rotated.  Lane l takes row (l & 7) of an 8-row group and
+// chunk (l >> 3) of a group of four 16-byte chunks, so every shared-memory
+// store instruction writes four runs of 128 contiguous bytes (8 rows of one
+// chunk): no bank conflicts.  Each pass issues the loads of all four rows of
+// the lane (data and table) before any arithmetic.  Rows whose token index
+// (tok0 + row) is not below n_tok are stored as zeros.  The first rotary_dim
+// features are rotated with the row's table row (its position; -1 = not
+// rotated): split-half pairs a chunk with its partner chunk (+ rd/16),
+// interleaved pairs sit inside one chunk.  Features past rotary_dim are copied.
+template <typename T, int LAYOUT, int D>
 __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int64_t n_tok,
                                                const int32_t *pos, const AttnArgs &a, uint8_t *tile,
                                                int warp, int lane)
@@ -210,11 +302,9 @@ __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int6
         r[g] = warp * 32 + g * 8 + rr;
         valid[g] = tok0 + r[g] < n_tok;
         src[g] = reinterpret_cast<const uint4 *>(rows + (int64_t)r[g] * D);
-        trow[g] = (ROT && valid[g]) ? attn_row(pos, tok0 + r[g], a.table_rows, a.flag, cc == 0) : -1;
+        trow[g] = valid[g] ? attn_row(pos, tok0 + r[g], a.table_rows, a.flag, cc == 0) : -1;
     }
-    // rotated chunks: each pass issues the loads of all four rows of the lane
-    // (data and table) before any arithmetic, so a pass costs one round trip
-    const int rot_chunks = ROT ? (LAYOUT == 0 ? h8 : rd / 8) : 0;
+    const int rot_chunks = LAYOUT == 0 ? h8 : rd / 8;
 #pragma unroll 1
     for (int c = cc; c < rot_chunks; c += 4) {
         if constexpr (LAYOUT == 0) {
@@ -277,10 +367,9 @@ __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int6
             }
         }
     }
-    // chunks copied unchanged: past the rotary span (or all, without ROT)
-    const int first_copy = ROT ? rd / 8 : 0;
+    // chunks copied unchanged: past the rotary span
 #pragma unroll 1
-    for (int c = first_copy + cc; c < CPR; c += 4) {
+    for (int c = rd / 8 + cc; c < CPR; c += 4) {
         uint4 x[G];
 #pragma unroll
         for (int g = 0; g < G; ++g)
@@ -291,59 +380,167 @@ __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int6
     }
 }
 
-// Value tile rows [32 * warp, 32 * warp + 32) straight into the MN-major
-// tile with cp.async (16-byte global -> shared copies, no registers; rows past
-// n_tok are zero-filled).  Completion: cp.async.wait_group by the caller.
-template <int D>
-__device__ __forceinline__ void warp_copy_vtile(const void *rows, int64_t tok0, int64_t n_tok,
-                                                uint8_t *tile, int warp, int lane)
+// Rotates the key tile in place (rows k0 .. k0 + 127, swizzled 128-byte
+// boxes as the TMA left them; rows past Sk hold zeros).  Item i = (row i mod
+// 128, chunk i / 128): consecutive lanes take consecutive rows of one chunk,
+// which the swizzle spreads over eight distinct 16-byte bank groups.  STAGED:
+// the keys sit at their own indices and their table rows were staged the
+// same way next to the tile (cos: rd / 64 boxes, then sin); otherwise each
+// row's position is read and its table row fetched from global memory.
+template <typename T, int LAYOUT, bool STAGED>
+__device__ __forceinline__ void rotate_key_tile(uint8_t *sK, const uint8_t *sT, int64_t k0,
+                                                const AttnArgs &a, int tid)
 {
-    constexpr int CPR = D / 8;
-    const int rr = lane & 7, cc = lane >> 3;       // 8 rows x 4 chunks: 512 contiguous bytes
+    const int rd = a.rotary_dim, h = rd >> 1, h8 = rd / 16, h4 = rd / 8;
+    const int per_row = LAYOUT == 0 ? h8 : h4;
+    const int items = kAttnKeys * per_row;
+    const uint8_t *sC = sT, *sS = sT + (size_t)(rd / 64) * kBoxBytes;
+    constexpr int NQ = LAYOUT == 0 ? 2 : 1;        // float4 table reads per item
+#pragma unroll 1
+    for (int i = tid; i < items; i += kAttnThreads) {
+        const int r = i & (kAttnKeys - 1), p = i >> 7;
+        float cs[8], sn[8];
+        if constexpr (STAGED) {
+            const int t0 = NQ * p;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const int r = warp * 32 + g * 8 + rr;
-        const bool valid = tok0 + r < n_tok;
+            for (int q = 0; q < NQ; ++q) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(sC + sw128(r, t0 + q));
+                const float4 s4 = *reinterpret_cast<const float4 *>(sS + sw128(r, t0 + q));
+                cs[4 * q] = c4.x; cs[4 * q + 1] = c4.y; cs[4 * q + 2] = c4.z; cs[4 * q + 3] = c4.w;
+                sn[4 * q] = s4.x; sn[4 * q + 1] = s4.y; sn[4 * q + 2] = s4.z; sn[4 * q + 3] = s4.w;
+            }
+        } else {
+            const int64_t tok = k0 + r;
+            if (tok >= a.Sk)
+                continue;
+            const int64_t tr = attn_row(a.pos_k, tok, a.table_rows, a.flag, p == 0);
+            if (tr < 0)
+                continue;
+            const float4 *cr = reinterpret_cast<const float4 *>(a.cos + tr * h + p * 4 * NQ);
+            const float4 *sr = reinterpret_cast<const float4 *>(a.sin + tr * h + p * 4 * NQ);
 #pragma unroll
-        for (int c = cc; c < CPR; c += 4) {
-            const uint8_t *src = static_cast<const uint8_t *>(rows) +
-                                 (valid ? ((int64_t)r * D * 2 + c * 16) : 0);
-            const uint32_t dst = attn_smem_u32(tile + (uint32_t)(r >> 3) * CPR * 128u +
-                                               (uint32_t)c * 128u + (uint32_t)(r & 7) * 16u);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                         "r"(valid ? 16 : 0)
-                         : "memory");
+            for (int q = 0; q < NQ; ++q) {
+                const float4 c4 = __ldg(cr + q);
+                const float4 s4 = __ldg(sr + q);
+                cs[4 * q] = c4.x; cs[4 * q + 1] = c4.y; cs[4 * q + 2] = c4.z; cs[4 * q + 3] = c4.w;
+                sn[4 * q] = s4.x; sn[4 * q + 1] = s4.y; sn[4 * q + 2] = s4.z; sn[4 * q + 3] = s4.w;
+            }
+        }
+        if constexpr (LAYOUT == 0) {
+            uint4 *p1 = reinterpret_cast<uint4 *>(sK + sw128(r, p));
+            uint4 *p2 = reinterpret_cast<uint4 *>(sK + sw128(r, p + h8));
+            float f1[8], f2[8];
+            Elt<T>::unpack(*p1, f1);
+            Elt<T>::unpack(*p2, f2);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                rotate_pair(f1[e], f2[e], cs[e], sn[e]);
+            *p1 = Elt<T>::pack(f1);
+            *p2 = Elt<T>::pack(f2);
+        } else {
+            uint4 *px = reinterpret_cast<uint4 *>(sK + sw128(r, p));
+            float f[8];
+            Elt<T>::unpack(*px, f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                rotate_pair(f[2 * e], f[2 * e + 1], cs[e], sn[e]);
+            *px = Elt<T>::pack(f);
         }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-template <typename T, int LAYOUT, int D>
-__global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs a)
+// Warp 0: request key tile k0 (and its staged table rows) into sK / sT,
+// completion on bar.  Lane 0 arms the barrier with the byte count first.
+template <int D, bool STAGED>
+__device__ __forceinline__ void issue_key_tile(const AttnMaps &m, uint8_t *sK, uint8_t *sT, int k0,
+                                               int zkv, int tboxes, uint64_t *bar, int lane)
+{
+    const uint32_t bytes = (uint32_t)(D / 64) * kBoxBytes + (STAGED ? 2u * tboxes * kBoxBytes : 0u);
+    if (lane == 0)
+        mbar_expect_tx(bar, bytes);
+    __syncwarp();
+    if (lane < D / 64)
+        tma_load_3d(sK + lane * kBoxBytes, &m.k, lane * 64, k0, zkv, bar);
+    if (STAGED && lane >= 8 && lane < 8 + 2 * tboxes) {
+        const int t = lane - 8;
+        const bool is_cos = t < tboxes;
+        tma_load_2d(sT + t * kBoxBytes, is_cos ? &m.cos : &m.sin, (is_cos ? t : t - tboxes) * 32,
+                    k0, bar);
+    }
+}
+
+// Warp 0: request value tile k0 into sV (MN-major SW128: columns 64 b ..
+// 64 b + 63 in box b, key r at row r), completion on bar.
+template <int D>
+__device__ __forceinline__ void issue_value_tile(const AttnMaps &m, uint8_t *sV, int k0, int zkv,
+                                                 uint64_t *bar, int lane)
+{
+    if (lane == 0)
+        mbar_expect_tx(bar, (uint32_t)(D / 64) * kBoxBytes);
+    __syncwarp();
+    if (lane < D / 64)
+        tma_load_3d(sV + lane * kBoxBytes, &m.v, lane * 64, k0, zkv, bar);
+}
+
+template <typename T, int LAYOUT, int D, bool STAGED>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    rope_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps, const int32_t pair_heads)
 {
     constexpr uint32_t kTile = kAttnRows * D * 2;  // bytes of a 128 x D tile
     constexpr uint32_t ab_format = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     extern __shared__ __align__(1024) uint8_t smem[];
+    // [Q_0][Q_1][K][V_0][V_1][table staging]
     uint8_t *sQ = smem;
-    uint8_t *sK = sQ + kTile;
+    uint8_t *sK = sQ + kAttnBlocks * kTile;
     uint8_t *sV = sK + kTile;
-    // P (128 x 128) reuses the K tile once S = Q K^T has been read out of it
-    // (the K tile is exactly P's size when D = 128)
-    uint8_t *sP = D == kAttnKeys ? sK : sV + kTile;
-    __shared__ __align__(8) uint64_t bar;
+    uint8_t *sT = sV + 2 * kTile;
+    __shared__ __align__(8) uint64_t bar_k, bar_s, bar_o, bar_v[2];
     __shared__ uint32_t tmem_base;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t bh = blockIdx.y;
-    const int64_t b = bh / a.Hq;
-    const int32_t hq = static_cast<int32_t>(bh - b * a.Hq);
-    const int32_t hk = hq / (a.Hq / a.Hk);
-    const int64_t q0 = (int64_t)blockIdx.x * kAttnRows;
-    const int64_t qi = q0 + tid;
-    const T *Q = static_cast<const T *>(a.q) + ((b * a.Hq + hq) * a.Sq) * D;
-    const T *K = static_cast<const T *>(a.k) + ((b * a.Hk + hk) * a.Sk) * D;
-    const T *Vg = static_cast<const T *>(a.v) + ((b * a.Hk + hk) * a.Sk) * D;
+    const int j = warp >> 2;                       // row block of this warp
+    const int wq = warp & 3;                       // TMEM lane quarter
+    const int row = tid & (kAttnRows - 1);
+    const int group = a.Hq / a.Hk;
+    // row block j: query head hq_j, query rows q0_j .. q0_j + 127; the longest
+    // CTAs (the last query tiles, under a causal mask) start first
+    int64_t b, q0_first, q_step;
+    int32_t hq_first, hq_step;
+    if (pair_heads) {
+        const int32_t pairs = a.Hq / 2;
+        b = blockIdx.y / pairs;
+        hq_first = (int32_t)(blockIdx.y - b * pairs) * 2;
+        hq_step = 1;
+        q0_first = (int64_t)(gridDim.x - 1 - blockIdx.x) * kAttnRows;
+        q_step = 0;
+    } else {
+        b = blockIdx.y / a.Hq;
+        hq_first = (int32_t)(blockIdx.y - b * a.Hq);
+        hq_step = 0;
+        q0_first = (int64_t)(gridDim.x - 1 - blockIdx.x) * 2 * kAttnRows;
+        q_step = kAttnRows;
+    }
+    const int32_t hq = hq_first + j * hq_step;
+    const int32_t hk = hq_first / group;
+    const int zkv = (int)(b * a.Hk + hk);
+    const int64_t q0 = q0_first + j * q_step;
+    const int64_t qi = q0 + row;
+    const T *Qh = static_cast<const T *>(a.q) + ((b * a.Hq + hq) * a.Sq) * D;
     T *O = static_cast<T *>(a.o) + ((b * a.Hq + hq) * a.Sq) * D;
+    const int tboxes = a.rotary_dim / 64;          // table boxes of cos (and of sin)
+
+    // key tiles the CTA's rows can see
+    const int64_t shift = a.Sk - a.Sq;             // bottom-right aligned causal mask
+    int64_t n_tiles = (a.Sk + kAttnKeys - 1) / kAttnKeys;
+    if (a.causal) {
+        int64_t last_row = q0_first + (kAttnBlocks - 1) * q_step + kAttnRows - 1;
+        if (last_row > a.Sq - 1)
+            last_row = a.Sq - 1;
+        const int64_t last = last_row + shift;     // last key visible to the CTA
+        const int64_t t = last < 0 ? 0 : last / kAttnKeys + 1;
+        if (t < n_tiles)
+            n_tiles = t;
+    }
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -352,83 +549,111 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(attn_smem_u32(&bar)) : "memory");
+        mbar_init(&bar_k, 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
+        mbar_init(&bar_v[0], 1);
+        mbar_init(&bar_v[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    // the first key tile and the first two value tiles, while Q is loaded
+    if (warp == 0 && n_tiles > 0) {
+        issue_key_tile<D, STAGED>(maps, sK, sT, 0, zkv, tboxes, &bar_k, lane);
+        issue_value_tile<D>(maps, sV, 0, zkv, &bar_v[0], lane);
+        if (n_tiles > 1)
+            issue_value_tile<D>(maps, sV + kTile, kAttnKeys, zkv, &bar_v[1], lane);
+    }
+    // barriers still owed a wait, and the parity each waits for next (value
+    // buffers: bit b for buffer b)
+    bool pend_k = n_tiles > 0, pend_s = false, pend_o = false;
+    uint32_t pend_v = (n_tiles > 0 ? 1u : 0u) | (n_tiles > 1 ? 2u : 0u);
+    uint32_t ph_k = 0, ph_s = 0, ph_o = 0, ph_v = 0;
 
-    // the query tile, rotated
-    warp_load_tile<T, LAYOUT, D, true>(Q + q0 * D, q0, a.Sq, a.pos_q, a, sQ, warp, lane);
-
+    // the query tile of each row block, rotated (by that block's four warps)
+    warp_load_tile<T, LAYOUT, D>(Qh + q0 * D, q0, a.Sq, a.pos_q, a, sQ + j * kTile, wq, lane);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t acc_base = tmem + (uint32_t)j * kBlockCols + ((uint32_t)(wq * 32) << 16);
     const uint32_t idesc_s = umma_idesc(128, kAttnKeys, ab_format, 0);
     const uint32_t idesc_o = umma_idesc(128, D, ab_format, 1);
 
-    // key tiles this query tile can see
-    const int64_t shift = a.Sk - a.Sq;             // bottom-right aligned causal mask
-    int64_t n_tiles = (a.Sk + kAttnKeys - 1) / kAttnKeys;
-    if (a.causal) {
-        const int64_t last = q0 + kAttnRows - 1 + shift;   // last key visible to this tile
-        const int64_t t = last < 0 ? 0 : last / kAttnKeys + 1;
-        if (t < n_tiles)
-            n_tiles = t;
-    }
-
     float m_ref = -INFINITY, l_run = 0.0f;         // reference max (log2 domain), sum
-    uint32_t phase = 0;
     bool ok = true;                                // CTA-uniform
     for (int64_t kt = 0; kt < n_tiles; ++kt) {
-        // 1. key tile (rotated) and value tile, loaded warp-cooperatively
         const int64_t k0 = kt * kAttnKeys;
-        warp_copy_vtile<D>(Vg + k0 * D, k0, a.Sk, sV, warp, lane);
-        warp_load_tile<T, LAYOUT, D, true>(K + k0 * D, k0, a.Sk, a.pos_k, a, sK, warp, lane);
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-
-        // 2. S = Q K^T
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma(tmem, umma_desc(attn_smem_u32(sQ) + kk * 4096u, 2048u, 128u),
-                     umma_desc(attn_smem_u32(sK) + kk * 4096u, 2048u, 128u), idesc_s, kk > 0);
-            umma_commit(&bar);
-        }
-        // while the MMAs run: pull the next tile's key and value rows into L2
-        if (kt + 1 < n_tiles) {
-            const int64_t nk = (kt + 1) * kAttnKeys + tid;
-            if (nk < a.Sk) {
-#pragma unroll
-                for (int off = 0; off < D; off += 64) {
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(K + nk * D + off));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(Vg + nk * D + off));
-                }
-            }
-        }
-        ok = __syncthreads_and(attn_wait(&bar, phase));
+        const bool next = kt + 1 < n_tiles;
+        // 1. the key tile (and its table rows) has landed: rotate it in place
+        ok = __syncthreads_and(attn_wait(&bar_k, ph_k));
         if (!ok)
             break;
-        phase ^= 1;
+        ph_k ^= 1;
+        pend_k = false;
+        rotate_key_tile<T, LAYOUT, STAGED>(sK, sT, k0, a, tid);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // 2. the previous O += P V has finished: P, O and its value buffer are free
+        ok = __syncthreads_and(kt == 0 || attn_wait(&bar_o, ph_o));
+        if (!ok)
+            break;
+        if (kt > 0) {
+            ph_o ^= 1;
+            pend_o = false;
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // 3. S = Q K^T for both row blocks; the value tile after the next one
+        //    goes into the buffer the previous product has released
+        if (warp == 0) {
+            if (lane == 0) {
+#pragma unroll
+                for (int blk = 0; blk < kAttnBlocks; ++blk)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ss(tmem + blk * kBlockCols,
+                                umma_desc(attn_smem_u32(sQ + blk * kTile) + kk * 2u * kChunkBytes,
+                                          kChunkBytes, 128u),
+                                umma_desc(attn_smem_u32(sK) + (kk >> 2) * kBoxBytes + (kk & 3) * 32u,
+                                          16u, 1024u, kSwizzle128),
+                                idesc_s, kk > 0);
+                umma_commit(&bar_s);
+            }
+            __syncwarp();
+            if (next && kt > 0)
+                issue_value_tile<D>(maps, sV + ((kt + 1) & 1) * kTile, (int)(k0 + kAttnKeys), zkv,
+                                    &bar_v[(kt + 1) & 1], lane);
+        }
+        pend_s = true;
+        if (next && kt > 0)
+            pend_v |= 1u << ((kt + 1) & 1);
+        // 4. S is ready; the key buffer and the table staging are free again
+        ok = __syncthreads_and(attn_wait(&bar_s, ph_s));
+        if (!ok)
+            break;
+        ph_s ^= 1;
+        pend_s = false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (next) {
+            if (warp == 0)
+                issue_key_tile<D, STAGED>(maps, sK, sT, (int)(k0 + kAttnKeys), zkv, tboxes, &bar_k,
+                                          lane);
+            pend_k = true;
+        }
 
-        // 3. online softmax of this thread's row (TMEM loads are warp-wide)
+        // 5. online softmax of this thread's row; P goes back into TMEM
         // columns of this tile visible to this row: [0, nvis)
         int64_t vis_end = a.Sk;                    // first invisible key
         if (a.causal && qi + shift + 1 < vis_end)
             vis_end = qi + shift + 1;
-        const int64_t nv = vis_end - kt * kAttnKeys;
+        const int64_t nv = vis_end - k0;
         const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
         float mx = -INFINITY;
         const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
 #pragma unroll 1
         for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
             float sv[32];
-            tmem_ld32(lane_base + c0, sv);
+            tmem_ld32(acc_base + c0, sv);
             if (full) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
@@ -454,7 +679,7 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
 #pragma unroll 1
         for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
             float sv[32];
-            tmem_ld32(lane_base + c0, sv);
+            tmem_ld32(acc_base + c0, sv);
             float pv[32];
             if (full) {
 #pragma unroll
@@ -469,55 +694,71 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
                     sum += pv[i];
                 }
             }
+            // keys c0 .. c0 + 31 -> columns c0 / 2 .. c0 / 2 + 15, all of
+            // which this thread has already read
+            uint32_t w[16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    f[e] = pv[c * 8 + e];
-                *reinterpret_cast<uint4 *>(sP + kmajor128(tid, c0 + c * 8)) = Elt<T>::pack(f);
-            }
+            for (int i = 0; i < 16; ++i)
+                w[i] = Elt<T>::f2_to_word(pv[2 * i], pv[2 * i + 1]);
+            tmem_st16(acc_base + c0 / 2, w);
         }
         l_run = l_run * alpha + sum;
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float ov[32];
-                tmem_ld32(lane_base + kAttnKeys + c0, ov);
+                tmem_ld32(acc_base + kAttnKeys + c0, ov);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     ov[i] *= alpha;
-                tmem_st32(lane_base + kAttnKeys + c0, ov);
+                tmem_st32(acc_base + kAttnKeys + c0, ov);
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-
-        // 4. O += P V
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kAttnKeys / 16; ++kk)
-                umma(tmem + kAttnKeys, umma_desc(attn_smem_u32(sP) + kk * 4096u, 2048u, 128u),
-                     umma_desc(attn_smem_u32(sV) + kk * 2u * (D / 8) * 128u, (D / 8) * 128u, 128u),
-                     idesc_o, (kt > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bar);
-        }
-        ok = __syncthreads_and(attn_wait(&bar, phase));
+        // 6. O += P V once the value tile has landed
+        const int vb = (int)(kt & 1);
+        ok = __syncthreads_and(attn_wait(&bar_v[vb], (ph_v >> vb) & 1u));
         if (!ok)
             break;
-        phase ^= 1;
+        ph_v ^= 1u << vb;
+        pend_v &= ~(1u << vb);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (tid == 0) {
+            const uint32_t v_addr = attn_smem_u32(sV + vb * kTile);
+#pragma unroll
+            for (int blk = 0; blk < kAttnBlocks; ++blk)
+#pragma unroll
+                for (int kk = 0; kk < kAttnKeys / 16; ++kk)
+                    umma_ts(tmem + blk * kBlockCols + kAttnKeys, tmem + blk * kBlockCols + kk * 8,
+                            umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128), idesc_o,
+                            (kt > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bar_o);
+        }
+        pend_o = true;
     }
+    if (ok && pend_o) {
+        ok = __syncthreads_and(attn_wait(&bar_o, ph_o));
+        if (ok)
+            pend_o = false;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
     if (!ok) {
-        // an MMA did not complete in time: report, give it one more bounded
-        // wait, free TMEM and leave without writing
+        // a copy or an MMA did not complete in time: report, give everything
+        // still in flight one more bounded wait, free TMEM, write nothing
         if (tid == 0)
             atomicOr(a.flag, 2);
-        (void)attn_wait(&bar, phase);
+        if (pend_k)
+            (void)attn_wait(&bar_k, ph_k);
+        if (pend_s)
+            (void)attn_wait(&bar_s, ph_s);
+        if (pend_o)
+            (void)attn_wait(&bar_o, ph_o);
+        if (pend_v & 1u)
+            (void)attn_wait(&bar_v[0], ph_v & 1u);
+        if (pend_v & 2u)
+            (void)attn_wait(&bar_v[1], (ph_v >> 1) & 1u);
     } else {
         // epilogue: O / l for this row (zeros when no key is visible); TMEM
         // loads are warp-wide, stores only for rows inside the sequence
@@ -527,7 +768,7 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
         for (int c0 = 0; c0 < D; c0 += 32) {
             float ov[32];
             if (n_tiles > 0) {
-                tmem_ld32(lane_base + kAttnKeys + c0, ov);
+                tmem_ld32(acc_base + kAttnKeys + c0, ov);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
@@ -553,30 +794,131 @@ __global__ void __launch_bounds__(kAttnRows, 2) rope_attn_kernel(const AttnArgs 
                      : "memory");
 }
 
-template <typename T>
-static cudaError_t launch_attn_t(const AttnArgs &a, int32_t D, int32_t layout, cudaStream_t st)
+// ---------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once.
+static EncodeTiledFn encode_tiled()
 {
-    const dim3 grid((unsigned)((a.Sq + kAttnRows - 1) / kAttnRows), (unsigned)(a.B * a.Hq));
-    auto go = [&](auto kernel, int d) -> cudaError_t {
-        const size_t smem = (size_t)3 * kAttnRows * d * 2 +
-                            (d == kAttnKeys ? 0 : (size_t)kAttnRows * kAttnKeys * 2);
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        kernel<<<grid, kAttnRows, smem, st>>>(a);
-        return cudaGetLastError();
-    };
-    if (D == 64)
-        return layout == 0 ? go(rope_attn_kernel<T, 0, 64>, 64) : go(rope_attn_kernel<T, 1, 64>, 64);
-    return layout == 0 ? go(rope_attn_kernel<T, 0, 128>, 128) : go(rope_attn_kernel<T, 1, 128>, 128);
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || p == nullptr)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// [heads][rows][D] 16-bit elements; box 64 elements x 128 rows x 1 head,
+// 128-byte swizzle.
+static bool encode_kv(EncodeTiledFn enc, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
+                      int64_t heads, int64_t rows, int32_t D)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kAttnKeys, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [table_rows][rotary_dim / 2] fp32; box 32 values x 128 rows, 128-byte
+// swizzle (rotary_dim a multiple of 64).
+static bool encode_table(EncodeTiledFn enc, CUtensorMap *m, const float *base, int64_t rows,
+                         int32_t half)
+{
+    const cuuint64_t dims[2] = {(cuuint64_t)half, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)half * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kAttnKeys};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Dynamic shared memory of one CTA: two query tiles, the key tile, two value
+// tiles and the table staging (two 128 x rotary_dim / 2 fp32 blocks at most).
+// With D = 64 the request is raised so that one CTA holds an SM (its 512 TMEM
+// columns are the whole SM's).
+static size_t attn_smem_bytes(int D)
+{
+    const size_t tile = (size_t)kAttnRows * D * 2;
+    const size_t need = kAttnBlocks * tile + tile + 2 * tile + (size_t)2 * (D / 64) * kBoxBytes;
+    const size_t one_per_sm = 120 * 1024;
+    return need > one_per_sm ? need : one_per_sm;
+}
+
+template <typename T, int LAYOUT, int D, bool STAGED>
+static cudaError_t launch_attn_kernel(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
+                                      cudaStream_t st)
+{
+    const int64_t qtiles = (a.Sq + kAttnRows - 1) / kAttnRows;
+    const int64_t heads = a.B * (pair_heads ? a.Hq / 2 : a.Hq);
+    if (heads > 65535)
+        return cudaErrorInvalidConfiguration;      // grid.y limit
+    const dim3 grid((unsigned)(pair_heads ? qtiles : (qtiles + 1) / 2), (unsigned)heads);
+    auto kernel = rope_attn_kernel<T, LAYOUT, D, STAGED>;
+    const size_t smem = attn_smem_bytes(D);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kernel<<<grid, kAttnThreads, smem, st>>>(a, maps, pair_heads);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_attn_d(const AttnArgs &a, const AttnMaps &maps, int32_t layout,
+                                 int pair_heads, cudaStream_t st)
+{
+    const bool staged = a.pos_k == nullptr && a.rotary_dim % 64 == 0;
+    if (layout == 0)
+        return staged ? launch_attn_kernel<T, 0, D, true>(a, maps, pair_heads, st)
+                      : launch_attn_kernel<T, 0, D, false>(a, maps, pair_heads, st);
+    return staged ? launch_attn_kernel<T, 1, D, true>(a, maps, pair_heads, st)
+                  : launch_attn_kernel<T, 1, D, false>(a, maps, pair_heads, st);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
                              cudaStream_t st)
 {
-    return dtype == 1 ? launch_attn_t<__nv_bfloat16>(a, D, layout, st)
-                      : launch_attn_t<__half>(a, D, layout, st);
+    AttnMaps maps;
+    memset(&maps, 0, sizeof maps);
+    if (a.Sk > 0) {
+        EncodeTiledFn enc = encode_tiled();
+        if (enc == nullptr)
+            return cudaErrorNotSupported;
+        const CUtensorMapDataType dt =
+            dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const int64_t heads = a.B * a.Hk;
+        if (!encode_kv(enc, &maps.k, a.k, dt, heads, a.Sk, D) ||
+            !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D))
+            return cudaErrorInvalidValue;
+        if (a.pos_k == nullptr && a.rotary_dim % 64 == 0 &&
+            (!encode_table(enc, &maps.cos, a.cos, a.table_rows, a.rotary_dim / 2) ||
+             !encode_table(enc, &maps.sin, a.sin, a.table_rows, a.rotary_dim / 2)))
+            return cudaErrorInvalidValue;
+    }
+    // two heads of one GQA group per CTA when the group size is even, else
+    // two consecutive query tiles of one head
+    const int pair_heads = (a.Hq / a.Hk) % 2 == 0 ? 1 : 0;
+    if (dtype == 1)
+        return D == 64 ? launch_attn_d<__nv_bfloat16, 64>(a, maps, layout, pair_heads, st)
+                       : launch_attn_d<__nv_bfloat16, 128>(a, maps, layout, pair_heads, st);
+    return D == 64 ? launch_attn_d<__half, 64>(a, maps, layout, pair_heads, st)
+                   : launch_attn_d<__half, 128>(a, maps, layout, pair_heads, st);
 }
 
 }  // namespace rope

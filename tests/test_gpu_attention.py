@@ -48,6 +48,11 @@ CASES = [
     dict(B=1, Hq=2, Hk=1, Sq=64, Sk=300, D=64, rd=64, dtype="bf16", layout="interleaved", causal=False),
     dict(B=1, Hq=2, Hk=2, Sq=1, Sk=300, D=128, rd=128, dtype="bf16", layout="split_half", causal=True),
     dict(B=1, Hq=2, Hk=2, Sq=300, Sk=100, D=128, rd=128, dtype="f16", layout="split_half", causal=True),
+    # eight key tiles: both value buffers alternate several times; Sq < Sk
+    dict(B=1, Hq=4, Hk=2, Sq=520, Sk=1000, D=128, rd=128, dtype="bf16", layout="split_half", causal=True),
+    # odd group (3): pairs of query tiles, the last CTA's second block past Sq
+    dict(B=2, Hq=6, Hk=2, Sq=300, Sk=300, D=64, rd=32, dtype="f16", layout="split_half", causal=False),
+    dict(B=1, Hq=3, Hk=1, Sq=257, Sk=390, D=128, rd=64, dtype="bf16", layout="interleaved", causal=True),
 ]
 
 
@@ -100,3 +105,23 @@ def test_attention_with_no_keys_is_zero_and_shift_invariant():
     b = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=p0 + 300, pos_k=p0 + 300,
                     causal=True)
     assert float((a.float() - b.float()).abs().max()) < 0.05
+
+
+def test_attention_gathered_positions_interleaved():
+    """Per-token positions (a shuffled set, some -1) with the interleaved
+    layout: the key rotation reads each row's table row by its position."""
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(1, 4, 2, 200, 333, 64, "f16", 11)
+    g = np.random.default_rng(5)
+    pq = g.permutation(600)[:200].astype(np.int32)
+    pk = g.permutation(600)[:333].astype(np.int32)
+    pq[::17] = -1
+    pk[::13] = -1
+    c32, s32 = oracle_tables(1e4, 64, 600)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=torch.from_numpy(pq).cuda(),
+                    pos_k=torch.from_numpy(pk).cuda(), rotary_dim=64, layout="interleaved",
+                    causal=False)
+    assert R.rope_check_errors() == R.ROPE_OK
+    _check(o, q, k, v, "f16", 64, O.INTERLEAVED, c32, s32, pq, pk, False, "gathered positions")
