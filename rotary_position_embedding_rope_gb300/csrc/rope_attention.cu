@@ -53,7 +53,9 @@ namespace rope {
 constexpr int kAttnRows = 128;
 constexpr int kAttnKeys = 128;
 constexpr int kAttnBlocks = 2;                 // row blocks per CTA
-constexpr int kAttnThreads = kAttnRows * kAttnBlocks;
+constexpr int kMathThreads = kAttnRows * kAttnBlocks;   // row-block warps 0 .. 7
+constexpr int kIssueWarp = kMathThreads / 32;              // warp 8: TMA and MMA issue
+constexpr int kAttnThreads = kMathThreads + 32;
 constexpr uint32_t kBlockCols = 256;           // TMEM columns of one row block (S + O)
 constexpr uint32_t kTmemCols = kBlockCols * kAttnBlocks;
 constexpr uint32_t kChunkBytes = kAttnKeys * 16;   // one 16-byte column of a 128-row tile
@@ -167,7 +169,10 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
                  : "memory");
 }
 
-__device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity)
+// Bounded wait for the phase of the given parity; false on expiry (~2 s of
+// clock) or once another thread of the CTA has raised *abort.
+__device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity,
+                                          const volatile int *abort = nullptr)
 {
     const long long t0 = clock64();
     while (true) {
@@ -180,9 +185,14 @@ __device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity)
                      : "memory");
         if (done)
             return true;
-        if (clock64() - t0 > kAttnWaitCycles)
+        if ((abort != nullptr && *abort) || clock64() - t0 > kAttnWaitCycles)
             return false;
     }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(attn_smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
@@ -380,76 +390,109 @@ __device__ __forceinline__ void warp_load_tile(const T *rows, int64_t tok0, int6
     }
 }
 
-// Rotates the key tile in place (rows k0 .. k0 + 127, swizzled 128-byte
-// boxes as the TMA left them; rows past Sk hold zeros).  Item i = (row i mod
-// 128, chunk i / 128): consecutive lanes take consecutive rows of one chunk,
-// which the swizzle spreads over eight distinct 16-byte bank groups.  STAGED:
-// the keys sit at their own indices and their table rows were staged the
-// same way next to the tile (cos: rd / 64 boxes, then sin); otherwise each
-// row's position is read and its table row fetched from global memory.
+// One (row, chunk) item of the key-tile rotation: the data chunk(s), their
+// shared-memory offsets and the cos/sin values.
+struct KeyItem {
+    uint4 x1, x2;
+    uint32_t o1, o2;
+    float cs[8], sn[8];
+    bool rot;
+};
+
+// Loads item i of the key-tile rotation (row i mod 128, chunk i / 128).
 template <typename T, int LAYOUT, bool STAGED>
-__device__ __forceinline__ void rotate_key_tile(uint8_t *sK, const uint8_t *sT, int64_t k0,
-                                                const AttnArgs &a, int tid)
+__device__ __forceinline__ void load_key_item(KeyItem &it, int i, const uint8_t *sK,
+                                              const uint8_t *sT, int64_t k0, const AttnArgs &a)
 {
-    const int rd = a.rotary_dim, h = rd >> 1, h8 = rd / 16, h4 = rd / 8;
-    const int per_row = LAYOUT == 0 ? h8 : h4;
-    const int items = kAttnKeys * per_row;
-    const uint8_t *sC = sT, *sS = sT + (size_t)(rd / 64) * kBoxBytes;
     constexpr int NQ = LAYOUT == 0 ? 2 : 1;        // float4 table reads per item
-#pragma unroll 1
-    for (int i = tid; i < items; i += kAttnThreads) {
-        const int r = i & (kAttnKeys - 1), p = i >> 7;
-        float cs[8], sn[8];
-        if constexpr (STAGED) {
-            const int t0 = NQ * p;
+    const int rd = a.rotary_dim, h = rd >> 1, h8 = rd / 16;
+    const int r = i & (kAttnKeys - 1), p = i >> 7;
+    it.o1 = sw128(r, p);
+    it.o2 = sw128(r, p + h8);
+    it.x1 = *reinterpret_cast<const uint4 *>(sK + it.o1);
+    if (LAYOUT == 0)
+        it.x2 = *reinterpret_cast<const uint4 *>(sK + it.o2);
+    it.rot = true;
+    if constexpr (STAGED) {
+        const uint8_t *sC = sT, *sS = sT + (size_t)(rd / 64) * kBoxBytes;
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float4 c4 = *reinterpret_cast<const float4 *>(sC + sw128(r, t0 + q));
-                const float4 s4 = *reinterpret_cast<const float4 *>(sS + sw128(r, t0 + q));
-                cs[4 * q] = c4.x; cs[4 * q + 1] = c4.y; cs[4 * q + 2] = c4.z; cs[4 * q + 3] = c4.w;
-                sn[4 * q] = s4.x; sn[4 * q + 1] = s4.y; sn[4 * q + 2] = s4.z; sn[4 * q + 3] = s4.w;
-            }
-        } else {
-            const int64_t tok = k0 + r;
-            if (tok >= a.Sk)
-                continue;
-            const int64_t tr = attn_row(a.pos_k, tok, a.table_rows, a.flag, p == 0);
-            if (tr < 0)
-                continue;
-            const float4 *cr = reinterpret_cast<const float4 *>(a.cos + tr * h + p * 4 * NQ);
-            const float4 *sr = reinterpret_cast<const float4 *>(a.sin + tr * h + p * 4 * NQ);
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float4 c4 = __ldg(cr + q);
-                const float4 s4 = __ldg(sr + q);
-                cs[4 * q] = c4.x; cs[4 * q + 1] = c4.y; cs[4 * q + 2] = c4.z; cs[4 * q + 3] = c4.w;
-                sn[4 * q] = s4.x; sn[4 * q + 1] = s4.y; sn[4 * q + 2] = s4.z; sn[4 * q + 3] = s4.w;
-            }
+        for (int q = 0; q < NQ; ++q) {
+            const float4 c4 = *reinterpret_cast<const float4 *>(sC + sw128(r, NQ * p + q));
+            const float4 s4 = *reinterpret_cast<const float4 *>(sS + sw128(r, NQ * p + q));
+            it.cs[4 * q] = c4.x; it.cs[4 * q + 1] = c4.y; it.cs[4 * q + 2] = c4.z; it.cs[4 * q + 3] = c4.w;
+            it.sn[4 * q] = s4.x; it.sn[4 * q + 1] = s4.y; it.sn[4 * q + 2] = s4.z; it.sn[4 * q + 3] = s4.w;
         }
-        if constexpr (LAYOUT == 0) {
-            uint4 *p1 = reinterpret_cast<uint4 *>(sK + sw128(r, p));
-            uint4 *p2 = reinterpret_cast<uint4 *>(sK + sw128(r, p + h8));
-            float f1[8], f2[8];
-            Elt<T>::unpack(*p1, f1);
-            Elt<T>::unpack(*p2, f2);
+    } else {
+        const int64_t tok = k0 + r;
+        const int64_t tr = tok < a.Sk ? attn_row(a.pos_k, tok, a.table_rows, a.flag, p == 0) : -1;
+        it.rot = tr >= 0;
+        const int64_t trc = tr < 0 ? 0 : tr;
+        const float4 *cr = reinterpret_cast<const float4 *>(a.cos + trc * h + p * 4 * NQ);
+        const float4 *sr = reinterpret_cast<const float4 *>(a.sin + trc * h + p * 4 * NQ);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                rotate_pair(f1[e], f2[e], cs[e], sn[e]);
-            *p1 = Elt<T>::pack(f1);
-            *p2 = Elt<T>::pack(f2);
-        } else {
-            uint4 *px = reinterpret_cast<uint4 *>(sK + sw128(r, p));
-            float f[8];
-            Elt<T>::unpack(*px, f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                rotate_pair(f[2 * e], f[2 * e + 1], cs[e], sn[e]);
-            *px = Elt<T>::pack(f);
+        for (int q = 0; q < NQ; ++q) {
+            const float4 c4 = __ldg(cr + q);
+            const float4 s4 = __ldg(sr + q);
+            it.cs[4 * q] = c4.x; it.cs[4 * q + 1] = c4.y; it.cs[4 * q + 2] = c4.z; it.cs[4 * q + 3] = c4.w;
+            it.sn[4 * q] = s4.x; it.sn[4 * q + 1] = s4.y; it.sn[4 * q + 2] = s4.z; it.sn[4 * q + 3] = s4.w;
         }
     }
 }
 
-// Warp 0: request key tile k0 (and its staged table rows) into sK / sT,
+// Rotates a loaded item and writes it back (unrotated rows stay as they are).
+template <typename T, int LAYOUT>
+__device__ __forceinline__ void store_key_item(KeyItem &it, uint8_t *sK)
+{
+    if (!it.rot)
+        return;
+    if constexpr (LAYOUT == 0) {
+        float f1[8], f2[8];
+        Elt<T>::unpack(it.x1, f1);
+        Elt<T>::unpack(it.x2, f2);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            rotate_pair(f1[e], f2[e], it.cs[e], it.sn[e]);
+        *reinterpret_cast<uint4 *>(sK + it.o1) = Elt<T>::pack(f1);
+        *reinterpret_cast<uint4 *>(sK + it.o2) = Elt<T>::pack(f2);
+    } else {
+        float f[8];
+        Elt<T>::unpack(it.x1, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            rotate_pair(f[2 * e], f[2 * e + 1], it.cs[e], it.sn[e]);
+        *reinterpret_cast<uint4 *>(sK + it.o1) = Elt<T>::pack(f);
+    }
+}
+
+// Rotates the key tile in place (rows k0 .. k0 + 127, swizzled 128-byte
+// boxes as the TMA left them; rows past Sk hold zeros), by the kMathThreads
+// threads of the row blocks.  Item i = (row i mod 128, chunk i / 128):
+// consecutive lanes take consecutive rows of one chunk, which the swizzle
+// spreads over eight distinct 16-byte bank groups.  Two items are loaded
+// before either is rotated.  STAGED: the keys sit at their own indices and
+// their table rows were staged the same way next to the tile (cos: rd / 64
+// boxes, then sin); otherwise each row's position is read and its table row
+// fetched from global memory.
+template <typename T, int LAYOUT, bool STAGED>
+__device__ __forceinline__ void rotate_key_tile(uint8_t *sK, const uint8_t *sT, int64_t k0,
+                                                const AttnArgs &a, int tid)
+{
+    const int per_row = LAYOUT == 0 ? a.rotary_dim / 16 : a.rotary_dim / 8;
+    const int items = kAttnKeys * per_row;
+#pragma unroll 1
+    for (int i = tid; i < items; i += 2 * kMathThreads) {
+        const bool second = i + kMathThreads < items;
+        KeyItem x, y;
+        load_key_item<T, LAYOUT, STAGED>(x, i, sK, sT, k0, a);
+        if (second)
+            load_key_item<T, LAYOUT, STAGED>(y, i + kMathThreads, sK, sT, k0, a);
+        store_key_item<T, LAYOUT>(x, sK);
+        if (second)
+            store_key_item<T, LAYOUT>(y, sK);
+    }
+}
+
+// Issue warp: request key tile k0 (and its staged table rows) into sK / sT,
 // completion on bar.  Lane 0 arms the barrier with the byte count first.
 template <int D, bool STAGED>
 __device__ __forceinline__ void issue_key_tile(const AttnMaps &m, uint8_t *sK, uint8_t *sT, int k0,
@@ -469,7 +512,7 @@ __device__ __forceinline__ void issue_key_tile(const AttnMaps &m, uint8_t *sK, u
     }
 }
 
-// Warp 0: request value tile k0 into sV (MN-major SW128: columns 64 b ..
+// Issue warp: request value tile k0 into sV (MN-major SW128: columns 64 b ..
 // 64 b + 63 in box b, key r at row r), completion on bar.
 template <int D>
 __device__ __forceinline__ void issue_value_tile(const AttnMaps &m, uint8_t *sV, int k0, int zkv,
@@ -494,11 +537,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *sK = sQ + kAttnBlocks * kTile;
     uint8_t *sV = sK + kTile;
     uint8_t *sT = sV + 2 * kTile;
-    __shared__ __align__(8) uint64_t bar_k, bar_s, bar_o, bar_v[2];
+    // completions: key tile + table landed (TMA), S ready, O += P V done
+    // (MMA commits), value tile landed (TMA, per buffer), key tile rotated
+    // and P ready (the kMathThreads row-block threads arrive)
+    __shared__ __align__(8) uint64_t bar_k, bar_s, bar_o, bar_v[2], bar_krot, bar_p;
     __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = warp >> 2;                       // row block of this warp
+    const bool math = warp < kIssueWarp;           // a row-block warp (else the issue warp)
+    const int j = math ? warp >> 2 : 0;            // row block of this warp
     const int wq = warp & 3;                       // TMEM lane quarter
     const int row = tid & (kAttnRows - 1);
     const int group = a.Hq / a.Hk;
@@ -554,58 +602,188 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(&bar_o, 1);
         mbar_init(&bar_v[0], 1);
         mbar_init(&bar_v[1], 1);
+        mbar_init(&bar_krot, kMathThreads);
+        mbar_init(&bar_p, kMathThreads);
+        abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     // the first key tile and the first two value tiles, while Q is loaded
-    if (warp == 0 && n_tiles > 0) {
+    if (warp == kIssueWarp && n_tiles > 0) {
         issue_key_tile<D, STAGED>(maps, sK, sT, 0, zkv, tboxes, &bar_k, lane);
         issue_value_tile<D>(maps, sV, 0, zkv, &bar_v[0], lane);
         if (n_tiles > 1)
             issue_value_tile<D>(maps, sV + kTile, kAttnKeys, zkv, &bar_v[1], lane);
     }
-    // barriers still owed a wait, and the parity each waits for next (value
-    // buffers: bit b for buffer b)
-    bool pend_k = n_tiles > 0, pend_s = false, pend_o = false;
-    uint32_t pend_v = (n_tiles > 0 ? 1u : 0u) | (n_tiles > 1 ? 2u : 0u);
-    uint32_t ph_k = 0, ph_s = 0, ph_o = 0, ph_v = 0;
-
     // the query tile of each row block, rotated (by that block's four warps)
-    warp_load_tile<T, LAYOUT, D>(Qh + q0 * D, q0, a.Sq, a.pos_q, a, sQ + j * kTile, wq, lane);
+    if (math)
+        warp_load_tile<T, LAYOUT, D>(Qh + q0 * D, q0, a.Sq, a.pos_q, a, sQ + j * kTile, wq, lane);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
-    const uint32_t acc_base = tmem + (uint32_t)j * kBlockCols + ((uint32_t)(wq * 32) << 16);
-    const uint32_t idesc_s = umma_idesc(128, kAttnKeys, ab_format, 0);
-    const uint32_t idesc_o = umma_idesc(128, D, ab_format, 1);
+    volatile int *abort = &abort_flag;
+    bool ok = true;
 
-    float m_ref = -INFINITY, l_run = 0.0f;         // reference max (log2 domain), sum
-    bool ok = true;                                // CTA-uniform
-    for (int64_t kt = 0; kt < n_tiles; ++kt) {
-        const int64_t k0 = kt * kAttnKeys;
-        const bool next = kt + 1 < n_tiles;
-        // 1. the key tile (and its table rows) has landed: rotate it in place
-        ok = __syncthreads_and(attn_wait(&bar_k, ph_k));
-        if (!ok)
-            break;
-        ph_k ^= 1;
-        pend_k = false;
-        rotate_key_tile<T, LAYOUT, STAGED>(sK, sT, k0, a, tid);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        // 2. the previous O += P V has finished: P, O and its value buffer are free
-        ok = __syncthreads_and(kt == 0 || attn_wait(&bar_o, ph_o));
-        if (!ok)
-            break;
-        if (kt > 0) {
-            ph_o ^= 1;
-            pend_o = false;
+    if (math) {
+        // ---- row-block warps: rotate each key tile, then the softmax of row qi
+        const uint32_t acc_base = tmem + (uint32_t)j * kBlockCols + ((uint32_t)(wq * 32) << 16);
+        float m_ref = -INFINITY, l_run = 0.0f;     // reference max (log2 domain), sum
+        uint32_t ph = 0;                           // parity of tile kt's phases
+        for (int64_t kt = 0; kt < n_tiles; ++kt, ph ^= 1) {
+            const int64_t k0 = kt * kAttnKeys;
+            // 1. the key tile (and its table rows) has landed: rotate it in place
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_k, ph, abort));
+            if (!ok)
+                break;
+            rotate_key_tile<T, LAYOUT, STAGED>(sK, sT, k0, a, tid);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&bar_krot);
+            // 2. S = Q K^T is ready; O += P V of the previous tile has finished
+            //    (the issue warp waits for it before S)
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_s, ph, abort) &&
+                                             (kt == 0 || attn_wait(&bar_o, ph ^ 1, abort)));
+            if (!ok)
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // 3. online softmax; P goes back into TMEM over S
+            // columns of this tile visible to this row: [0, nvis)
+            int64_t vis_end = a.Sk;                // first invisible key
+            if (a.causal && qi + shift + 1 < vis_end)
+                vis_end = qi + shift + 1;
+            const int64_t nv = vis_end - k0;
+            const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
+            float mx = -INFINITY;
+            const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
+#pragma unroll 1
+            for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
+                float sv[32];
+                tmem_ld32(acc_base + c0, sv);
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx = fmaxf(mx, sv[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < nvis)
+                            mx = fmaxf(mx, sv[i]);
+                }
+            }
+            mx *= a.scale_log2;                    // scale > 0: max commutes with it
+            // The exponentials use a reference max m_ref that only moves when
+            // the row max exceeds it by more than 8 (factor 256): P stays <=
+            // 256, exact in fp32 and bf16/fp16 range, and O is rescaled only then.
+            float alpha = 1.0f;
+            if (mx > m_ref + 8.0f) {
+                alpha = m_ref == -INFINITY ? 0.0f : fast_exp2(m_ref - mx);
+                m_ref = mx;
+            }
+            const float m_new = m_ref;
+            float sum = 0.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
+                float sv[32];
+                tmem_ld32(acc_base + c0, sv);
+                float pv[32];
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        pv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
+                        sum += pv[i];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        pv[i] = c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
+                        sum += pv[i];
+                    }
+                }
+                // keys c0 .. c0 + 31 -> columns c0 / 2 .. c0 / 2 + 15, all of
+                // which this thread has already read
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = Elt<T>::f2_to_word(pv[2 * i], pv[2 * i + 1]);
+                tmem_st16(acc_base + c0 / 2, w);
+            }
+            l_run = l_run * alpha + sum;
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float ov[32];
+                    tmem_ld32(acc_base + kAttnKeys + c0, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ov[i] *= alpha;
+                    tmem_st32(acc_base + kAttnKeys + c0, ov);
+                }
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&bar_p);
         }
+        // the last O += P V
+        if (ok && n_tiles > 0)
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph ^ 1, abort));
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // 3. S = Q K^T for both row blocks; the value tile after the next one
-        //    goes into the buffer the previous product has released
-        if (warp == 0) {
+        if (!ok) {
+            *abort = 1;
+        } else {
+            // epilogue: O / l for this row (zeros when no key is visible);
+            // TMEM loads are warp-wide, stores only for rows inside the sequence
+            const float inv = (n_tiles > 0 && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+            uint4 *dst = reinterpret_cast<uint4 *>(O + qi * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float ov[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(acc_base + kAttnKeys + c0, ov);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ov[i] = 0.0f;
+                }
+                if (qi < a.Sq) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[e] = ov[c * 8 + e] * inv;
+                        dst[(c0 + c * 8) / 8] = Elt<T>::pack(f);
+                    }
+                }
+            }
+        }
+    } else {
+        // ---- issue warp: TMA copies one tile ahead, the MMAs (lane 0)
+        const uint32_t idesc_s = umma_idesc(128, kAttnKeys, ab_format, 0);
+        const uint32_t idesc_o = umma_idesc(128, D, ab_format, 1);
+        // barriers with a copy or MMA in flight, and their next parities
+        bool pend_k = n_tiles > 0, pend_s = false, pend_o = false;
+        uint32_t pend_v = (n_tiles > 0 ? 1u : 0u) | (n_tiles > 1 ? 2u : 0u);
+        uint32_t ph_k = 0, ph_s = 0, ph_o = 0, ph_v = 0;
+        for (int64_t kt = 0; kt < n_tiles; ++kt) {
+            const int64_t k0 = kt * kAttnKeys;
+            const bool next = kt + 1 < n_tiles;
+            // the key tile is rotated; the previous O += P V has finished
+            // (P, O and its value buffer are free)
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_krot, (uint32_t)(kt & 1), abort));
+            if (!ok)
+                break;
+            if (kt > 0) {
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph_o, abort));
+                if (!ok)
+                    break;
+                ph_o ^= 1;
+                pend_o = false;
+            }
+            ph_k ^= 1;                             // the math warps waited for it
+            pend_k = false;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // S = Q K^T for both row blocks
             if (lane == 0) {
 #pragma unroll
                 for (int blk = 0; blk < kAttnBlocks; ++blk)
@@ -619,175 +797,74 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 idesc_s, kk > 0);
                 umma_commit(&bar_s);
             }
+            pend_s = true;
             __syncwarp();
-            if (next && kt > 0)
+            // the value tile after the next one, into the buffer just released
+            if (next && kt > 0) {
                 issue_value_tile<D>(maps, sV + ((kt + 1) & 1) * kTile, (int)(k0 + kAttnKeys), zkv,
                                     &bar_v[(kt + 1) & 1], lane);
-        }
-        pend_s = true;
-        if (next && kt > 0)
-            pend_v |= 1u << ((kt + 1) & 1);
-        // 4. S is ready; the key buffer and the table staging are free again
-        ok = __syncthreads_and(attn_wait(&bar_s, ph_s));
-        if (!ok)
-            break;
-        ph_s ^= 1;
-        pend_s = false;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (next) {
-            if (warp == 0)
+                pend_v |= 1u << ((kt + 1) & 1);
+            }
+            // S is ready: the key buffer and the table staging are free again
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_s, ph_s, abort));
+            if (!ok)
+                break;
+            ph_s ^= 1;
+            pend_s = false;
+            if (next) {
                 issue_key_tile<D, STAGED>(maps, sK, sT, (int)(k0 + kAttnKeys), zkv, tboxes, &bar_k,
                                           lane);
-            pend_k = true;
-        }
-
-        // 5. online softmax of this thread's row; P goes back into TMEM
-        // columns of this tile visible to this row: [0, nvis)
-        int64_t vis_end = a.Sk;                    // first invisible key
-        if (a.causal && qi + shift + 1 < vis_end)
-            vis_end = qi + shift + 1;
-        const int64_t nv = vis_end - k0;
-        const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
-        float mx = -INFINITY;
-        const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
-#pragma unroll 1
-        for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
-            float sv[32];
-            tmem_ld32(acc_base + c0, sv);
-            if (full) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    mx = fmaxf(mx, sv[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c0 + i < nvis)
-                        mx = fmaxf(mx, sv[i]);
+                pend_k = true;
             }
-        }
-        mx *= a.scale_log2;                        // scale > 0: max commutes with it
-        // The exponentials use a reference max m_ref that only moves when the
-        // row max exceeds it by more than 8 (factor 256): P stays <= 256,
-        // exact in fp32 and bf16/fp16 range, and O is rescaled only then.
-        float alpha = 1.0f;
-        if (mx > m_ref + 8.0f) {
-            alpha = m_ref == -INFINITY ? 0.0f : fast_exp2(m_ref - mx);
-            m_ref = mx;
-        }
-        const float m_new = m_ref;
-        float sum = 0.0f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
-            float sv[32];
-            tmem_ld32(acc_base + c0, sv);
-            float pv[32];
-            if (full) {
+            // P ready and the value tile landed: O += P V
+            const int vb = (int)(kt & 1);
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_p, (uint32_t)(kt & 1), abort) &&
+                                             attn_wait(&bar_v[vb], (ph_v >> vb) & 1u, abort));
+            if (!ok)
+                break;
+            ph_v ^= 1u << vb;
+            pend_v &= ~(1u << vb);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (lane == 0) {
+                const uint32_t v_addr = attn_smem_u32(sV + vb * kTile);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
-                    sum += pv[i];
-                }
-            } else {
+                for (int blk = 0; blk < kAttnBlocks; ++blk)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
-                    sum += pv[i];
-                }
+                    for (int kk = 0; kk < kAttnKeys / 16; ++kk)
+                        umma_ts(tmem + blk * kBlockCols + kAttnKeys, tmem + blk * kBlockCols + kk * 8,
+                                umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128),
+                                idesc_o, (kt > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bar_o);
             }
-            // keys c0 .. c0 + 31 -> columns c0 / 2 .. c0 / 2 + 15, all of
-            // which this thread has already read
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                w[i] = Elt<T>::f2_to_word(pv[2 * i], pv[2 * i + 1]);
-            tmem_st16(acc_base + c0 / 2, w);
+            pend_o = true;
+            __syncwarp();
         }
-        l_run = l_run * alpha + sum;
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float ov[32];
-                tmem_ld32(acc_base + kAttnKeys + c0, ov);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    ov[i] *= alpha;
-                tmem_st32(acc_base + kAttnKeys + c0, ov);
-            }
+        if (ok && pend_o) {
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph_o, abort));
+            if (ok)
+                pend_o = false;
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        // 6. O += P V once the value tile has landed
-        const int vb = (int)(kt & 1);
-        ok = __syncthreads_and(attn_wait(&bar_v[vb], (ph_v >> vb) & 1u));
-        if (!ok)
-            break;
-        ph_v ^= 1u << vb;
-        pend_v &= ~(1u << vb);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (tid == 0) {
-            const uint32_t v_addr = attn_smem_u32(sV + vb * kTile);
-#pragma unroll
-            for (int blk = 0; blk < kAttnBlocks; ++blk)
-#pragma unroll
-                for (int kk = 0; kk < kAttnKeys / 16; ++kk)
-                    umma_ts(tmem + blk * kBlockCols + kAttnKeys, tmem + blk * kBlockCols + kk * 8,
-                            umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128), idesc_o,
-                            (kt > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bar_o);
-        }
-        pend_o = true;
-    }
-    if (ok && pend_o) {
-        ok = __syncthreads_and(attn_wait(&bar_o, ph_o));
-        if (ok)
-            pend_o = false;
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-
-    if (!ok) {
-        // a copy or an MMA did not complete in time: report, give everything
-        // still in flight one more bounded wait, free TMEM, write nothing
-        if (tid == 0)
-            atomicOr(a.flag, 2);
-        if (pend_k)
-            (void)attn_wait(&bar_k, ph_k);
-        if (pend_s)
-            (void)attn_wait(&bar_s, ph_s);
-        if (pend_o)
-            (void)attn_wait(&bar_o, ph_o);
-        if (pend_v & 1u)
-            (void)attn_wait(&bar_v[0], ph_v & 1u);
-        if (pend_v & 2u)
-            (void)attn_wait(&bar_v[1], (ph_v >> 1) & 1u);
-    } else {
-        // epilogue: O / l for this row (zeros when no key is visible); TMEM
-        // loads are warp-wide, stores only for rows inside the sequence
-        const float inv = (n_tiles > 0 && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-        uint4 *dst = reinterpret_cast<uint4 *>(O + qi * D);
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float ov[32];
-            if (n_tiles > 0) {
-                tmem_ld32(acc_base + kAttnKeys + c0, ov);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    ov[i] = 0.0f;
-            }
-            if (qi < a.Sq) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        f[e] = ov[c * 8 + e] * inv;
-                    dst[(c0 + c * 8) / 8] = Elt<T>::pack(f);
-                }
-            }
+        if (!ok) {
+            *abort = 1;
+            // give every copy and MMA still in flight one more bounded wait
+            if (pend_k)
+                (void)attn_wait(&bar_k, ph_k);
+            if (pend_s)
+                (void)attn_wait(&bar_s, ph_s);
+            if (pend_o)
+                (void)attn_wait(&bar_o, ph_o);
+            if (pend_v & 1u)
+                (void)attn_wait(&bar_v[0], ph_v & 1u);
+            if (pend_v & 2u)
+                (void)attn_wait(&bar_v[1], (ph_v >> 1) & 1u);
         }
     }
+    // every role has left its loop; a copy or an MMA that did not complete in
+    // time is reported and nothing was written
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if (tid == 0 && abort_flag)
+        atomicOr(a.flag, 2);
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
