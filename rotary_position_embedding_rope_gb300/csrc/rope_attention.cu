@@ -537,10 +537,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *sK = sQ + kAttnBlocks * kTile;
     uint8_t *sV = sK + kTile;
     uint8_t *sT = sV + 2 * kTile;
-    // completions: key tile + table landed (TMA), S ready, O += P V done
-    // (MMA commits), value tile landed (TMA, per buffer), key tile rotated
-    // and P ready (the kMathThreads row-block threads arrive)
-    __shared__ __align__(8) uint64_t bar_k, bar_s, bar_o, bar_v[2], bar_krot, bar_p;
+    // completions: key tile + table landed (TMA), value tile landed (TMA, per
+    // buffer), S ready and O += P V done (MMA commits, per row block), key
+    // tile rotated (the kMathThreads row-block threads arrive) and P ready
+    // (the block's 128 threads arrive)
+    __shared__ __align__(8) uint64_t bar_k, bar_v[2], bar_s[2], bar_o[2], bar_krot, bar_p[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -598,12 +599,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     if (tid == 0) {
         mbar_init(&bar_k, 1);
-        mbar_init(&bar_s, 1);
-        mbar_init(&bar_o, 1);
         mbar_init(&bar_v[0], 1);
         mbar_init(&bar_v[1], 1);
+        for (int blk = 0; blk < kAttnBlocks; ++blk) {
+            mbar_init(&bar_s[blk], 1);
+            mbar_init(&bar_o[blk], 1);
+            mbar_init(&bar_p[blk], kAttnRows);
+        }
         mbar_init(&bar_krot, kMathThreads);
-        mbar_init(&bar_p, kMathThreads);
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -640,10 +643,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             rotate_key_tile<T, LAYOUT, STAGED>(sK, sT, k0, a, tid);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(&bar_krot);
-            // 2. S = Q K^T is ready; O += P V of the previous tile has finished
-            //    (the issue warp waits for it before S)
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_s, ph, abort) &&
-                                             (kt == 0 || attn_wait(&bar_o, ph ^ 1, abort)));
+            // 2. this block's S = Q K^T is ready; its O += P V of the previous
+            //    tile has finished (the issue warp waits for it before S)
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_s[j], ph, abort) &&
+                                             (kt == 0 || attn_wait(&bar_o[j], ph ^ 1, abort)));
             if (!ok)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -722,11 +725,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&bar_p);
+            mbar_arrive(&bar_p[j]);
         }
         // the last O += P V
         if (ok && n_tiles > 0)
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph ^ 1, abort));
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_o[j], ph ^ 1, abort));
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ok) {
             *abort = 1;
@@ -761,32 +764,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // ---- issue warp: TMA copies one tile ahead, the MMAs (lane 0)
         const uint32_t idesc_s = umma_idesc(128, kAttnKeys, ab_format, 0);
         const uint32_t idesc_o = umma_idesc(128, D, ab_format, 1);
-        // barriers with a copy or MMA in flight, and their next parities
-        bool pend_k = n_tiles > 0, pend_s = false, pend_o = false;
+        // copies in flight (bar_k; bar_v bit b) and the parities they complete
+        // next; every commit covers all earlier MMAs, so the last one covers them all
+        bool pend_k = n_tiles > 0, pend_mma = false;
         uint32_t pend_v = (n_tiles > 0 ? 1u : 0u) | (n_tiles > 1 ? 2u : 0u);
-        uint32_t ph_k = 0, ph_s = 0, ph_o = 0, ph_v = 0;
+        uint32_t ph_k = 0, ph_v = 0, last_ph = 0;
+        uint64_t *last_bar = &bar_s[0];
         for (int64_t kt = 0; kt < n_tiles; ++kt) {
             const int64_t k0 = kt * kAttnKeys;
             const bool next = kt + 1 < n_tiles;
-            // the key tile is rotated; the previous O += P V has finished
-            // (P, O and its value buffer are free)
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_krot, (uint32_t)(kt & 1), abort));
+            const uint32_t ph = (uint32_t)(kt & 1);
+            // the key tile is rotated
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_krot, ph, abort));
             if (!ok)
                 break;
-            if (kt > 0) {
-                ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph_o, abort));
-                if (!ok)
-                    break;
-                ph_o ^= 1;
-                pend_o = false;
-            }
             ph_k ^= 1;                             // the math warps waited for it
             pend_k = false;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // S = Q K^T for both row blocks
-            if (lane == 0) {
-#pragma unroll
-                for (int blk = 0; blk < kAttnBlocks; ++blk)
+            // S = Q K^T per row block, once the block's previous O += P V has
+            // finished (P shares S's columns)
+            for (int blk = 0; blk < kAttnBlocks; ++blk) {
+                if (kt > 0) {
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_o[blk], ph ^ 1, abort));
+                    if (!ok)
+                        break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         umma_ss(tmem + blk * kBlockCols,
@@ -795,64 +798,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 umma_desc(attn_smem_u32(sK) + (kk >> 2) * kBoxBytes + (kk & 3) * 32u,
                                           16u, 1024u, kSwizzle128),
                                 idesc_s, kk > 0);
-                umma_commit(&bar_s);
+                    umma_commit(&bar_s[blk]);
+                }
+                __syncwarp();
+                pend_mma = true;
+                last_bar = &bar_s[blk];
+                last_ph = ph;
             }
-            pend_s = true;
-            __syncwarp();
-            // the value tile after the next one, into the buffer just released
+            if (!ok)
+                break;
+            // the value tile after the next one, into the buffer both products
+            // of the previous tile have released
             if (next && kt > 0) {
                 issue_value_tile<D>(maps, sV + ((kt + 1) & 1) * kTile, (int)(k0 + kAttnKeys), zkv,
                                     &bar_v[(kt + 1) & 1], lane);
                 pend_v |= 1u << ((kt + 1) & 1);
             }
-            // S is ready: the key buffer and the table staging are free again
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_s, ph_s, abort));
+            // both S are ready: the key buffer and the table staging are free
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_s[kAttnBlocks - 1], ph, abort));
             if (!ok)
                 break;
-            ph_s ^= 1;
-            pend_s = false;
             if (next) {
                 issue_key_tile<D, STAGED>(maps, sK, sT, (int)(k0 + kAttnKeys), zkv, tboxes, &bar_k,
                                           lane);
                 pend_k = true;
             }
-            // P ready and the value tile landed: O += P V
+            // O += P V per row block as its P becomes ready
             const int vb = (int)(kt & 1);
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_p, (uint32_t)(kt & 1), abort) &&
-                                             attn_wait(&bar_v[vb], (ph_v >> vb) & 1u, abort));
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_v[vb], (ph_v >> vb) & 1u, abort));
             if (!ok)
                 break;
             ph_v ^= 1u << vb;
             pend_v &= ~(1u << vb);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (lane == 0) {
-                const uint32_t v_addr = attn_smem_u32(sV + vb * kTile);
-#pragma unroll
-                for (int blk = 0; blk < kAttnBlocks; ++blk)
+            const uint32_t v_addr = attn_smem_u32(sV + vb * kTile);
+            for (int blk = 0; blk < kAttnBlocks; ++blk) {
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_p[blk], ph, abort));
+                if (!ok)
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < kAttnKeys / 16; ++kk)
                         umma_ts(tmem + blk * kBlockCols + kAttnKeys, tmem + blk * kBlockCols + kk * 8,
                                 umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128),
                                 idesc_o, (kt > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bar_o);
+                    umma_commit(&bar_o[blk]);
+                }
+                __syncwarp();
+                last_bar = &bar_o[blk];
+                last_ph = ph;
             }
-            pend_o = true;
-            __syncwarp();
+            if (!ok)
+                break;
         }
-        if (ok && pend_o) {
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_o, ph_o, abort));
+        if (ok && pend_mma) {
+            ok = __all_sync(0xffffffffu, attn_wait(last_bar, last_ph, abort));
             if (ok)
-                pend_o = false;
+                pend_mma = false;
         }
         if (!ok) {
             *abort = 1;
             // give every copy and MMA still in flight one more bounded wait
             if (pend_k)
                 (void)attn_wait(&bar_k, ph_k);
-            if (pend_s)
-                (void)attn_wait(&bar_s, ph_s);
-            if (pend_o)
-                (void)attn_wait(&bar_o, ph_o);
+            if (pend_mma)
+                (void)attn_wait(last_bar, last_ph);
             if (pend_v & 1u)
                 (void)attn_wait(&bar_v[0], ph_v & 1u);
             if (pend_v & 2u)
