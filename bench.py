@@ -48,11 +48,13 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
                   for f in ("rope_kernels.cuh", "rope_bulk.cuh", "rope_internal.cuh", "rope_api.cu")]
+ATTN_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
+                for f in ("rope_attention.cu", "rope_kernels.cuh", "rope_internal.cuh", "rope_api.cu")]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES if sources is None else sources:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -208,9 +210,9 @@ def hbm_peak():
 KERNEL_NAMES = {1: "rope_bulk_kernel", 2: "rope_scalar_kernel", 3: "rope_vec_kernel"}
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of the rotation kernel from a committed ncu summary,
-    or None when there is none or the kernel sources changed since."""
+def profiled_traffic(kernel: str, workload: str, sources=None):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, or None
+    when there is none or the kernel sources changed since."""
     path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel, workload))
     try:
         text = open(path).read()
@@ -218,7 +220,7 @@ def profiled_traffic(kernel: str, workload: str):
         return None
     src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9,]+)", text)
-    if not src or not val or src.group(1) != kernel_source_hash():
+    if not src or not val or src.group(1) != kernel_source_hash(sources):
         return None
     return int(val.group(1).replace(",", ""))
 
@@ -447,7 +449,8 @@ def attention_arm(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "peak_source": "%s bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
-                         "traffic": None, "kernel": "rope_attn_kernel"},
+                         "traffic": profiled_traffic("rope_attn_kernel", a["name"], ATTN_SOURCES),
+                         "kernel": "rope_attn_kernel"},
             "unfused_context": unfused,
             "gpu_launches": steps,
             "clocks": sampler.summary(),
