@@ -428,8 +428,11 @@ def attention_arm(args):
         c32, s32 = O.load().tables(a["theta"], a["rotary_dim"], a["S"], 1.0, "f32")
         nq = 64
         t0 = time.perf_counter()
-        OA.attention(W.bits(q[:1, :1, :nq].cpu()), W.bits(k[:1, :1].cpu()), W.bits(v[:1, :1].cpu()),
-                     O.BF16, a["rotary_dim"], O.SPLIT_HALF, c32, s32, causal=True)
+        # the last nq query rows (at their own positions) against every key
+        pos_q = np.arange(a["S"] - nq, a["S"], dtype=np.int32)
+        OA.attention(W.bits(q[:1, :1, a["S"] - nq:].cpu()), W.bits(k[:1, :1].cpu()),
+                     W.bits(v[:1, :1].cpu()), O.BF16, a["rotary_dim"], O.SPLIT_HALF, c32, s32,
+                     pos_q=pos_q, causal=True)
         el = time.perf_counter() - t0
         sf = attention_flops(1, 1, nq, a["S"], a["D"], True)
         cpu = {"value": round(sf / el / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count() or 0,
