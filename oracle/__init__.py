@@ -20,6 +20,7 @@ LIBRARY = os.path.join(HERE, "librope_oracle.so")
 
 F32, BF16, F16, F64 = 0, 1, 2, 3
 SPLIT_HALF, INTERLEAVED = 0, 1
+FREQ_LANG, FREQ_PIXEL, FREQ_CONSTANT = 0, 1, 2
 OK, BAD_ARG, POS_OUT_OF_RANGE = 0, 1, 4
 
 # numpy container type used for the element bits of each oracle dtype
@@ -78,6 +79,19 @@ class Oracle:
             fn = getattr(lib, name)
             fn.argtypes = [c.c_double, c.c_int32, c.c_int64, c.c_double, c.c_void_p, c.c_void_p]
             fn.restype = c.c_int
+        lib.oracle_freq_ex.argtypes = [c.c_int32, c.c_double, c.c_double, c.c_int32, c.c_int32]
+        lib.oracle_freq_ex.restype = c.c_double
+        lib.oracle_position.argtypes = [c.c_int64, c.c_double, c.c_double]
+        lib.oracle_position.restype = c.c_double
+        lib.oracle_xpos_scale.argtypes = [c.c_int32, c.c_int32, c.c_double, c.c_int32, c.c_double,
+                                          c.c_double, c.c_double]
+        lib.oracle_xpos_scale.restype = c.c_double
+        for name in ("oracle_tables_ex_f64", "oracle_tables_ex_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [c.c_int32, c.c_double, c.c_double, c.c_int32, c.c_int64, c.c_double,
+                           c.c_double, c.c_int32, c.c_double, c.c_double, c.c_double, c.c_void_p,
+                           c.c_void_p]
+            fn.restype = c.c_int
         lib.oracle_rotate_row_f64.argtypes = [
             c.c_void_p, c.c_void_p, c.c_int32, c.c_int32, c.c_int32,
             c.c_void_p, c.c_void_p, c.c_int32,
@@ -127,6 +141,33 @@ class Oracle:
         rc = fn(theta, rotary_dim, max_pos, interpolate_factor, _ptr(cos), _ptr(sin))
         if rc != OK:
             raise ValueError("oracle tables: bad arguments (code %d)" % rc)
+        return cos, sin
+
+    def freq_ex(self, mode: int, theta: float, max_freq: float, rotary_dim: int, i: int) -> float:
+        return self.lib.oracle_freq_ex(mode, theta, max_freq, rotary_dim, i)
+
+    def position(self, m: int, pos_offset: float, pos_divisor: float) -> float:
+        return self.lib.oracle_position(m, pos_offset, pos_divisor)
+
+    def xpos_scale(self, rotary_dim: int, i: int, p: float, sign: int, base: float, gamma: float,
+                   center: float) -> float:
+        return self.lib.oracle_xpos_scale(rotary_dim, i, p, sign, base, gamma, center)
+
+    def tables_ex(self, mode: int, rotary_dim: int, rows: int, theta: float = 10000.0,
+                  max_freq: float = 10.0, pos_offset: float = 0.0, pos_divisor: float = 1.0,
+                  xpos_sign: int = 0, xpos_base: float = 512.0, xpos_gamma: float = 0.4,
+                  xpos_center: float = 0.0, precision: str = "f64"):
+        """cos, sin tables [rows, rotary_dim // 2] of a frequency mode, row m at
+        position pos_offset + m / pos_divisor, optionally XPOS-scaled."""
+        h = rotary_dim // 2
+        dt = np.float64 if precision == "f64" else np.float32
+        cos = np.empty((rows, h), dtype=dt)
+        sin = np.empty((rows, h), dtype=dt)
+        fn = self.lib.oracle_tables_ex_f64 if precision == "f64" else self.lib.oracle_tables_ex_f32
+        rc = fn(mode, theta, max_freq, rotary_dim, rows, pos_offset, pos_divisor, xpos_sign,
+                xpos_base, xpos_gamma, xpos_center, _ptr(cos), _ptr(sin))
+        if rc != OK:
+            raise ValueError("oracle tables_ex: bad arguments (code %d)" % rc)
         return cos, sin
 
     # --- rotation -------------------------------------------------------------

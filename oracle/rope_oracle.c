@@ -34,6 +34,10 @@
 #include <stdint.h>
 #include <string.h>
 
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
 /* Element types understood by the oracle.  ORACLE_F64 exists only so the
  * invariant tests can run the rotation with no rounding of the output. */
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_F64 = 3 };
@@ -41,6 +45,8 @@ enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_F64 = 3 };
 enum { ORACLE_SPLIT_HALF = 0, ORACLE_INTERLEAVED = 1 };
 /* Return codes. */
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_POS_OUT_OF_RANGE = 4 };
+/* frequency modes (freqs_for) */
+enum { ORACLE_FREQ_LANG = 0, ORACLE_FREQ_PIXEL = 1, ORACLE_FREQ_CONSTANT = 2 };
 
 /* ------------------------------------------------------------------------ */
 /* Exact decoding of the 16-bit storage types into fp64.                     */
@@ -193,6 +199,130 @@ int oracle_tables_f32(double theta, int32_t rotary_dim, int64_t max_pos,
                                     oracle_inv_freq(theta, rotary_dim, i));
             cos_out[m * h + i] = oracle_f64_to_f32(cos(a));
             sin_out[m * h + i] = oracle_f64_to_f32(sin(a));
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Frequency modes, row positions and the XPOS scale.                        */
+/*   [RET, RotaryEmbedding / Key Parameters] names the modes freqs_for =     */
+/*   'lang' | 'pixel' | 'constant' and use_xpos, but prints no formula.      */
+/*   The formulas restated here are the published ones:                      */
+/*   - lang: theta^(-2i/rotary_dim) (as above);                              */
+/*   - pixel: the Fourier features of Jaegle et al., "Perceiver: General     */
+/*     Perception with Iterative Attention" (ICML 2021): frequencies spaced  */
+/*     linearly from 1 to max_freq/2, times pi, for positions in [-1, 1];    */
+/*   - constant: every pair at frequency 1;                                  */
+/*   - XPOS: Sun et al., "A Length-Extrapolatable Transformer" (2022): pair  */
+/*     i carries zeta_i = (2i/rotary_dim + gamma) / (1 + gamma); the query   */
+/*     at position n is scaled by zeta_i^(n/B) and the key by zeta_i^(-n/B), */
+/*     so a query-key product depends on the distance only (gamma = 0.4,     */
+/*     B = 512 in the paper).  A common centre c (n - c) cancels likewise.   */
+/* ------------------------------------------------------------------------ */
+
+/* Frequency of pair i (h = rotary_dim/2 pairs). */
+double oracle_freq_ex(int32_t mode, double theta, double max_freq, int32_t rotary_dim, int32_t i)
+{
+    const int32_t h = rotary_dim / 2;
+    if (mode == ORACLE_FREQ_PIXEL) {
+        if (h == 1)
+            return M_PI;
+        return M_PI * (1.0 + (double)i * (max_freq / 2.0 - 1.0) / (double)(h - 1));
+    }
+    if (mode == ORACLE_FREQ_CONSTANT)
+        return 1.0;
+    return oracle_inv_freq(theta, rotary_dim, i);
+}
+
+/* Position of table row m. */
+double oracle_position(int64_t m, double pos_offset, double pos_divisor)
+{
+    return pos_offset + (double)m / pos_divisor;
+}
+
+/* XPOS scale of pair i at position p: zeta_i^(sign * (p - center) / base). */
+double oracle_xpos_scale(int32_t rotary_dim, int32_t i, double p, int32_t sign, double base,
+                         double gamma, double center)
+{
+    const double zeta = (2.0 * (double)i / (double)rotary_dim + gamma) / (1.0 + gamma);
+    return pow(zeta, (double)sign * (p - center) / base);
+}
+
+static int tables_ex_args_ok(int32_t mode, double theta, double max_freq, int32_t rotary_dim,
+                             int64_t rows, double pos_offset, double pos_divisor, int32_t xpos_sign,
+                             double xpos_base, double xpos_gamma, double xpos_center)
+{
+    if (mode != ORACLE_FREQ_LANG && mode != ORACLE_FREQ_PIXEL && mode != ORACLE_FREQ_CONSTANT)
+        return 0;
+    if (rotary_dim < 2 || (rotary_dim & 1) || rows < 0)
+        return 0;
+    if (mode == ORACLE_FREQ_LANG && !(theta > 0.0 && isfinite(theta)))
+        return 0;
+    if (mode == ORACLE_FREQ_PIXEL && !(max_freq > 0.0 && isfinite(max_freq)))
+        return 0;
+    if (!isfinite(pos_offset) || !(pos_divisor > 0.0 && isfinite(pos_divisor)))
+        return 0;
+    if (xpos_sign < -1 || xpos_sign > 1)
+        return 0;
+    if (xpos_sign != 0 && !(xpos_base > 0.0 && isfinite(xpos_base) && xpos_gamma > 0.0 &&
+                            isfinite(xpos_gamma) && isfinite(xpos_center)))
+        return 0;
+    return 1;
+}
+
+/* fp64 tables [rows, rotary_dim/2]: row m holds, for pair i,
+ *   s * cos(p_m * w_i) and s * sin(p_m * w_i),
+ * p_m = pos_offset + m / pos_divisor, w_i the mode's frequency, and s the XPOS
+ * scale (1 when xpos_sign == 0). */
+int oracle_tables_ex_f64(int32_t mode, double theta, double max_freq, int32_t rotary_dim,
+                         int64_t rows, double pos_offset, double pos_divisor, int32_t xpos_sign,
+                         double xpos_base, double xpos_gamma, double xpos_center, double *cos_out,
+                         double *sin_out)
+{
+    int32_t h, i;
+    int64_t m;
+    if (!tables_ex_args_ok(mode, theta, max_freq, rotary_dim, rows, pos_offset, pos_divisor,
+                           xpos_sign, xpos_base, xpos_gamma, xpos_center) ||
+        !cos_out || !sin_out)
+        return ORACLE_BAD_ARG;
+    h = rotary_dim / 2;
+    for (m = 0; m < rows; ++m) {
+        const double p = oracle_position(m, pos_offset, pos_divisor);
+        for (i = 0; i < h; ++i) {
+            const double a = p * oracle_freq_ex(mode, theta, max_freq, rotary_dim, i);
+            const double sc = xpos_sign == 0 ? 1.0
+                                             : oracle_xpos_scale(rotary_dim, i, p, xpos_sign,
+                                                                 xpos_base, xpos_gamma, xpos_center);
+            cos_out[m * h + i] = sc * cos(a);
+            sin_out[m * h + i] = sc * sin(a);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The same tables, each entry rounded once to fp32. */
+int oracle_tables_ex_f32(int32_t mode, double theta, double max_freq, int32_t rotary_dim,
+                         int64_t rows, double pos_offset, double pos_divisor, int32_t xpos_sign,
+                         double xpos_base, double xpos_gamma, double xpos_center, float *cos_out,
+                         float *sin_out)
+{
+    int32_t h, i;
+    int64_t m;
+    if (!tables_ex_args_ok(mode, theta, max_freq, rotary_dim, rows, pos_offset, pos_divisor,
+                           xpos_sign, xpos_base, xpos_gamma, xpos_center) ||
+        !cos_out || !sin_out)
+        return ORACLE_BAD_ARG;
+    h = rotary_dim / 2;
+    for (m = 0; m < rows; ++m) {
+        const double p = oracle_position(m, pos_offset, pos_divisor);
+        for (i = 0; i < h; ++i) {
+            const double a = p * oracle_freq_ex(mode, theta, max_freq, rotary_dim, i);
+            const double sc = xpos_sign == 0 ? 1.0
+                                             : oracle_xpos_scale(rotary_dim, i, p, xpos_sign,
+                                                                 xpos_base, xpos_gamma, xpos_center);
+            cos_out[m * h + i] = oracle_f64_to_f32(sc * cos(a));
+            sin_out[m * h + i] = oracle_f64_to_f32(sc * sin(a));
         }
     }
     return ORACLE_OK;

@@ -12,7 +12,11 @@ Independent references used here:
     comparison over the full list of finite bfloat16 / float16 values;
   * closed forms evaluated with sympy at 40 significant digits;
   * invariants of a rotation: identity at position 0, norm preservation,
-    backward after forward, relative-position property, layout permutation.
+    backward after forward, relative-position property, layout permutation;
+  * defining properties of the frequency modes and of XPOS: linear pixel
+    spacing with fixed endpoints, the constant mode's closed form, query and
+    key scales that cancel, a log-scale linear in the position, an affine
+    zeta reaching 1, and the relative-position property with scaling.
 """
 from __future__ import annotations
 
@@ -428,6 +432,160 @@ def pin_rounded_outputs_are_rne_of_f64(o):
     flat_b, flat_y = yb.reshape(-1), y64.reshape(-1)
     for j in np.random.default_rng(9).integers(0, flat_y.size, 300):
         assert flat_b[j] == _bruteforce_rne(float(flat_y[j]), "bf16")
+
+
+# --------------------------------------------------------------------------
+# frequency modes, row positions and the XPOS scale
+# ("rotary-embedding-torch", RotaryEmbedding / Key Parameters names them;
+# Perceiver's Fourier features and the XPOS paper define them)
+# --------------------------------------------------------------------------
+def pin_freq_lang_mode_is_the_plain_table(o):
+    # lang mode at positions m / f is exactly the table of rope_tables_build
+    for f in (1.0, 2.0, 3.0):
+        for prec in ("f64", "f32"):
+            c0, s0 = o.tables(1e4, 64, 50, f, prec)
+            c1, s1 = o.tables_ex(O.FREQ_LANG, 64, 50, theta=1e4, pos_divisor=f, precision=prec)
+            assert np.array_equal(c0, c1) and np.array_equal(s0, s1), (f, prec)
+
+
+def pin_freq_constant_mode_closed_form(o):
+    # every pair turns at frequency 1: the angle is the position itself
+    c, s = o.tables_ex(O.FREQ_CONSTANT, 8, 20, pos_offset=-3.5, pos_divisor=4.0)
+    for m in range(20):
+        p = -3.5 + m / 4.0
+        assert np.all(np.abs(c[m] - math.cos(p)) <= 1e-15) and np.all(np.abs(s[m] - math.sin(p)) <= 1e-15)
+    with_theta = o.tables_ex(O.FREQ_CONSTANT, 8, 20, theta=3.0, pos_offset=-3.5, pos_divisor=4.0)
+    assert np.array_equal(with_theta[0], c)            # theta plays no part
+
+
+def pin_freq_pixel_mode_spacing(o):
+    # Perceiver: frequencies spaced linearly from 1 to max_freq / 2, times pi
+    for mu, rd in ((10.0, 16), (224.0, 64), (3.0, 4)):
+        h = rd // 2
+        w = np.array([o.freq_ex(O.FREQ_PIXEL, 1e4, mu, rd, i) for i in range(h)])
+        assert abs(w[0] - math.pi) <= 1e-15 * math.pi
+        assert abs(w[-1] - math.pi * mu / 2) <= 4e-16 * math.pi * mu
+        d = np.diff(w)
+        assert np.all(np.abs(d - d[0]) <= 1e-13 * abs(w[-1])), (mu, rd)
+    assert o.freq_ex(O.FREQ_PIXEL, 1e4, 10.0, 2, 0) == math.pi      # one pair: the start
+    # max_freq 2: every frequency is pi, so positions -1 and 1 give cos = -1, sin ~ 0
+    c, s = o.tables_ex(O.FREQ_PIXEL, 8, 2, max_freq=2.0, pos_offset=-1.0, pos_divisor=0.5)
+    assert np.all(np.abs(c + 1.0) <= 1e-15) and np.all(np.abs(s) <= 1e-15)
+    # positions span [-1, 1] with divisor (rows - 1) / 2
+    assert o.position(0, -1.0, 3.5) == -1.0 and o.position(7, -1.0, 3.5) == 1.0
+
+
+def _xpos_magnitude(c, s):
+    return np.sqrt(c * c + s * s)
+
+
+def pin_xpos_identity_at_centre(o):
+    # at the centre the scale is zeta^0 = 1: the table is the unscaled one
+    base = o.tables_ex(O.FREQ_LANG, 16, 9, theta=1e4, pos_offset=0.0)
+    for sign in (1, -1):
+        xs = o.tables_ex(O.FREQ_LANG, 16, 9, theta=1e4, xpos_sign=sign, xpos_center=4.0)
+        assert np.array_equal(xs[0][4], base[0][4]) and np.array_equal(xs[1][4], base[1][4])
+
+
+def pin_xpos_query_key_scales_cancel(o):
+    # the query is scaled by zeta^(n/B) and the key by zeta^(-n/B): at one
+    # position the magnitudes multiply to 1, and the phases are the plain ones
+    kw = dict(theta=1e4, xpos_base=64.0, xpos_center=10.0)
+    cq, sq = o.tables_ex(O.FREQ_LANG, 32, 40, xpos_sign=1, **kw)
+    ck, sk = o.tables_ex(O.FREQ_LANG, 32, 40, xpos_sign=-1, **kw)
+    c0, s0 = o.tables_ex(O.FREQ_LANG, 32, 40, theta=1e4)
+    assert np.all(np.abs(_xpos_magnitude(cq, sq) * _xpos_magnitude(ck, sk) - 1.0) <= 1e-13)
+    assert np.all(np.abs(np.arctan2(sq, cq) - np.arctan2(s0, c0)) <= 1e-13)
+    # past the centre the query shrinks and the key grows (zeta < 1)
+    mq = _xpos_magnitude(cq, sq)
+    assert np.all(mq[11:] < 1.0) and np.all(mq[:10] > 1.0)
+
+
+def pin_xpos_log_scale_linear_in_position(o):
+    # log|scale| = (p - c) / B * log(zeta): linear in p, with slope 1/B
+    for B in (8.0, 512.0):
+        c, s = o.tables_ex(O.FREQ_CONSTANT, 16, 30, pos_divisor=1.0, xpos_sign=1, xpos_base=B,
+                           xpos_center=3.0)
+        L = np.log(_xpos_magnitude(c, s))                # [rows, pairs]
+        assert np.all(np.abs(np.diff(L, n=2, axis=0)) <= 1e-12)
+        # one base length past the centre, the scale is zeta itself, whatever B is
+        cB, sB = o.tables_ex(O.FREQ_CONSTANT, 16, 1, pos_offset=3.0 + B, xpos_sign=1, xpos_base=B,
+                             xpos_center=3.0)
+        z = _xpos_magnitude(cB, sB)[0]
+        if B == 8.0:
+            z8 = z
+        else:
+            assert np.all(np.abs(z - z8) <= 1e-14)
+
+
+def pin_xpos_zeta_affine_reaching_one(o):
+    # zeta_i is affine in i/rd, zeta_0 / (1 - zeta_0) = gamma, and it would
+    # reach exactly 1 at i = rd/2 (one pair past the last)
+    for rd, gamma in ((16, 0.4), (64, 0.4), (8, 1.5)):
+        h = rd // 2
+        z = np.array([o.xpos_scale(rd, i, 1.0, 1, 1.0, gamma, 0.0) for i in range(h)])
+        d = np.diff(z)
+        assert np.all(np.abs(d - d[0]) <= 1e-15), (rd, gamma)
+        assert abs(z[-1] + d[0] - 1.0) <= 1e-14
+        assert abs(z[0] / (1.0 - z[0]) - gamma) <= 1e-14
+    # the same fraction i / rd gives the same zeta
+    assert o.xpos_scale(16, 3, 1.0, 1, 1.0, 0.4, 0.0) == o.xpos_scale(32, 6, 1.0, 1, 1.0, 0.4, 0.0)
+
+
+def pin_xpos_relative_position(o):
+    # <f_q(q, m), f_k(k, n)> depends on m - n only (brute force)
+    rows, rd = 64, 16
+    kw = dict(theta=1e4, xpos_base=32.0, xpos_center=0.0)
+    cq, sq = o.tables_ex(O.FREQ_LANG, rd, rows, xpos_sign=1, **kw)
+    ck, sk = o.tables_ex(O.FREQ_LANG, rd, rows, xpos_sign=-1, **kw)
+    g = np.random.default_rng(17)
+    q, k = g.standard_normal(rd), g.standard_normal(rd)
+    for layout in (O.SPLIT_HALF, O.INTERLEAVED):
+        xq = np.broadcast_to(q, (1, 1, rows, rd)).copy()
+        xk = np.broadcast_to(k, (1, 1, rows, rd)).copy()
+        _, rq = _apply64(o, xq, rd, layout, False, False, None, cq, sq)
+        _, rk = _apply64(o, xk, rd, layout, False, False, None, ck, sk)
+        G = rq[0, 0] @ rk[0, 0].T
+        tol = 1e-11 * np.linalg.norm(q) * np.linalg.norm(k)
+        for t in range(32):
+            assert np.all(np.abs(G[t:t + 32, t:t + 32] - G[:32, :32]) <= tol), (layout, t)
+        # a plain rotation of the key breaks it
+        c0, s0 = o.tables_ex(O.FREQ_LANG, rd, rows, theta=1e4)
+        _, rk0 = _apply64(o, xk, rd, layout, False, False, None, c0, s0)
+        G0 = rq[0, 0] @ rk0[0, 0].T
+        assert np.max(np.abs(G0[5:37, 5:37] - G0[:32, :32])) > 1e-6
+
+
+def pin_tables_ex_rejects_bad_arguments(o):
+    good = dict(theta=1e4, max_freq=10.0, pos_offset=0.0, pos_divisor=1.0, xpos_sign=0,
+                xpos_base=512.0, xpos_gamma=0.4, xpos_center=0.0)
+    bad = [(3, {}), (O.FREQ_LANG, dict(theta=0.0)), (O.FREQ_PIXEL, dict(max_freq=-1.0)),
+           (O.FREQ_LANG, dict(pos_divisor=0.0)), (O.FREQ_LANG, dict(pos_offset=float("nan"))),
+           (O.FREQ_LANG, dict(xpos_sign=2)), (O.FREQ_LANG, dict(xpos_sign=1, xpos_base=0.0)),
+           (O.FREQ_LANG, dict(xpos_sign=-1, xpos_gamma=0.0))]
+    for mode, over in bad:
+        args = dict(good, **over)
+        try:
+            o.tables_ex(mode, 8, 4, **args)
+        except ValueError:
+            continue
+        raise AssertionError("accepted %r %r" % (mode, over))
+    o.tables_ex(O.FREQ_PIXEL, 8, 4, **dict(good, theta=0.0))   # theta unused by pixel mode
+
+
+def pin_tables_ex_f32_is_f64_rounded_once(o):
+    # the stored fp32 tables of every mode, scaled or not, are the fp64 ones
+    # rounded once to nearest (numpy's conversion)
+    cases = [dict(mode=O.FREQ_LANG, theta=5e5), dict(mode=O.FREQ_PIXEL, max_freq=64.0, pos_offset=-1.0,
+                                                     pos_divisor=15.5),
+             dict(mode=O.FREQ_CONSTANT, pos_offset=2.0), dict(mode=O.FREQ_LANG, xpos_sign=1, xpos_center=7.0),
+             dict(mode=O.FREQ_PIXEL, xpos_sign=-1, xpos_base=16.0, pos_divisor=3.0)]
+    for kw in cases:
+        kw = dict(kw)
+        mode = kw.pop("mode")
+        c64, s64 = o.tables_ex(mode, 32, 32, precision="f64", **kw)
+        c32, s32 = o.tables_ex(mode, 32, 32, precision="f32", **kw)
+        assert np.array_equal(c64.astype(np.float32), c32) and np.array_equal(s64.astype(np.float32), s32), kw
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

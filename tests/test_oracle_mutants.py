@@ -51,6 +51,26 @@ MUTANTS = [
                          "                                   (const char *)x_in + (row + d) * es, es);",
                          "else store_elem(y_bits, dtype, row + d, 0.0);")]),
     ("tail_dropped_f64", [("for (d = rotary_dim; d < D; ++d)\n        y[d] = x[d];", "")]),
+    # frequency modes, row positions, XPOS
+    ("pixel_without_pi", [("return M_PI * (1.0 + (double)i", "return (1.0 + (double)i")]),
+    ("pixel_spacing_over_h", [("/ (double)(h - 1));", "/ (double)h);")]),
+    ("pixel_max_freq_not_halved", [("(max_freq / 2.0 - 1.0)", "(max_freq - 1.0)")]),
+    ("constant_mode_uses_theta", [("if (mode == ORACLE_FREQ_CONSTANT)\n        return 1.0;",
+                                   "if (mode == ORACLE_FREQ_CONSTANT)\n        return theta;")]),
+    ("position_multiplies_divisor", [("return pos_offset + (double)m / pos_divisor;",
+                                      "return pos_offset + (double)m * pos_divisor;")]),
+    ("position_offset_ignored", [("return pos_offset + (double)m / pos_divisor;",
+                                  "return (double)m / pos_divisor;")]),
+    ("xpos_zeta_denominator", [("+ gamma) / (1.0 + gamma);", "+ gamma) / (2.0 + gamma);")]),
+    ("xpos_zeta_over_half_dim", [("(2.0 * (double)i / (double)rotary_dim + gamma)",
+                                  "((double)i / (double)rotary_dim + gamma)")]),
+    ("xpos_sign_ignored", [("pow(zeta, (double)sign * (p - center) / base)", "pow(zeta, (p - center) / base)")]),
+    ("xpos_centre_ignored", [("pow(zeta, (double)sign * (p - center) / base)", "pow(zeta, (double)sign * p / base)")]),
+    ("xpos_base_multiplies", [("pow(zeta, (double)sign * (p - center) / base)",
+                               "pow(zeta, (double)sign * (p - center) * base)")]),
+    ("xpos_sine_unscaled_f64", [("sin_out[m * h + i] = sc * sin(a);", "sin_out[m * h + i] = sin(a);")]),
+    ("xpos_f32_unscaled", [("cos_out[m * h + i] = oracle_f64_to_f32(sc * cos(a));",
+                            "cos_out[m * h + i] = oracle_f64_to_f32(cos(a));")]),
 ]
 
 RUNNER = r"""
