@@ -469,6 +469,97 @@ def attention_arm(args):
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
+# --------------------------------------------------------------------------
+# XPOS rotation (--op xpos): frequency tables with the query/key scale folded in
+# --------------------------------------------------------------------------
+XPOS_SCALE_BASE = 512.0
+
+
+def xpos_arm(args):
+    """Llama-shaped layer with XPOS: Q rotated with the +1 table and K with the
+    -1 table (one launch each), forward and backward, in place."""
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from rotary_position_embedding_rope_gb300 import _build
+    if local == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    import rotary_position_embedding_rope_gb300 as R
+
+    w = W.BY_NAME[DEFAULT_WORKLOAD]
+    stream = torch.cuda.current_stream(device)
+    kw = dict(theta=w.theta, xpos_scale_base=XPOS_SCALE_BASE, xpos_center=w.table_rows / 2,
+              device=device, stream=stream)
+    tq = R.build_tables_ex("lang", w.rotary_dim, w.table_rows, xpos_sign=1, **kw)
+    tk = R.build_tables_ex("lang", w.rotary_dim, w.table_rows, xpos_sign=-1, **kw)
+    g = torch.Generator().manual_seed(w.seed)
+    nsets = 2
+    sets = []
+    for _ in range(nsets):
+        q = W.draw((w.B, w.Hq, w.S, w.D), w.dtype, g).to(device)
+        k = W.draw((w.B, w.Hk, w.S, w.D), w.dtype, g).to(device)
+        sets.append((q, k, q.clone(), k.clone()))
+
+    def step(i):
+        q, k, dq, dk = sets[i % nsets]
+        R.apply_qk_xpos(q, k, tq, tk, stream=stream)
+        R.apply_qk_xpos(dq, dk, tq, tk, backward=True, stream=stream)
+
+    warmup = max(3, args.warmup)
+    steps = max(1, min(args.steps, 1000))
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+    ms = e0.elapsed_time(e1)
+    # per direction: the fused call's bytes plus one more table (Q and K each
+    # read their own)
+    table = w.S * (w.rotary_dim // 2) * 4 * 2
+    bytes_step = 2 * (W.algorithmic_bytes(w) + table)
+    max_ms, all_bytes = aggregate(dist, device, ms, bytes_step * steps)
+    value = all_bytes / (max_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    if rank == 0:
+        line = {
+            "metric": "XPOS rotation of Q and K, fwd/bwd achieved HBM GB/s", "op": "xpos",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(max_ms / steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "q_shape": [w.B, w.Hq, w.S, w.D],
+                       "k_shape": [w.B, w.Hk, w.S, w.D], "tables": "lang theta=%g, XPOS base %g "
+                       "centre %g, +1 for Q, -1 for K" % (w.theta, XPOS_SCALE_BASE, w.table_rows / 2),
+                       "step": "Q and K forward, dQ and dK backward: 4 launches",
+                       "bytes_per_step": bytes_step,
+                       "l2": "inputs larger than L2: %d rotating sets of Q,K,dQ,dK" % nsets},
+            "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(value / world / peak, 4),
+                         "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+                         "traffic": None, "kernel": "rope_vec_kernel"},
+            "gpu_launches": 4 * steps,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,10 +569,17 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", choices=["rope", "attention"], default="rope",
+    ap.add_argument("--op", choices=["rope", "attention", "xpos"], default="rope",
                     help="rope: the fused Q+K rotation (default); attention: attention with the "
-                         "rotation fused into the Q/K tile loads")
+                         "rotation fused into the Q/K tile loads; xpos: the rotation with XPOS "
+                         "tables, one launch per tensor")
     args = ap.parse_args()
+    if args.op == "xpos":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "xpos",
+                              "unavailable": "the reference arm times the rotation only"}))
+            return 0
+        return xpos_arm(args)
     if args.op == "attention":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": "attention",

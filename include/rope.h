@@ -53,6 +53,8 @@ typedef enum {
 
 typedef enum { ROPE_SPLIT_HALF = 0, ROPE_INTERLEAVED = 1 } rope_layout;
 typedef enum { ROPE_F32 = 0, ROPE_BF16 = 1, ROPE_F16 = 2 } rope_dtype;
+/* frequency modes ("rotary-embedding-torch", RotaryEmbedding: freqs_for) */
+typedef enum { ROPE_FREQ_LANG = 0, ROPE_FREQ_PIXEL = 1, ROPE_FREQ_CONSTANT = 2 } rope_freq_mode;
 
 /*
  * rope_tables_build -- fill the cos/sin table.
@@ -76,6 +78,45 @@ typedef enum { ROPE_F32 = 0, ROPE_BF16 = 1, ROPE_F16 = 2 } rope_dtype;
 rope_status rope_tables_build(double theta, int32_t rotary_dim, int64_t max_pos,
                               double interpolate_factor, float *cos_out, float *sin_out,
                               void *stream);
+
+/*
+ * rope_tables_build_ex -- the cos/sin table of a frequency mode, at given
+ * row positions, optionally with the XPOS scale folded in.
+ *
+ * Source: "rotary-embedding-torch", RotaryEmbedding / Key Parameters names
+ * freqs_for = 'lang' (default) | 'pixel' | 'constant' and use_xpos (length
+ * extrapolation) without formulas; the published definitions are used.  For
+ * row m and pair i (0 <= i < h = rotary_dim/2):
+ *     p     = pos_offset + m / pos_divisor
+ *     w_i   = theta^(-2i / rotary_dim)                     ROPE_FREQ_LANG
+ *           = pi * (1 + i * (max_freq/2 - 1) / (h - 1))    ROPE_FREQ_PIXEL
+ *             (pi when h = 1; Perceiver's Fourier features, positions
+ *             usually in [-1, 1]: pos_offset = -1, pos_divisor = (rows-1)/2)
+ *           = 1                                            ROPE_FREQ_CONSTANT
+ *     s     = 1 when xpos_sign = 0, else (XPOS, Sun et al. 2022)
+ *             zeta_i^(xpos_sign * (p - xpos_center) / xpos_scale_base),
+ *             zeta_i = (2i/rotary_dim + xpos_gamma) / (1 + xpos_gamma)
+ *     cos_out[m][i] = s * cos(p * w_i), sin_out[m][i] = s * sin(p * w_i),
+ * all in fp64, each stored rounded once to fp32.  XPOS scales the query by
+ * zeta^(+n/B) and the key by zeta^(-n/B): build one table with xpos_sign =
+ * +1 for Q and one with -1 for K and rotate each with rope_apply_q (the
+ * backward flag, which negates the sine, then gives the XPOS gradient too).
+ * ROPE_FREQ_LANG with pos_offset = 0 and pos_divisor = interpolate_factor
+ * reproduces rope_tables_build bit for bit.
+ *
+ * cos_out, sin_out: device, caller-owned, float[rows * rotary_dim/2] each.
+ * Errors: ROPE_ERR_UNSUPPORTED for an unknown mode; ROPE_ERR_INVALID_ARG if
+ *   rotary_dim < 2 or odd, rows < 0, theta <= 0 (lang), max_freq <= 0
+ *   (pixel), pos_divisor <= 0, a non-finite pos_offset / pos_divisor,
+ *   xpos_sign outside {-1, 0, 1}, and with xpos_sign != 0 a scale base or
+ *   gamma <= 0 or a non-finite centre; null or overlapping outputs with
+ *   rows > 0.  rows = 0 is a no-op.  ROPE_ERR_CUDA if the launch fails.
+ */
+rope_status rope_tables_build_ex(int32_t freq_mode, double theta, double max_freq,
+                                 int32_t rotary_dim, int64_t rows, double pos_offset,
+                                 double pos_divisor, int32_t xpos_sign, double xpos_scale_base,
+                                 double xpos_gamma, double xpos_center, float *cos_out,
+                                 float *sin_out, void *stream);
 
 /*
  * rope_apply_qk -- rotate Q and K in place, in one launch.

@@ -29,7 +29,8 @@ __all__ = [
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
     "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
-    "attention",
+    "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
+    "build_tables_ex", "apply_qk_xpos",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
@@ -37,6 +38,8 @@ __all__ = [
 VARIANT_BULK, VARIANT_ELEMENTWISE, VARIANT_VECTOR = 1, 2, 3
 ROPE_SPLIT_HALF, ROPE_INTERLEAVED = 0, 1
 ROPE_F32, ROPE_BF16, ROPE_F16 = 0, 1, 2
+ROPE_FREQ_LANG, ROPE_FREQ_PIXEL, ROPE_FREQ_CONSTANT = 0, 1, 2
+_FREQ_CODE = {"lang": ROPE_FREQ_LANG, "pixel": ROPE_FREQ_PIXEL, "constant": ROPE_FREQ_CONSTANT}
 _DTYPE_CODE = {torch.float32: ROPE_F32, torch.bfloat16: ROPE_BF16, torch.float16: ROPE_F16}
 _LAYOUT_CODE = {"split_half": ROPE_SPLIT_HALF, "interleaved": ROPE_INTERLEAVED}
 
@@ -69,6 +72,10 @@ def load_library() -> ctypes.CDLL:
     P = c.c_void_p
     lib.rope_tables_build.argtypes = [c.c_double, c.c_int32, c.c_int64, c.c_double, P, P, P]
     lib.rope_tables_build.restype = c.c_int
+    lib.rope_tables_build_ex.argtypes = [c.c_int32, c.c_double, c.c_double, c.c_int32, c.c_int64,
+                                         c.c_double, c.c_double, c.c_int32, c.c_double, c.c_double,
+                                         c.c_double, P, P, P]
+    lib.rope_tables_build_ex.restype = c.c_int
     lib.rope_apply_qk.argtypes = [P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32, c.c_int64,
                                   c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
                                   c.c_int32, c.c_int64, P]
@@ -146,6 +153,22 @@ def rope_tables_build(theta, rotary_dim, max_pos, interpolate_factor, cos_out, s
     _check(st, "rope_tables_build")
 
 
+def rope_tables_build_ex(freq_mode, theta, max_freq, rotary_dim, rows, pos_offset, pos_divisor,
+                         xpos_sign, xpos_scale_base, xpos_gamma, xpos_center, cos_out, sin_out,
+                         stream=None):
+    lib = load_library()
+    for t, n in ((cos_out, "cos_out"), (sin_out, "sin_out")):
+        if isinstance(t, torch.Tensor) and (t.dtype != torch.float32 or
+                                            t.numel() < rows * (rotary_dim // 2)):
+            raise ValueError("%s must be float32 with at least rows*rotary_dim/2 elements" % n)
+    st = lib.rope_tables_build_ex(int(freq_mode), float(theta), float(max_freq), int(rotary_dim),
+                                  int(rows), float(pos_offset), float(pos_divisor), int(xpos_sign),
+                                  float(xpos_scale_base), float(xpos_gamma), float(xpos_center),
+                                  _addr(cos_out, "cos_out"), _addr(sin_out, "sin_out"),
+                                  _stream(stream))
+    _check(st, "rope_tables_build_ex")
+
+
 def rope_apply_qk(q, k, cos, sin, pos_idx, B, Hq, Hk, S, D, rotary_dim, layout,
                   seq_before_head, backward, dtype, table_rows, stream=None):
     lib = load_library()
@@ -216,6 +239,24 @@ def build_tables(theta: float, rotary_dim: int, max_pos: int, interpolate_factor
     return cos, sin
 
 
+def build_tables_ex(freqs_for: str, rotary_dim: int, rows: int, theta: float = 10000.0,
+                    max_freq: float = 10.0, pos_offset: float = 0.0, pos_divisor: float = 1.0,
+                    xpos_sign: int = 0, xpos_scale_base: float = 512.0, xpos_gamma: float = 0.4,
+                    xpos_center: float = 0.0, device=None, stream=None):
+    """Allocate and fill fp32 cos/sin tables [rows, rotary_dim // 2] of the mode
+    ``freqs_for`` ('lang', 'pixel' or 'constant'), row m at position
+    pos_offset + m / pos_divisor, XPOS-scaled when xpos_sign is +1 (queries) or
+    -1 (keys)."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    h = rotary_dim // 2
+    cos = torch.empty((rows, h), dtype=torch.float32, device=device)
+    sin = torch.empty((rows, h), dtype=torch.float32, device=device)
+    rope_tables_build_ex(_FREQ_CODE[freqs_for], theta, max_freq, rotary_dim, rows, pos_offset,
+                         pos_divisor, xpos_sign, xpos_scale_base, xpos_gamma, xpos_center, cos,
+                         sin, stream)
+    return cos, sin
+
+
 def _shape4(x: torch.Tensor, seq_before_head: bool):
     if x.dim() != 4:
         raise ValueError("expected a 4-D tensor, got shape %s" % (tuple(x.shape),))
@@ -275,6 +316,19 @@ def apply_q(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
     rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rd, _LAYOUT_CODE[layout],
                  int(seq_before_head), int(backward), _DTYPE_CODE[x.dtype], cos.shape[0], stream)
     return x
+
+
+def apply_qk_xpos(q: torch.Tensor, k: torch.Tensor, tables_q, tables_k,
+                  pos_idx: torch.Tensor | None = None, rotary_dim: int | None = None,
+                  layout: str = "split_half", seq_before_head: bool = False,
+                  backward: bool = False, stream=None):
+    """XPOS: rotate Q with its table (xpos_sign +1) and K with its table
+    (xpos_sign -1), in place: one launch per tensor."""
+    apply_q(q, tables_q[0], tables_q[1], pos_idx, rotary_dim, layout, seq_before_head, backward,
+            stream)
+    apply_q(k, tables_k[0], tables_k[1], pos_idx, rotary_dim, layout, seq_before_head, backward,
+            stream)
+    return q, k
 
 
 def _positions(pos_idx, B: int, S: int):

@@ -85,6 +85,41 @@ __global__ void rope_table_kernel(double theta, int32_t rotary_dim, int64_t max_
     }
 }
 
+// Tables of a frequency mode at row positions pos_offset + m / pos_divisor,
+// scaled by zeta_i^(xpos_sign (p - centre) / base) when xpos_sign != 0 (the
+// XPOS query/key scale folded into the table).  One column per thread: the
+// frequency and zeta are computed once, then fp64 sincos and pow per entry.
+__global__ void rope_table_ex_kernel(int32_t mode, double theta, double max_freq,
+                                     int32_t rotary_dim, int64_t rows, double pos_offset,
+                                     double pos_divisor, int32_t xpos_sign, double xpos_base,
+                                     double xpos_gamma, double xpos_center, float *cos_out,
+                                     float *sin_out)
+{
+    const int32_t h = rotary_dim / 2;
+    const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= h)
+        return;
+    double w;
+    if (mode == ROPE_FREQ_PIXEL)
+        w = h == 1 ? M_PI : M_PI * (1.0 + (double)i * (max_freq / 2.0 - 1.0) / (double)(h - 1));
+    else if (mode == ROPE_FREQ_CONSTANT)
+        w = 1.0;
+    else
+        w = pow(theta, -(2.0 * (double)i) / (double)rotary_dim);
+    const double zeta = (2.0 * (double)i / (double)rotary_dim + xpos_gamma) / (1.0 + xpos_gamma);
+    for (int64_t m = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; m < rows;
+         m += (int64_t)gridDim.y * blockDim.y) {
+        const double p = pos_offset + (double)m / pos_divisor;
+        const double angle = p * w;
+        const double sc =
+            xpos_sign == 0 ? 1.0 : pow(zeta, (double)xpos_sign * (p - xpos_center) / xpos_base);
+        double sv, cv;
+        sincos(angle, &sv, &cv);
+        cos_out[m * h + i] = __double2float_rn(sc * cv);
+        sin_out[m * h + i] = __double2float_rn(sc * sv);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Argument checks and kernel choice (host only; no CUDA calls).
 // ---------------------------------------------------------------------------
@@ -280,6 +315,46 @@ rope_status rope_tables_build(double theta, int32_t rotary_dim, int64_t max_pos,
     const dim3 grid((unsigned)((h + 31) / 32), (unsigned)(rows_blocks < 8192 ? rows_blocks : 8192));
     rope_table_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
         theta, rotary_dim, max_pos, interpolate_factor, cos_out, sin_out);
+    return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA;
+}
+
+rope_status rope_tables_build_ex(int32_t freq_mode, double theta, double max_freq,
+                                 int32_t rotary_dim, int64_t rows, double pos_offset,
+                                 double pos_divisor, int32_t xpos_sign, double xpos_scale_base,
+                                 double xpos_gamma, double xpos_center, float *cos_out,
+                                 float *sin_out, void *stream)
+{
+    if (freq_mode != ROPE_FREQ_LANG && freq_mode != ROPE_FREQ_PIXEL &&
+        freq_mode != ROPE_FREQ_CONSTANT)
+        return ROPE_ERR_UNSUPPORTED;
+    if (rotary_dim < 2 || (rotary_dim & 1) || rows < 0)
+        return ROPE_ERR_INVALID_ARG;
+    if (freq_mode == ROPE_FREQ_LANG && !(theta > 0.0 && std::isfinite(theta)))
+        return ROPE_ERR_INVALID_ARG;
+    if (freq_mode == ROPE_FREQ_PIXEL && !(max_freq > 0.0 && std::isfinite(max_freq)))
+        return ROPE_ERR_INVALID_ARG;
+    if (!std::isfinite(pos_offset) || !(pos_divisor > 0.0 && std::isfinite(pos_divisor)))
+        return ROPE_ERR_INVALID_ARG;
+    if (xpos_sign < -1 || xpos_sign > 1)
+        return ROPE_ERR_INVALID_ARG;
+    if (xpos_sign != 0 &&
+        !(xpos_scale_base > 0.0 && std::isfinite(xpos_scale_base) && xpos_gamma > 0.0 &&
+          std::isfinite(xpos_gamma) && std::isfinite(xpos_center)))
+        return ROPE_ERR_INVALID_ARG;
+    if (rows == 0)
+        return ROPE_OK;
+    const int64_t h = rotary_dim / 2;
+    int64_t n = 0, bytes = 0;
+    if (!mul_ok(rows, h, &n) || !mul_ok(n, 4, &bytes))
+        return ROPE_ERR_INVALID_ARG;
+    if (cos_out == nullptr || sin_out == nullptr || ranges_overlap(cos_out, bytes, sin_out, bytes))
+        return ROPE_ERR_INVALID_ARG;
+    const dim3 block(32, 8);
+    const int64_t rows_blocks = (rows + block.y - 1) / block.y;
+    const dim3 grid((unsigned)((h + 31) / 32), (unsigned)(rows_blocks < 8192 ? rows_blocks : 8192));
+    rope_table_ex_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
+        freq_mode, theta, max_freq, rotary_dim, rows, pos_offset, pos_divisor, xpos_sign,
+        xpos_scale_base, xpos_gamma, xpos_center, cos_out, sin_out);
     return cudaGetLastError() == cudaSuccess ? ROPE_OK : ROPE_ERR_CUDA;
 }
 

@@ -121,6 +121,39 @@ def test_tables_build_rejects_bad_arguments(lib, theta, rd, max_pos, f, cos, sin
     assert lib.rope_tables_build(theta, rd, max_pos, f, cos, sin, None) == status
 
 
+TEX = dict(mode=0, theta=1e4, max_freq=10.0, rd=64, rows=16, off=0.0, div=1.0, sign=0, base=512.0,
+           gamma=0.4, centre=0.0, cos=A16 * 2000, sin=A16 * 3000)
+
+
+def tex_args(**over):
+    a = dict(TEX, **over)
+    return (a["mode"], a["theta"], a["max_freq"], a["rd"], a["rows"], a["off"], a["div"], a["sign"],
+            a["base"], a["gamma"], a["centre"], a["cos"], a["sin"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(mode=3), R.ROPE_ERR_UNSUPPORTED),
+    (dict(mode=-1), R.ROPE_ERR_UNSUPPORTED),
+    (dict(rd=7), R.ROPE_ERR_INVALID_ARG),
+    (dict(rd=0), R.ROPE_ERR_INVALID_ARG),
+    (dict(rows=-1), R.ROPE_ERR_INVALID_ARG),
+    (dict(theta=0.0), R.ROPE_ERR_INVALID_ARG),            # lang needs theta > 0
+    (dict(mode=1, max_freq=0.0), R.ROPE_ERR_INVALID_ARG),  # pixel needs max_freq > 0
+    (dict(div=0.0), R.ROPE_ERR_INVALID_ARG),
+    (dict(div=float("inf")), R.ROPE_ERR_INVALID_ARG),
+    (dict(off=float("nan")), R.ROPE_ERR_INVALID_ARG),
+    (dict(sign=2), R.ROPE_ERR_INVALID_ARG),
+    (dict(sign=1, base=0.0), R.ROPE_ERR_INVALID_ARG),
+    (dict(sign=-1, gamma=0.0), R.ROPE_ERR_INVALID_ARG),
+    (dict(sign=1, centre=float("inf")), R.ROPE_ERR_INVALID_ARG),
+    (dict(cos=None), R.ROPE_ERR_INVALID_ARG),
+    (dict(sin=A16 * 2000), R.ROPE_ERR_INVALID_ARG),        # outputs overlap
+    (dict(rows=0, cos=None, sin=None), R.ROPE_OK),         # empty: no-op
+])
+def test_tables_build_ex_rejects_bad_arguments(lib, over, status):
+    assert lib.rope_tables_build_ex(*tex_args(**over)) == status
+
+
 @pytest.mark.parametrize("over,variant", [
     (dict(), 3),                                   # bf16 split-half, rd*2 = 128 B: vectorised
     (dict(layout=1), 3),
