@@ -215,6 +215,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
         v[i] = __uint_as_float(r[i]);
 }
 
+// Like tmem_ld32 but without the wait: several loads can be in flight
+// before one tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t addr, float *v)
+{
+    uint32_t *r = reinterpret_cast<uint32_t *>(v);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -657,19 +675,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 vis_end = qi + shift + 1;
             const int64_t nv = vis_end - k0;
             const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
-            float mx = -INFINITY;
             const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
+            // S is read in halves of 64 columns, two loads in flight per wait
+            constexpr int kHalf = kAttnKeys / 2;
+            float mx = -INFINITY;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
-                float sv[32];
-                tmem_ld32(acc_base + c0, sv);
+            for (int c0 = 0; c0 < kAttnKeys; c0 += kHalf) {
+                float sv[kHalf];
+                tmem_ld32_nowait(acc_base + c0, sv);
+                tmem_ld32_nowait(acc_base + c0 + 32, sv + 32);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < kHalf; ++i)
                         mx = fmaxf(mx, sv[i]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < kHalf; ++i)
                         if (c0 + i < nvis)
                             mx = fmaxf(mx, sv[i]);
                 }
@@ -686,30 +708,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float m_new = m_ref;
             float sum = 0.0f;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kAttnKeys; c0 += 32) {
-                float sv[32];
-                tmem_ld32(acc_base + c0, sv);
-                float pv[32];
+            for (int c0 = 0; c0 < kAttnKeys; c0 += kHalf) {
+                float sv[kHalf];
+                tmem_ld32_nowait(acc_base + c0, sv);
+                tmem_ld32_nowait(acc_base + c0 + 32, sv + 32);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                uint32_t w[kHalf / 2];
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        pv[i] = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
-                        sum += pv[i];
+                    for (int i = 0; i < kHalf; i += 2) {
+                        const float p0 = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
+                        const float p1 = fast_exp2(fmaf(sv[i + 1], a.scale_log2, -m_new));
+                        sum += p0 + p1;
+                        w[i / 2] = Elt<T>::f2_to_word(p0, p1);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        pv[i] = c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
-                        sum += pv[i];
+                    for (int i = 0; i < kHalf; i += 2) {
+                        const float p0 =
+                            c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
+                        const float p1 =
+                            c0 + i + 1 < nvis ? fast_exp2(fmaf(sv[i + 1], a.scale_log2, -m_new)) : 0.0f;
+                        sum += p0 + p1;
+                        w[i / 2] = Elt<T>::f2_to_word(p0, p1);
                     }
                 }
-                // keys c0 .. c0 + 31 -> columns c0 / 2 .. c0 / 2 + 15, all of
+                // keys c0 .. c0 + 63 -> columns c0 / 2 .. c0 / 2 + 31, all of
                 // which this thread has already read
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = Elt<T>::f2_to_word(pv[2 * i], pv[2 * i + 1]);
-                tmem_st16(acc_base + c0 / 2, w);
+                tmem_st16(acc_base + c0 / 2, *reinterpret_cast<const uint32_t(*)[16]>(w));
+                tmem_st16(acc_base + c0 / 2 + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
             }
             l_run = l_run * alpha + sum;
             if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
