@@ -985,10 +985,19 @@ static cudaError_t launch_attn_kernel(const AttnArgs &a, const AttnMaps &maps, i
     const dim3 grid((unsigned)(pair_heads ? qtiles : (qtiles + 1) / 2), (unsigned)heads);
     auto kernel = rope_attn_kernel<T, LAYOUT, D, STAGED>;
     const size_t smem = attn_smem_bytes(D);
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    // the shared-memory limit is raised once per kernel instance and device
+    static std::atomic<uint64_t> raised{0};       // bit d: done on device d (d < 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit == 0 || !(raised.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        raised.fetch_or(bit, std::memory_order_acq_rel);
+    }
     kernel<<<grid, kAttnThreads, smem, st>>>(a, maps, pair_heads);
     return cudaGetLastError();
 }

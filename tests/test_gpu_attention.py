@@ -53,6 +53,8 @@ CASES = [
     # odd group (3): pairs of query tiles, the last CTA's second block past Sq
     dict(B=2, Hq=6, Hk=2, Sq=300, Sk=300, D=64, rd=32, dtype="f16", layout="split_half", causal=False),
     dict(B=1, Hq=3, Hk=1, Sq=257, Sk=390, D=128, rd=64, dtype="bf16", layout="interleaved", causal=True),
+    # interleaved, full rotary span: table chunks from the second staged table box
+    dict(B=1, Hq=4, Hk=1, Sq=300, Sk=300, D=128, rd=128, dtype="bf16", layout="interleaved", causal=True),
 ]
 
 
