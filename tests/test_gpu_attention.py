@@ -127,3 +127,41 @@ def test_attention_gathered_positions_interleaved():
                     causal=False)
     assert R.rope_check_errors() == R.ROPE_OK
     _check(o, q, k, v, "f16", 64, O.INTERLEAVED, c32, s32, pq, pk, False, "gathered positions")
+
+
+def _fuzz_cases(n=24, seed=2024):
+    g = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        D = int(g.choice([64, 128]))
+        Hk = int(g.integers(1, 4))
+        cases.append(dict(
+            i=i, B=int(g.integers(1, 3)), Hk=Hk, Hq=Hk * int(g.integers(1, 5)), D=D,
+            rd=16 * int(g.integers(1, D // 16 + 1)), layout=str(g.choice(["split_half", "interleaved"])),
+            dtype=str(g.choice(["bf16", "f16"])), Sq=int(g.integers(1, 400)), Sk=int(g.integers(1, 400)),
+            causal=bool(g.integers(0, 2)), pos=str(g.choice(["none", "none", "random"])),
+            seed=int(g.integers(0, 2 ** 31))))
+    return cases
+
+
+@pytest.mark.parametrize("c", _fuzz_cases(), ids=lambda c: "fuzz%02d" % c["i"])
+def test_attention_fuzz(c):
+    """Seeded random shapes, spans, layouts, types, masks and positions."""
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], c["seed"])
+    g = np.random.default_rng(c["seed"])
+    rows = max(c["Sq"], c["Sk"]) + 16
+    pq = pk = None
+    if c["pos"] == "random":
+        pq = g.integers(-1, rows, c["Sq"]).astype(np.int32)
+        pk = g.integers(-1, rows, c["Sk"]).astype(np.int32)
+    c32, s32 = oracle_tables(1e4, c["rd"], rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg,
+                    pos_q=None if pq is None else torch.from_numpy(pq).cuda(),
+                    pos_k=None if pk is None else torch.from_numpy(pk).cuda(),
+                    rotary_dim=c["rd"], layout=c["layout"], causal=c["causal"])
+    assert R.rope_check_errors() == R.ROPE_OK
+    _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, pq, pk, c["causal"],
+           str(c))

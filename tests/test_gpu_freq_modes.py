@@ -166,3 +166,34 @@ def test_attention_with_pixel_tables():
     got = out.float().cpu().numpy().astype(np.float64)
     tol = 2.0 ** -8 * (float(v.float().abs().max()) + np.abs(ref))
     assert np.all(np.abs(got - ref) <= tol)
+
+
+def _table_fuzz(n=16, seed=77):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        mode = str(g.choice(["lang", "pixel", "constant"]))
+        c = dict(mode=mode, rd=2 * int(g.integers(1, 65)), rows=int(g.integers(1, 3000)),
+                 pos_offset=float(g.uniform(-100, 100)), pos_divisor=float(g.uniform(0.25, 8.0)))
+        if mode == "lang":
+            c["theta"] = float(10 ** g.uniform(2, 6))
+        if mode == "pixel":
+            c["max_freq"] = float(g.uniform(1.0, 256.0))
+        if g.integers(0, 2):
+            # a base of at least the rows' largest distance from the centre keeps
+            # the scale within [zeta, 1 / zeta], inside fp32's range
+            centre = float(g.uniform(-50, 50))
+            p_lo = c["pos_offset"]
+            p_hi = c["pos_offset"] + (c["rows"] - 1) / c["pos_divisor"]
+            reach = max(abs(p_lo - centre), abs(p_hi - centre), 1.0)
+            c.update(xpos_sign=int(g.choice([-1, 1])), xpos_scale_base=reach * float(g.uniform(1, 4)),
+                     xpos_gamma=float(g.uniform(0.1, 2.0)), xpos_center=centre)
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("c", _table_fuzz(), ids=lambda c: "%s_rd%d_rows%d_x%d" % (
+    c["mode"], c["rd"], c["rows"], c.get("xpos_sign", 0)))
+def test_tables_ex_fuzz(c):
+    """Seeded random modes, widths, positions and XPOS parameters."""
+    test_tables_ex_match_oracle(c)
