@@ -20,6 +20,11 @@ is the bytes all ranks moved divided by the slowest rank's time.
 ``--impl reference`` times the plain CPU oracle on this host's cores (the
 pages publish no runnable implementation), on a bounded sample of the same
 workload per step.
+
+Two more operations have their own lines (not the contract line):
+``--op attention`` times the attention with fused rotation (TFLOP/s on the
+visible causal pairs of a Llama-3-8B-shaped prefill), ``--op xpos`` the
+rotation with XPOS tables (one launch per tensor).
 """
 from __future__ import annotations
 

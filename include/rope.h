@@ -211,7 +211,8 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
  *    [B, Hq, Sq, D], written; all of `dtype` (ROPE_BF16 or ROPE_F16), dense.
  *    Hq must be a multiple of Hk (GQA/MQA: query head h uses key/value head
  *    h / (Hq/Hk)).
- * cos, sin: the rotation table (rope_tables_build), [table_rows, rotary_dim/2].
+ * cos, sin: the rotation table (rope_tables_build or rope_tables_build_ex, any
+ *    frequency mode), [table_rows, rotary_dim/2].
  * pos_q, pos_k: device int32 [Sq], [Sk] or NULL (row = index); -1 leaves a
  *    token unrotated (pos_mask); other out-of-range values are not rotated and
  *    raise the flag that rope_check_errors reports.
@@ -225,8 +226,12 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
  *    P v product (fp32 accumulation), o is rounded once.
  * Errors: ROPE_ERR_UNSUPPORTED for other dtypes, D, rotary_dim, layouts or
  *    pointers not 16-byte aligned; ROPE_ERR_INVALID_ARG for bad sizes, null
- *    pointers, o overlapping an input; ROPE_ERR_CUDA if the launch fails.
- *    B, Hq or Sq zero: nothing to do, ROPE_OK.  Asynchronous on `stream`.
+ *    pointers, o overlapping an input; ROPE_ERR_CUDA if the launch fails,
+ *    which includes more than 65535 (batch, query-head pair) units -- B *
+ *    Hq / 2 when Hq / Hk is even, else B * Hq.  B, Hq or Sq zero: nothing to
+ *    do, ROPE_OK.  Asynchronous on `stream`; rope_check_errors later reports
+ *    out-of-range positions and, should a wait inside the kernel expire (about
+ *    2 s; o is then not written), ROPE_ERR_KERNEL_TIMEOUT.
  */
 rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void *o,
                                const float *cos, const float *sin, const int32_t *pos_q,
@@ -239,8 +244,9 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
  * rope_check_errors -- synchronise `stream`, then report and clear the
  * current device's error flag.
  * Returns ROPE_ERR_CUDA if the stream reports an error, else
- * ROPE_ERR_KERNEL_TIMEOUT if a wait inside the bulk-staged kernel expired
- * (about 2 s; that launch stopped early and its output is incomplete), else
+ * ROPE_ERR_KERNEL_TIMEOUT if a wait inside the bulk-staged rotation kernel or
+ * the attention kernel expired (about 2 s; that launch stopped early and its
+ * output is incomplete), else
  * ROPE_ERR_POS_OUT_OF_RANGE if any launch since the last check met an
  * out-of-range position index, else ROPE_OK.  The flag is shared by all
  * streams of the device.

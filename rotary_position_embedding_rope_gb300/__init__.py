@@ -12,6 +12,11 @@ library, and a missing library is an error, never a fallback.
 that read the sizes from tensor shapes and allocate tables and outputs with
 torch.  ``autograd.rotary_qk`` wraps the out-of-place call in a
 ``torch.autograd.Function`` (backward = rotation by the negated angle).
+``build_tables_ex`` builds the table of a frequency mode ('lang', 'pixel',
+'constant') at given positions, optionally XPOS-scaled; ``apply_qk_xpos``
+rotates Q and K with their own XPOS tables.  ``attention`` calls
+``rope_attention_fwd``: attention with the rotation fused into the Q/K tile
+loads.  ``host.HostRotator`` rotates tensors that live in pinned host memory.
 """
 from __future__ import annotations
 

@@ -11,32 +11,35 @@
 //
 // One CTA = two row blocks of 128 query rows that read the same key/value
 // head: two query heads of one GQA group (same rows), or, when the group
-// size is odd, two consecutive query tiles of one head.  256 threads; warps
-// 4j .. 4j+3 own row block j, thread t row t mod 128, which is also TMEM lane
-// t mod 128 of block j's accumulators (S: columns [256j, 256j+128), O:
-// [256j+128, 256j+128+D)).
+// size is odd, two consecutive query tiles of one head.  288 threads: warps
+// 4j .. 4j+3 own row block j (thread t: row t mod 128, which is also TMEM lane
+// t mod 128 of block j's accumulators, S in columns [256j, 256j+128), O in
+// [256j+128, 256j+128+D)); warp 8 issues every TMA copy and MMA.  The roles
+// meet only through mbarriers, never a CTA-wide barrier inside the loop.
 //
 // Key tile kt, in shared memory:
 //   * K rows arrive by TMA (cp.async.bulk.tensor, boxes of 64 elements x 128
 //     rows, 128-byte swizzle: the K-major SW128 operand layout); the table
 //     rows of the keys arrive the same way (boxes of 32 fp32 values), when
 //     the keys sit at their own indices and rotary_dim is a multiple of 64.
-//     Both are requested one tile ahead, so their latency hides behind the
-//     previous tile's softmax.
-//   * Every thread rotates its (row, chunk pair) items of the key tile in
-//     place (rotate_pair: Kahan-compensated, one rounding to the element type).
-//   * Thread 0 issues S = Q K^T for both row blocks (tcgen05.mma, fp32 in TMEM).
+//     Both are requested as soon as the previous tile's S is done, so their
+//     latency hides behind that tile's softmax.
+//   * The 256 row-block threads rotate the key tile in place (rotate_pair:
+//     Kahan-compensated, one rounding to the element type, as in the
+//     rotation kernels).
+//   * Warp 8 issues S = Q K^T per row block (tcgen05.mma, fp32 in TMEM).
 //   * Each thread reads its S row (tcgen05.ld), applies the mask and the
 //     online softmax in the exp2 domain and writes P as bf16/fp16 back into
 //     the first 64 columns of its S row (tcgen05.st); O is rescaled in TMEM
 //     when the reference max moved.
-//   * Thread 0 issues O += P V with P read from TMEM and V (TMA, two buffers,
-//     MN-major SW128) from shared memory.  That product overlaps the next
-//     tile's rotation.
+//   * Warp 8 issues O += P V per row block with P read from TMEM and V (TMA,
+//     two buffers, MN-major SW128) from shared memory.  That product overlaps
+//     the next tile's rotation.
 // The epilogue divides by the softmax sum and writes O.  Causal tiles past
 // the diagonal are skipped.  Every mbarrier wait is bounded (~2 s of clock):
-// on expiry the CTA raises the timeout flag, waits (bounded) for its copies
-// and MMAs in flight, frees its TMEM and returns.
+// a role whose wait expires raises a shared abort flag that ends the other
+// roles' waits; warp 8 then waits (bounded) for its copies and MMAs in
+// flight, TMEM is freed and the timeout flag is raised.
 #include <atomic>
 #include <cstring>
 #include <type_traits>
