@@ -349,6 +349,10 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
+def flops_of(a):
+    return attention_flops(a["B"], a["Hq"], a["S"], a["S"], a["D"], a["causal"])
+
+
 def attention_arm(args):
     world, rank, local = dist_info()
     torch.cuda.set_device(local)
@@ -369,12 +373,13 @@ def attention_arm(args):
     cos, sin = R.build_tables(a["theta"], a["rotary_dim"], a["S"], device=device)
     stream = torch.cuda.current_stream(device)
     o = torch.empty_like(q)
+    kws = torch.empty_like(k)          # receives rot(K) once per call
     warmup = max(3, args.warmup)
     steps = max(1, min(args.steps, 200))
 
-    def step():
+    def step(ws=kws):
         R.attention(q, k, v, cos, sin, rotary_dim=a["rotary_dim"], causal=a["causal"], out=o,
-                    stream=stream)
+                    k_workspace=ws, stream=stream)
 
     for _ in range(warmup):
         step()
@@ -392,9 +397,24 @@ def attention_arm(args):
     torch.cuda.synchronize(device)
     sampler.stop()
     ms = e0.elapsed_time(e1) / steps
-    flops = attention_flops(a["B"], a["Hq"], a["S"], a["S"], a["D"], a["causal"])
+    flops = flops_of(a)
     max_ms, all_flops = aggregate(dist, device, ms * steps, flops * steps)
     tflops = all_flops / (max_ms * 1e-3) / 1e12
+
+    # context: the same call with the key tiles rotated inside the attention
+    # kernel (no workspace: one launch per call)
+    for _ in range(warmup):
+        step(None)
+    torch.cuda.synchronize(device)
+    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    i0.record(stream)
+    for _ in range(steps):
+        step(None)
+    i1.record(stream)
+    torch.cuda.synchronize(device)
+    ims = i0.elapsed_time(i1) / steps
+    inkernel = {"ms": round(ims, 4), "tflops": round(flops_of(a) / (ims * 1e-3) / 1e12, 1),
+                "what": "k_workspace=None: each CTA rotates its key tiles (rope_attn_kernel)"}
 
     # context: the same result from the unfused path (rotation kernel, then
     # torch's scaled_dot_product_attention on the rotated tensors)
@@ -457,10 +477,14 @@ def attention_arm(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "peak_source": "%s bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
-                         "traffic": profiled_traffic("rope_attn_kernel", a["name"], ATTN_SOURCES),
-                         "kernel": "rope_attn_kernel"},
+                         "traffic": profiled_traffic("rope_attn_pp_kernel", a["name"],
+                                                     ATTN_SOURCES),
+                         "kernel": "rope_attn_pp_kernel",
+                         "note": "achieved = flops per call / the call's time, which also holds "
+                                 "the launch that rotates K into the workspace"},
+            "inkernel_keys_context": inkernel,
             "unfused_context": unfused,
-            "gpu_launches": steps,
+            "gpu_launches": 2 * steps,
             "clocks": sampler.summary(),
             "cpu_baseline": cpu,
         }

@@ -221,15 +221,25 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
  *    to the bottom right (query i sees key j when j <= i + Sk - Sq); a query
  *    row that sees no key gets zeros.
  * softmax_scale: > 0, or <= 0 for 1/sqrt(D).
+ * k_workspace: NULL, or a device buffer of workspace_bytes >= B * Hk * Sk *
+ *    D * 2 bytes, 16-byte aligned, overlapping no other argument; owned by
+ *    the caller and overwritten.  NULL: every CTA rotates the key tiles it
+ *    reads in shared memory, and rot(K) is never written.  Given: rot(K) is
+ *    written there once per call by the rotation kernel (rope_apply_qk's
+ *    arithmetic, so the same bits), then the attention kernel reads the
+ *    rotated keys, and its two row blocks no longer wait for a joint key
+ *    rotation.  Under GQA every key tile is read by many CTAs, so for long
+ *    sequences the workspace path is the faster one; both give the same
+ *    result bit for bit.  Q is rotated inside the attention kernel either way.
  * Arithmetic: the rotated q and k rows are rounded to `dtype`, S = q k^T is
  *    accumulated in fp32 in tensor memory, P is rounded to `dtype` for the
  *    P v product (fp32 accumulation), o is rounded once.
  * Errors: ROPE_ERR_UNSUPPORTED for other dtypes, D, rotary_dim, layouts or
  *    pointers not 16-byte aligned; ROPE_ERR_INVALID_ARG for bad sizes, null
- *    pointers, o overlapping an input; ROPE_ERR_CUDA if the launch fails,
- *    which includes more than 65535 (batch, query-head pair) units -- B *
- *    Hq / 2 when Hq / Hk is even, else B * Hq.  B, Hq or Sq zero: nothing to
- *    do, ROPE_OK.  Asynchronous on `stream`; rope_check_errors later reports
+ *    pointers, o overlapping an input, a workspace too small or overlapping;
+ *    ROPE_ERR_CUDA if the launch fails, which includes more than 65535
+ *    query tiles per head -- Sq > 65535 * 128 when Hq / Hk is even, else
+ *    Sq > 65535 * 256.  B, Hq or Sq zero: nothing to do, ROPE_OK.  Asynchronous on `stream`; rope_check_errors later reports
  *    out-of-range positions and, should a wait inside the kernel expire (about
  *    2 s; o is then not written), ROPE_ERR_KERNEL_TIMEOUT.
  */
@@ -238,7 +248,8 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
                                const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
                                int64_t Sk, int32_t D, int32_t rotary_dim, int32_t layout,
                                int32_t causal, float softmax_scale, int32_t dtype,
-                               int64_t table_rows, void *stream);
+                               int64_t table_rows, void *k_workspace, int64_t workspace_bytes,
+                               void *stream);
 
 /*
  * rope_check_errors -- synchronise `stream`, then report and clear the

@@ -16,7 +16,7 @@ torch.  ``autograd.rotary_qk`` wraps the out-of-place call in a
 'constant') at given positions, optionally XPOS-scaled; ``apply_qk_xpos``
 rotates Q and K with their own XPOS tables.  ``attention`` calls
 ``rope_attention_fwd``: attention with the rotation fused into the Q/K tile
-loads.  ``host.HostRotator`` rotates tensors that live in pinned host memory.
+loads (or, with a key workspace, keys rotated once beforehand).  ``host.HostRotator`` rotates tensors that live in pinned host memory.
 """
 from __future__ import annotations
 
@@ -103,7 +103,8 @@ def load_library() -> ctypes.CDLL:
     lib.rope_apply_qk_out.restype = c.c_int
     lib.rope_attention_fwd.argtypes = [P, P, P, P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32,
                                        c.c_int64, c.c_int64, c.c_int32, c.c_int32, c.c_int32,
-                                       c.c_int32, c.c_float, c.c_int32, c.c_int64, P]
+                                       c.c_int32, c.c_float, c.c_int32, c.c_int64, P,
+                                       c.c_int64, P]
     lib.rope_attention_fwd.restype = c.c_int
     lib.rope_force_kernel_variant.argtypes = [c.c_int32]
     lib.rope_force_kernel_variant.restype = c.c_int
@@ -387,13 +388,16 @@ def rotate_qk(q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor, sin: t
 
 
 def rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim,
-                       layout, causal, softmax_scale, dtype, table_rows, stream=None):
+                       layout, causal, softmax_scale, dtype, table_rows, k_workspace=None,
+                       workspace_bytes=0, stream=None):
     lib = load_library()
     st = lib.rope_attention_fwd(_addr(q, "q"), _addr(k, "k"), _addr(v, "v"), _addr(o, "o"),
                                 _addr(cos, "cos"), _addr(sin, "sin"), _addr(pos_q, "pos_q"),
                                 _addr(pos_k, "pos_k"), int(B), int(Hq), int(Hk), int(Sq), int(Sk),
                                 int(D), int(rotary_dim), int(layout), int(causal),
-                                float(softmax_scale), int(dtype), int(table_rows), _stream(stream))
+                                float(softmax_scale), int(dtype), int(table_rows),
+                                _addr(k_workspace, "k_workspace"), int(workspace_bytes),
+                                _stream(stream))
     _check(st, "rope_attention_fwd")
 
 
@@ -401,15 +405,27 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
               sin: torch.Tensor, pos_q: torch.Tensor | None = None,
               pos_k: torch.Tensor | None = None, rotary_dim: int | None = None,
               layout: str = "split_half", causal: bool = False, scale: float | None = None,
-              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """softmax(scale * rot(q) rot(k)^T + mask) v with q [B,Hq,Sq,D], k/v [B,Hk,Sk,D]."""
+              out: torch.Tensor | None = None, k_workspace="auto", stream=None) -> torch.Tensor:
+    """softmax(scale * rot(q) rot(k)^T + mask) v with q [B,Hq,Sq,D], k/v [B,Hk,Sk,D].
+
+    k_workspace: "auto" allocates a buffer like k that receives rot(K) (the
+    keys are rotated once, then read rotated by the attention kernel); a
+    tensor of k's size is used as that buffer; None rotates the key tiles
+    inside the attention kernel instead (nothing extra is written).  The
+    result is the same bit for bit.
+    """
     B, Hq, Sq, D = q.shape
     _, Hk, Sk, _ = k.shape
     if v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k and v must have the same shape, and q, k, v the same dtype")
     rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
     o = torch.empty_like(q) if out is None else out
+    if isinstance(k_workspace, str):
+        if k_workspace != "auto":
+            raise ValueError("k_workspace must be 'auto', None or a tensor")
+        k_workspace = torch.empty_like(k)
+    ws_bytes = 0 if k_workspace is None else k_workspace.numel() * k_workspace.element_size()
     rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rd,
                        _LAYOUT_CODE[layout], int(causal), -1.0 if scale is None else scale,
-                       _DTYPE_CODE[q.dtype], cos.shape[0], stream)
+                       _DTYPE_CODE[q.dtype], cos.shape[0], k_workspace, ws_bytes, stream)
     return o

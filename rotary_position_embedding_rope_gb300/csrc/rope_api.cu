@@ -419,7 +419,8 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
                                const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
                                int64_t Sk, int32_t D, int32_t rotary_dim, int32_t layout,
                                int32_t causal, float softmax_scale, int32_t dtype,
-                               int64_t table_rows, void *stream)
+                               int64_t table_rows, void *k_workspace, int64_t workspace_bytes,
+                               void *stream)
 {
     if (dtype != ROPE_BF16 && dtype != ROPE_F16)
         return ROPE_ERR_UNSUPPORTED;
@@ -453,8 +454,23 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
         ranges_overlap(o, qb, sin, tabb) || ranges_overlap(o, qb, pos_q, Sq * 4) ||
         ranges_overlap(o, qb, pos_k, Sk * 4))
         return ROPE_ERR_INVALID_ARG;
+    // the key workspace receives rot(K): at least kb bytes, aligned, and
+    // disjoint from every other buffer of the call
+    void *ws = Sk > 0 ? k_workspace : nullptr;
+    if (ws != nullptr) {
+        if (workspace_bytes < kb)
+            return ROPE_ERR_INVALID_ARG;
+        if (!aligned16(ws))
+            return ROPE_ERR_UNSUPPORTED;
+        if (ranges_overlap(ws, kb, q, qb) || ranges_overlap(ws, kb, k, kb) ||
+            ranges_overlap(ws, kb, v, kb) || ranges_overlap(ws, kb, o, qb) ||
+            ranges_overlap(ws, kb, cos, tabb) || ranges_overlap(ws, kb, sin, tabb) ||
+            ranges_overlap(ws, kb, pos_q, Sq * 4) || ranges_overlap(ws, kb, pos_k, Sk * 4))
+            return ROPE_ERR_INVALID_ARG;
+    }
     AttnArgs a;
     a.q = q; a.k = k; a.v = v; a.o = o;
+    a.k_rot = ws;
     a.cos = cos; a.sin = sin;
     a.pos_q = pos_q; a.pos_k = pos_k;
     a.B = B; a.Hq = Hq; a.Hk = Hk; a.Sq = Sq; a.Sk = Sk;
@@ -466,6 +482,15 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
     int32_t *taken = nullptr;
     if (flag_addresses(&a.flag, &taken) != cudaSuccess)
         return ROPE_ERR_CUDA;
+    if (ws != nullptr) {
+        // rot(K) into the workspace, by the rotation kernel on the same stream
+        // (out of place: -1 and out-of-range positions copy the key unchanged)
+        const CallArgs c = {nullptr, k, nullptr, ws, cos, sin, pos_k, 0, B, 0, Hk, Sk, D,
+                            rotary_dim, layout, 0, 0, dtype, table_rows};
+        const rope_status s = apply_call(c, stream);
+        if (s != ROPE_OK)
+            return s;
+    }
     return launch_attention(a, D, layout, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ROPE_OK
                : ROPE_ERR_CUDA;

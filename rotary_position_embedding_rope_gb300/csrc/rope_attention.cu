@@ -67,11 +67,12 @@ constexpr uint32_t kSwizzle128 = 2;                // descriptor layout type: 12
 constexpr long long kAttnWaitCycles = 4000000000LL;
 
 // Tensor maps of one call, all with 128-byte swizzle: K and V as
-// [B * Hk][Sk][D] (box: 64 elements x 128 rows), the cos and sin tables as
+// [B * Hk][Sk][D] and Q as [B * Hq][Sq][D] (box: 64 elements x 128 rows; Q
+// only for rope_attn_pp_kernel), the cos and sin tables as
 // [table_rows][rotary_dim / 2] fp32 (box: 32 values x 128 rows).  A box lands
 // as 128 rows of 128 bytes, the 16-byte chunk c of row r at chunk c ^ (r & 7).
 struct AttnMaps {
-    CUtensorMap k, v, cos, sin;
+    CUtensorMap k, v, cos, sin, q;
 };
 
 __device__ __forceinline__ uint32_t attn_smem_u32(const void *p)
@@ -420,10 +421,13 @@ struct KeyItem {
     bool rot;
 };
 
-// Loads item i of the key-tile rotation (row i mod 128, chunk i / 128).
+// Loads item i of a tile rotation (row i mod 128, chunk i / 128) from a
+// tile of swizzled boxes whose row r holds token k0 + r of a sequence of S
+// tokens with positions pos (NULL: the token index).
 template <typename T, int LAYOUT, bool STAGED>
 __device__ __forceinline__ void load_key_item(KeyItem &it, int i, const uint8_t *sK,
-                                              const uint8_t *sT, int64_t k0, const AttnArgs &a)
+                                              const uint8_t *sT, int64_t k0, const int32_t *pos,
+                                              int64_t S, const AttnArgs &a)
 {
     constexpr int NQ = LAYOUT == 0 ? 2 : 1;        // float4 table reads per item
     const int rd = a.rotary_dim, h = rd >> 1, h8 = rd / 16;
@@ -445,7 +449,7 @@ __device__ __forceinline__ void load_key_item(KeyItem &it, int i, const uint8_t 
         }
     } else {
         const int64_t tok = k0 + r;
-        const int64_t tr = tok < a.Sk ? attn_row(a.pos_k, tok, a.table_rows, a.flag, p == 0) : -1;
+        const int64_t tr = tok < S ? attn_row(pos, tok, a.table_rows, a.flag, p == 0) : -1;
         it.rot = tr >= 0;
         const int64_t trc = tr < 0 ? 0 : tr;
         const float4 *cr = reinterpret_cast<const float4 *>(a.cos + trc * h + p * 4 * NQ);
@@ -485,31 +489,33 @@ __device__ __forceinline__ void store_key_item(KeyItem &it, uint8_t *sK)
     }
 }
 
-// Rotates the key tile in place (rows k0 .. k0 + 127, swizzled 128-byte
-// boxes as the TMA left them; rows past Sk hold zeros), by the kMathThreads
-// threads of the row blocks.  Item i = (row i mod 128, chunk i / 128):
-// consecutive lanes take consecutive rows of one chunk, which the swizzle
-// spreads over eight distinct 16-byte bank groups.  Two items are loaded
-// before either is rotated.  STAGED: the keys sit at their own indices and
-// their table rows were staged the same way next to the tile (cos: rd / 64
-// boxes, then sin); otherwise each row's position is read and its table row
-// fetched from global memory.
-template <typename T, int LAYOUT, bool STAGED>
-__device__ __forceinline__ void rotate_key_tile(uint8_t *sK, const uint8_t *sT, int64_t k0,
-                                                const AttnArgs &a, int tid)
+// Rotates a 128-row tile in place (rows k0 .. k0 + 127 of a sequence of S
+// tokens with positions pos, in swizzled 128-byte boxes as the TMA left them;
+// rows past S hold zeros) by NT threads, tid in [0, NT).  Item i = (row i mod
+// 128, chunk i / 128): consecutive lanes take consecutive rows of one chunk,
+// which the swizzle spreads over eight distinct 16-byte bank groups.  NF
+// items are loaded before any is rotated.  STAGED: the tokens sit at their
+// own indices and their table rows were staged the same way next to the
+// tile (cos: rd / 64 boxes, then sin); otherwise each row's position is read
+// and its table row fetched from global memory.
+template <typename T, int LAYOUT, bool STAGED, int NT, int NF>
+__device__ __forceinline__ void rotate_tile(uint8_t *sK, const uint8_t *sT, int64_t k0,
+                                            const int32_t *pos, int64_t S, const AttnArgs &a,
+                                            int tid)
 {
     const int per_row = LAYOUT == 0 ? a.rotary_dim / 16 : a.rotary_dim / 8;
     const int items = kAttnKeys * per_row;
 #pragma unroll 1
-    for (int i = tid; i < items; i += 2 * kMathThreads) {
-        const bool second = i + kMathThreads < items;
-        KeyItem x, y;
-        load_key_item<T, LAYOUT, STAGED>(x, i, sK, sT, k0, a);
-        if (second)
-            load_key_item<T, LAYOUT, STAGED>(y, i + kMathThreads, sK, sT, k0, a);
-        store_key_item<T, LAYOUT>(x, sK);
-        if (second)
-            store_key_item<T, LAYOUT>(y, sK);
+    for (int i = tid; i < items; i += NF * NT) {
+        KeyItem x[NF];
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            if (i + f * NT < items)
+                load_key_item<T, LAYOUT, STAGED>(x[f], i + f * NT, sK, sT, k0, pos, S, a);
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            if (i + f * NT < items)
+                store_key_item<T, LAYOUT>(x[f], sK);
     }
 }
 
@@ -546,6 +552,164 @@ __device__ __forceinline__ void issue_value_tile(const AttnMaps &m, uint8_t *sV,
         tma_load_3d(sV + lane * kBoxBytes, &m.v, lane * 64, k0, zkv, bar);
 }
 
+// The work of one CTA: batch b and key/value head zkv = b * Hk + hk; row
+// block j holds query head hq_first + j * hq_step, rows q0_first + j * q_step
+// .. + 127 (two query heads of one GQA group when pair_heads, else two
+// consecutive query tiles of one head); n_tiles = the key tiles those rows
+// can see.  blockIdx.x is the (batch, head) unit and blockIdx.y the query
+// tile, last tile first: the hardware hands out blocks x fastest, so under a
+// causal mask every CTA of the longest query tiles starts before any of the
+// shorter ones (longest job first; the short ones fill the end).
+struct AttnWork {
+    int64_t b, q0_first, q_step, n_tiles;
+    int32_t hq_first, hq_step, zkv;
+};
+
+__device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_heads)
+{
+    AttnWork w;
+    if (pair_heads) {
+        const int32_t pairs = a.Hq / 2;
+        w.b = blockIdx.x / pairs;
+        w.hq_first = (int32_t)(blockIdx.x - w.b * pairs) * 2;
+        w.hq_step = 1;
+        w.q0_first = (int64_t)(gridDim.y - 1 - blockIdx.y) * kAttnRows;
+        w.q_step = 0;
+    } else {
+        w.b = blockIdx.x / a.Hq;
+        w.hq_first = (int32_t)(blockIdx.x - w.b * a.Hq);
+        w.hq_step = 0;
+        w.q0_first = (int64_t)(gridDim.y - 1 - blockIdx.y) * 2 * kAttnRows;
+        w.q_step = kAttnRows;
+    }
+    w.zkv = (int32_t)(w.b * a.Hk + w.hq_first / (a.Hq / a.Hk));
+    const int64_t shift = a.Sk - a.Sq;             // bottom-right aligned causal mask
+    w.n_tiles = (a.Sk + kAttnKeys - 1) / kAttnKeys;
+    if (a.causal) {
+        int64_t last_row = w.q0_first + (kAttnBlocks - 1) * w.q_step + kAttnRows - 1;
+        if (last_row > a.Sq - 1)
+            last_row = a.Sq - 1;
+        const int64_t last = last_row + shift;     // last key visible to the CTA
+        const int64_t t = last < 0 ? 0 : last / kAttnKeys + 1;
+        if (t < w.n_tiles)
+            w.n_tiles = t;
+    }
+    return w;
+}
+
+// One online-softmax step of query row qi on the key tile at k0.  The row's
+// S = Q K^T sits in TMEM columns [acc, acc + 128) of its lane and its O in
+// [acc + 128, acc + 128 + D).  The 128 S values are read once and held in
+// registers.  Computes the row max over the visible keys, moves the lazy
+// reference max m_ref when needed, writes P = 2^(s * scale * log2(e) -
+// m_ref) as packed 16-bit values over the first 64 columns of S, updates the
+// running sum l_run and rescales O when the reference moved (not on the first
+// tile: O holds nothing yet).  The max and the sum keep eight and four
+// partial results, so no long chain of dependent instructions sets the
+// latency.  Warp-collective; the caller waits for the TMEM stores before
+// signalling that P is ready.
+template <typename T, int D>
+__device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int64_t k0,
+                                             int64_t shift, const AttnArgs &a, bool not_first,
+                                             float &m_ref, float &l_run)
+{
+    // columns of this tile visible to this row: [0, nvis)
+    int64_t vis_end = a.Sk;                // first invisible key
+    if (a.causal && qi + shift + 1 < vis_end)
+        vis_end = qi + shift + 1;
+    const int64_t nv = vis_end - k0;
+    const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
+    const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
+    float sv[kAttnKeys];
+#pragma unroll
+    for (int c0 = 0; c0 < kAttnKeys; c0 += 32)
+        tmem_ld32_nowait(acc_base + c0, sv + c0);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (!full) {
+#pragma unroll
+        for (int i = 0; i < kAttnKeys; ++i)
+            sv[i] = i < nvis ? sv[i] : -INFINITY;  // masked keys: 2^-inf = 0 below
+    }
+    float m8[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        m8[r] = sv[r];
+#pragma unroll
+    for (int i = 8; i < kAttnKeys; ++i)
+        m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
+    float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    mx *= a.scale_log2;                    // scale > 0: max commutes with it
+    // The exponentials use a reference max m_ref that only moves when the
+    // row max exceeds it by more than 8 (factor 256): P stays <= 256, exact
+    // in fp32 and bf16/fp16 range, and O is rescaled only then.
+    float alpha = 1.0f;
+    if (mx > m_ref + 8.0f) {
+        alpha = m_ref == -INFINITY ? 0.0f : fast_exp2(m_ref - mx);
+        m_ref = mx;
+    }
+    // m_ref is -inf only while the row has seen no visible key; every key
+    // of this tile is then masked (-inf) and gives 2^-inf = 0
+    const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
+    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    uint32_t w[kAttnKeys / 2];
+#pragma unroll
+    for (int i = 0; i < kAttnKeys; i += 2) {
+        const float p0 = fast_exp2(fmaf(sv[i], a.scale_log2, neg_m));
+        const float p1 = fast_exp2(fmaf(sv[i + 1], a.scale_log2, neg_m));
+        s4[(i >> 1) & 3] += p0 + p1;
+        w[i >> 1] = Elt<T>::f2_to_word(p0, p1);
+    }
+    // keys 2c, 2c + 1 -> column c (the even key in the low half)
+#pragma unroll
+    for (int c = 0; c < kAttnKeys / 2; c += 16)
+        tmem_st16(acc_base + c, *reinterpret_cast<const uint32_t(*)[16]>(w + c));
+    l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+    if (not_first && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            tmem_ld32(acc_base + kAttnKeys + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ov[i] *= alpha;
+            tmem_st32(acc_base + kAttnKeys + c0, ov);
+        }
+    }
+}
+
+// Epilogue of query row qi: O / l from TMEM columns [acc + 128, acc + 128 +
+// D), rounded once, to the row of O (zeros when the row saw no key).  TMEM
+// loads are warp-wide; rows at or past Sq store nothing.
+template <typename T, int D>
+__device__ __forceinline__ void store_o_row(uint32_t acc_base, T *O, int64_t qi, int64_t Sq,
+                                            bool any_key, float l_run)
+{
+    const float inv = (any_key && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    uint4 *dst = reinterpret_cast<uint4 *>(O + qi * D);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        if (any_key) {
+            tmem_ld32(acc_base + kAttnKeys + c0, ov);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ov[i] = 0.0f;
+        }
+        if (qi < Sq) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    f[e] = ov[c * 8 + e] * inv;
+                dst[(c0 + c * 8) / 8] = Elt<T>::pack(f);
+            }
+        }
+    }
+}
+
 template <typename T, int LAYOUT, int D, bool STAGED>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     rope_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps, const int32_t pair_heads)
@@ -571,46 +735,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int j = math ? warp >> 2 : 0;            // row block of this warp
     const int wq = warp & 3;                       // TMEM lane quarter
     const int row = tid & (kAttnRows - 1);
-    const int group = a.Hq / a.Hk;
-    // row block j: query head hq_j, query rows q0_j .. q0_j + 127; the longest
-    // CTAs (the last query tiles, under a causal mask) start first
-    int64_t b, q0_first, q_step;
-    int32_t hq_first, hq_step;
-    if (pair_heads) {
-        const int32_t pairs = a.Hq / 2;
-        b = blockIdx.y / pairs;
-        hq_first = (int32_t)(blockIdx.y - b * pairs) * 2;
-        hq_step = 1;
-        q0_first = (int64_t)(gridDim.x - 1 - blockIdx.x) * kAttnRows;
-        q_step = 0;
-    } else {
-        b = blockIdx.y / a.Hq;
-        hq_first = (int32_t)(blockIdx.y - b * a.Hq);
-        hq_step = 0;
-        q0_first = (int64_t)(gridDim.x - 1 - blockIdx.x) * 2 * kAttnRows;
-        q_step = kAttnRows;
-    }
-    const int32_t hq = hq_first + j * hq_step;
-    const int32_t hk = hq_first / group;
-    const int zkv = (int)(b * a.Hk + hk);
-    const int64_t q0 = q0_first + j * q_step;
+    const AttnWork w = attn_work(a, pair_heads);
+    const int32_t hq = w.hq_first + j * w.hq_step;
+    const int zkv = w.zkv;
+    const int64_t q0 = w.q0_first + j * w.q_step;
     const int64_t qi = q0 + row;
-    const T *Qh = static_cast<const T *>(a.q) + ((b * a.Hq + hq) * a.Sq) * D;
-    T *O = static_cast<T *>(a.o) + ((b * a.Hq + hq) * a.Sq) * D;
+    const T *Qh = static_cast<const T *>(a.q) + ((w.b * a.Hq + hq) * a.Sq) * D;
+    T *O = static_cast<T *>(a.o) + ((w.b * a.Hq + hq) * a.Sq) * D;
     const int tboxes = a.rotary_dim / 64;          // table boxes of cos (and of sin)
-
-    // key tiles the CTA's rows can see
     const int64_t shift = a.Sk - a.Sq;             // bottom-right aligned causal mask
-    int64_t n_tiles = (a.Sk + kAttnKeys - 1) / kAttnKeys;
-    if (a.causal) {
-        int64_t last_row = q0_first + (kAttnBlocks - 1) * q_step + kAttnRows - 1;
-        if (last_row > a.Sq - 1)
-            last_row = a.Sq - 1;
-        const int64_t last = last_row + shift;     // last key visible to the CTA
-        const int64_t t = last < 0 ? 0 : last / kAttnKeys + 1;
-        if (t < n_tiles)
-            n_tiles = t;
-    }
+    const int64_t n_tiles = w.n_tiles;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -661,7 +795,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = __all_sync(0xffffffffu, attn_wait(&bar_k, ph, abort));
             if (!ok)
                 break;
-            rotate_key_tile<T, LAYOUT, STAGED>(sK, sT, k0, a, tid);
+            rotate_tile<T, LAYOUT, STAGED, kMathThreads, 2>(sK, sT, k0, a.pos_k, a.Sk, a, tid);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(&bar_krot);
             // 2. this block's S = Q K^T is ready; its O += P V of the previous
@@ -672,87 +806,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // 3. online softmax; P goes back into TMEM over S
-            // columns of this tile visible to this row: [0, nvis)
-            int64_t vis_end = a.Sk;                // first invisible key
-            if (a.causal && qi + shift + 1 < vis_end)
-                vis_end = qi + shift + 1;
-            const int64_t nv = vis_end - k0;
-            const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
-            const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
-            // S is read in halves of 64 columns, two loads in flight per wait
-            constexpr int kHalf = kAttnKeys / 2;
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kAttnKeys; c0 += kHalf) {
-                float sv[kHalf];
-                tmem_ld32_nowait(acc_base + c0, sv);
-                tmem_ld32_nowait(acc_base + c0 + 32, sv + 32);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < kHalf; ++i)
-                        mx = fmaxf(mx, sv[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kHalf; ++i)
-                        if (c0 + i < nvis)
-                            mx = fmaxf(mx, sv[i]);
-                }
-            }
-            mx *= a.scale_log2;                    // scale > 0: max commutes with it
-            // The exponentials use a reference max m_ref that only moves when
-            // the row max exceeds it by more than 8 (factor 256): P stays <=
-            // 256, exact in fp32 and bf16/fp16 range, and O is rescaled only then.
-            float alpha = 1.0f;
-            if (mx > m_ref + 8.0f) {
-                alpha = m_ref == -INFINITY ? 0.0f : fast_exp2(m_ref - mx);
-                m_ref = mx;
-            }
-            const float m_new = m_ref;
-            float sum = 0.0f;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kAttnKeys; c0 += kHalf) {
-                float sv[kHalf];
-                tmem_ld32_nowait(acc_base + c0, sv);
-                tmem_ld32_nowait(acc_base + c0 + 32, sv + 32);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                uint32_t w[kHalf / 2];
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < kHalf; i += 2) {
-                        const float p0 = fast_exp2(fmaf(sv[i], a.scale_log2, -m_new));
-                        const float p1 = fast_exp2(fmaf(sv[i + 1], a.scale_log2, -m_new));
-                        sum += p0 + p1;
-                        w[i / 2] = Elt<T>::f2_to_word(p0, p1);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kHalf; i += 2) {
-                        const float p0 =
-                            c0 + i < nvis ? fast_exp2(fmaf(sv[i], a.scale_log2, -m_new)) : 0.0f;
-                        const float p1 =
-                            c0 + i + 1 < nvis ? fast_exp2(fmaf(sv[i + 1], a.scale_log2, -m_new)) : 0.0f;
-                        sum += p0 + p1;
-                        w[i / 2] = Elt<T>::f2_to_word(p0, p1);
-                    }
-                }
-                // keys c0 .. c0 + 63 -> columns c0 / 2 .. c0 / 2 + 31, all of
-                // which this thread has already read
-                tmem_st16(acc_base + c0 / 2, *reinterpret_cast<const uint32_t(*)[16]>(w));
-                tmem_st16(acc_base + c0 / 2 + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
-            }
-            l_run = l_run * alpha + sum;
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float ov[32];
-                    tmem_ld32(acc_base + kAttnKeys + c0, ov);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] *= alpha;
-                    tmem_st32(acc_base + kAttnKeys + c0, ov);
-                }
-            }
+            softmax_tile<T, D>(acc_base, qi, k0, shift, a, kt > 0, m_ref, l_run);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
@@ -764,31 +818,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) {
             *abort = 1;
         } else {
-            // epilogue: O / l for this row (zeros when no key is visible);
-            // TMEM loads are warp-wide, stores only for rows inside the sequence
-            const float inv = (n_tiles > 0 && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-            uint4 *dst = reinterpret_cast<uint4 *>(O + qi * D);
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float ov[32];
-                if (n_tiles > 0) {
-                    tmem_ld32(acc_base + kAttnKeys + c0, ov);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] = 0.0f;
-                }
-                if (qi < a.Sq) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] = ov[c * 8 + e] * inv;
-                        dst[(c0 + c * 8) / 8] = Elt<T>::pack(f);
-                    }
-                }
-            }
+            // epilogue: O / l for this row
+            store_o_row<T, D>(acc_base, O, qi, a.Sq, n_tiles > 0, l_run);
         }
     } else {
         // ---- issue warp: TMA copies one tile ahead, the MMAs (lane 0)
@@ -912,6 +943,299 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Attention over keys rotated beforehand (rope_attention_fwd with a key
+// workspace: the rotation kernel writes rot(K) there once per call, so no
+// CTA spends issue slots rotating key tiles).  Q is still rotated as its
+// tile is loaded.  Freed of the joint key rotation, the two row blocks run
+// out of step: while one block's warps compute the softmax of a key tile,
+// the tensor cores run the other block's products.
+//
+// 352 threads: warps 0-7 the two row blocks (as in rope_attn_kernel), warps
+// 8 and 9 issue the MMAs of row block 0 and 1, warp 10 the TMA copies.  One
+// issuing warp per block: a warp that issues MMAs stalls while the tensor
+// pipe is full, and a shared issuer would hold one block's ready P behind
+// the other block's products.  Shared memory: Q_0, Q_1, two key stages, two
+// value stages (6 tiles of 128 x D).  Block j's issuer runs, per key tile kt,
+//   O_j += P_j V(kt) (once P_j is in TMEM); S_j = Q_j K(kt+1) (once that
+//   product has finished: P_j sits in the columns S_j overwrites)
+// and both issuers release a key or value stage (arrival count 2).  Every
+// wait is bounded as in rope_attn_kernel.
+// ---------------------------------------------------------------------------
+constexpr int kPpMmaWarp = kMathThreads / 32;      // warps 8, 9: MMA issue of blocks 0, 1
+constexpr int kPpTmaWarp = kPpMmaWarp + kAttnBlocks;   // warp 10
+constexpr int kPpThreads = kMathThreads + 32 * (kAttnBlocks + 1);
+constexpr int kPpStages = 2;                       // key and value stages
+
+template <typename T, int LAYOUT, int D, bool STAGED_Q>
+__global__ void __launch_bounds__(kPpThreads, 1)
+    rope_attn_pp_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps,
+                        const int32_t pair_heads)
+{
+    constexpr uint32_t kTile = kAttnRows * D * 2;  // bytes of a 128 x D tile
+    constexpr uint32_t ab_format = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    // [Q_0][Q_1][K stage 0][V stage 0][K stage 1][V stage 1].  STAGED_Q: the
+    // table rows of the query tiles (both blocks hold the same rows) land in
+    // stage 1 first (cos: rd / 64 boxes, then sin; at most 2 tiles' bytes),
+    // which receives its key and value tiles once Q is rotated.
+    uint8_t *sQ = smem;
+    uint8_t *sKV = sQ + kAttnBlocks * kTile;
+    auto sK = [&](int stage) { return sKV + stage * 2 * kTile; };
+    auto sV = [&](int stage) { return sKV + stage * 2 * kTile + kTile; };
+    const int tboxes = a.rotary_dim / 64;          // table boxes of cos (and of sin)
+    // stage landed (TMA) / stage free (one MMA commit from each issuer), per
+    // stage; S ready and O += P V done (MMA commits), P ready (the block's
+    // 128 threads), per block
+    __shared__ __align__(8) uint64_t bar_kfull[kPpStages], bar_kfree[kPpStages],
+        bar_vfull[kPpStages], bar_vfree[kPpStages], bar_s[kAttnBlocks], bar_o[kAttnBlocks],
+        bar_p[kAttnBlocks], bar_q;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool math = warp < kPpMmaWarp;
+    const int j = math ? warp >> 2 : 0;
+    const int wq = warp & 3;
+    const int row = tid & (kAttnRows - 1);
+    const AttnWork w = attn_work(a, pair_heads);
+    const int32_t hq = w.hq_first + j * w.hq_step;
+    const int64_t q0 = w.q0_first + j * w.q_step;
+    const int64_t qi = q0 + row;
+    T *O = static_cast<T *>(a.o) + ((w.b * a.Hq + hq) * a.Sq) * D;
+    const int64_t shift = a.Sk - a.Sq;
+    const int64_t n_tiles = w.n_tiles;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(attn_smem_u32(&tmem_base)), "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kPpStages; ++s) {
+            mbar_init(&bar_kfull[s], 1);
+            mbar_init(&bar_kfree[s], kAttnBlocks);
+            mbar_init(&bar_vfull[s], 1);
+            mbar_init(&bar_vfree[s], kAttnBlocks);
+        }
+        for (int blk = 0; blk < kAttnBlocks; ++blk) {
+            mbar_init(&bar_s[blk], 1);
+            mbar_init(&bar_o[blk], 1);
+            mbar_init(&bar_p[blk], kAttnRows);
+        }
+        mbar_init(&bar_q, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // both query tiles (and their table rows), then the key and value tiles
+    // of stage 0 (and of stage 1 when it holds no table rows)
+    const int64_t first_stages = STAGED_Q ? 1 : kPpStages;
+    if (warp == kPpTmaWarp) {
+        constexpr int kBoxes = D / 64;             // 64-element boxes per row
+        if (lane == 0)
+            mbar_expect_tx(&bar_q, (uint32_t)(kAttnBlocks * kBoxes + (STAGED_Q ? 2 * tboxes : 0)) *
+                                       kBoxBytes);
+        __syncwarp();
+        if (lane < kAttnBlocks * kBoxes) {
+            const int blk = lane / kBoxes, box = lane % kBoxes;
+            tma_load_3d(sQ + blk * kTile + box * kBoxBytes, &maps.q, box * 64,
+                        (int)(w.q0_first + blk * w.q_step),
+                        (int)(w.b * a.Hq + w.hq_first + blk * w.hq_step), &bar_q);
+        }
+        if (STAGED_Q && lane >= 8 && lane < 8 + 2 * tboxes) {
+            const int t = lane - 8;
+            const bool is_cos = t < tboxes;
+            tma_load_2d(sK(1) + t * kBoxBytes, is_cos ? &maps.cos : &maps.sin,
+                        (is_cos ? t : t - tboxes) * 32, (int)w.q0_first, &bar_q);
+        }
+        for (int64_t kt = 0; kt < first_stages && kt < n_tiles; ++kt) {
+            issue_key_tile<D, false>(maps, sK((int)kt), nullptr, (int)(kt * kAttnKeys), w.zkv, 0,
+                                     &bar_kfull[kt], lane);
+            issue_value_tile<D>(maps, sV((int)kt), (int)(kt * kAttnKeys), w.zkv, &bar_vfull[kt],
+                                lane);
+        }
+    }
+    // each row block rotates its query tile in place (rows past Sq: zeros)
+    bool q_ok = true;
+    if (math) {
+        q_ok = __all_sync(0xffffffffu, attn_wait(&bar_q, 0u));
+        if (q_ok)
+            rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(sQ + j * kTile, sK(1), q0, a.pos_q,
+                                                           a.Sq, a, row);
+        else
+            abort_flag = 1;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base;
+    volatile int *abort = &abort_flag;
+    bool ok = !*abort;                             // false: the query tiles never landed
+
+    if (math) {
+        // ---- row-block warps: the softmax of row qi, tile after tile
+        const uint32_t acc_base = tmem + (uint32_t)j * kBlockCols + ((uint32_t)(wq * 32) << 16);
+        float m_ref = -INFINITY, l_run = 0.0f;
+        for (int64_t kt = 0; kt < n_tiles; ++kt) {
+            // S of this block is ready (its previous O += P V has finished:
+            // the MMA warp waited for it before issuing S)
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_s[j], (uint32_t)(kt & 1), abort));
+            if (!ok)
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            softmax_tile<T, D>(acc_base, qi, kt * kAttnKeys, shift, a, kt > 0, m_ref, l_run);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&bar_p[j]);
+        }
+        // the last O += P V
+        if (ok && n_tiles > 0)
+            ok = __all_sync(0xffffffffu,
+                            attn_wait(&bar_o[j], (uint32_t)((n_tiles - 1) & 1), abort));
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (!ok)
+            *abort = 1;
+        else
+            store_o_row<T, D>(acc_base, O, qi, a.Sq, n_tiles > 0, l_run);
+    } else if (warp < kPpTmaWarp) {
+        // ---- MMA issue of row block jb (lane 0 issues; the waits are warp-wide)
+        const int jb = warp - kPpMmaWarp;
+        const uint32_t idesc_s = umma_idesc(128, kAttnKeys, ab_format, 0);
+        const uint32_t idesc_o = umma_idesc(128, D, ab_format, 1);
+        const uint32_t acc = tmem + (uint32_t)jb * kBlockCols;
+        const uint32_t q_addr = attn_smem_u32(sQ + jb * kTile);
+        uint64_t *last_bar = nullptr;              // the last commit covers every MMA before it
+        uint32_t last_ph = 0;
+        // S = Q_jb K(stage), completion on bar_s[jb]; releases the key stage
+        auto issue_s = [&](int stage) {
+            if (lane == 0) {
+                const uint32_t k_addr = attn_smem_u32(sK(stage));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(acc,
+                            umma_desc(q_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32u, 16u, 1024u,
+                                      kSwizzle128),
+                            umma_desc(k_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32u, 16u, 1024u,
+                                      kSwizzle128),
+                            idesc_s, kk > 0);
+                umma_commit(&bar_s[jb]);
+                umma_commit(&bar_kfree[stage]);
+            }
+            __syncwarp();
+        };
+        if (n_tiles > 0) {
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_kfull[0], 0u, abort));
+            if (ok) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                issue_s(0);
+                last_bar = &bar_s[jb];
+                last_ph = 0;
+            }
+        }
+        for (int64_t kt = 0; ok && kt < n_tiles; ++kt) {
+            const int st = (int)(kt % kPpStages);
+            const uint32_t use_ph = (uint32_t)((kt / kPpStages) & 1);
+            const int nst = (int)((kt + 1) % kPpStages);
+            const uint32_t nuse_ph = (uint32_t)(((kt + 1) / kPpStages) & 1);
+            // O_jb += P_jb V(kt) once the value tile has landed and P is in TMEM
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_vfull[st], use_ph, abort) &&
+                                             attn_wait(&bar_p[jb], (uint32_t)(kt & 1), abort));
+            if (!ok)
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (lane == 0) {
+                const uint32_t v_addr = attn_smem_u32(sV(st));
+#pragma unroll
+                for (int kk = 0; kk < kAttnKeys / 16; ++kk)
+                    umma_ts(acc + kAttnKeys, acc + kk * 8,
+                            umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128), idesc_o,
+                            (kt > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bar_o[jb]);
+                umma_commit(&bar_vfree[st]);
+            }
+            __syncwarp();
+            last_bar = &bar_o[jb];
+            last_ph = (uint32_t)(kt & 1);
+            if (kt + 1 >= n_tiles)
+                break;
+            // S_jb of the next key tile, once that tile has landed and this
+            // block's O += P V has released the columns of P
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_kfull[nst], nuse_ph, abort) &&
+                                             attn_wait(&bar_o[jb], (uint32_t)(kt & 1), abort));
+            if (!ok)
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            issue_s(nst);
+            last_bar = &bar_s[jb];
+            last_ph = (uint32_t)((kt + 1) & 1);
+        }
+        if (ok && last_bar != nullptr)
+            ok = __all_sync(0xffffffffu, attn_wait(last_bar, last_ph, abort));
+        if (!ok) {
+            *abort = 1;
+            if (last_bar != nullptr)
+                (void)attn_wait(last_bar, last_ph);   // the MMAs in flight
+        }
+    } else {
+        // ---- TMA warp: tile kt into stage kt mod 2 once the products of
+        // tile kt - 2 have released it
+        int64_t k_last[kPpStages], v_last[kPpStages];   // last tile copied into a stage (-1: none)
+#pragma unroll
+        for (int s = 0; s < kPpStages; ++s) {
+            k_last[s] = s < n_tiles && s < first_stages ? s : -1;
+            v_last[s] = k_last[s];
+        }
+        // stage 1 held the query tiles' table rows until the rotation above
+        for (int64_t kt = first_stages; ok && kt < kPpStages && kt < n_tiles; ++kt) {
+            issue_key_tile<D, false>(maps, sK((int)kt), nullptr, (int)(kt * kAttnKeys), w.zkv, 0,
+                                     &bar_kfull[kt], lane);
+            issue_value_tile<D>(maps, sV((int)kt), (int)(kt * kAttnKeys), w.zkv, &bar_vfull[kt],
+                                lane);
+            k_last[kt] = v_last[kt] = kt;
+        }
+        for (int64_t kt = kPpStages; ok && kt < n_tiles; ++kt) {
+            const int st = (int)(kt % kPpStages);
+            const uint32_t free_ph = (uint32_t)(((kt / kPpStages) - 1) & 1);
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_kfree[st], free_ph, abort));
+            if (!ok)
+                break;
+            issue_key_tile<D, false>(maps, sK(st), nullptr, (int)(kt * kAttnKeys), w.zkv, 0,
+                                     &bar_kfull[st], lane);
+            k_last[st] = kt;
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_vfree[st], free_ph, abort));
+            if (!ok)
+                break;
+            issue_value_tile<D>(maps, sV(st), (int)(kt * kAttnKeys), w.zkv, &bar_vfull[st],
+                                lane);
+            v_last[st] = kt;
+        }
+        if (!ok) {
+            *abort = 1;
+            // one more bounded wait for the query tiles and the last copies
+            // into each stage
+            (void)attn_wait(&bar_q, 0u);
+#pragma unroll
+            for (int s = 0; s < kPpStages; ++s) {
+                if (k_last[s] >= 0)
+                    (void)attn_wait(&bar_kfull[s], (uint32_t)((k_last[s] / kPpStages) & 1));
+                if (v_last[s] >= 0)
+                    (void)attn_wait(&bar_vfull[s], (uint32_t)((v_last[s] / kPpStages) & 1));
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (tid == 0 && abort_flag)
+        atomicOr(a.flag, 2);
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -965,29 +1289,40 @@ static bool encode_table(EncodeTiledFn enc, CUtensorMap *m, const float *base, i
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Dynamic shared memory of one CTA: two query tiles, the key tile, two value
-// tiles and the table staging (two 128 x rotary_dim / 2 fp32 blocks at most).
-// With D = 64 the request is raised so that one CTA holds an SM (its 512 TMEM
-// columns are the whole SM's).
-static size_t attn_smem_bytes(int D)
+// Dynamic shared memory of one CTA.  rope_attn_kernel: two query tiles, the
+// key tile, two value tiles and the table staging (two 128 x rotary_dim / 2
+// fp32 blocks at most); rope_attn_pp_kernel: two query tiles and two stages
+// of key and value tiles.  With D = 64 the request is raised so that one CTA
+// holds an SM (its 512 TMEM columns are the whole SM's).
+static size_t attn_smem_bytes(int D, bool prerotated)
 {
     const size_t tile = (size_t)kAttnRows * D * 2;
-    const size_t need = kAttnBlocks * tile + tile + 2 * tile + (size_t)2 * (D / 64) * kBoxBytes;
+    const size_t need = prerotated
+                            ? kAttnBlocks * tile + 2 * kPpStages * tile
+                            : kAttnBlocks * tile + tile + 2 * tile + (size_t)2 * (D / 64) * kBoxBytes;
     const size_t one_per_sm = 120 * 1024;
     return need > one_per_sm ? need : one_per_sm;
 }
 
-template <typename T, int LAYOUT, int D, bool STAGED>
-static cudaError_t launch_attn_kernel(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
-                                      cudaStream_t st)
+// rope_attn_pp_kernel stages the query tiles' table rows when both row
+// blocks hold the same rows (two heads of a GQA group), the rows sit at
+// their own indices and rotary_dim is a multiple of 64 (whole table boxes).
+static bool pp_staged_q(const AttnArgs &a, int pair_heads)
+{
+    return pair_heads && a.pos_q == nullptr && a.rotary_dim % 64 == 0;
+}
+
+// Launches one attention kernel instance over (query tiles, head units).
+template <auto Kernel>
+static cudaError_t launch_attn(int threads, size_t smem, const AttnArgs &a, const AttnMaps &maps,
+                               int pair_heads, cudaStream_t st)
 {
     const int64_t qtiles = (a.Sq + kAttnRows - 1) / kAttnRows;
     const int64_t heads = a.B * (pair_heads ? a.Hq / 2 : a.Hq);
-    if (heads > 65535)
-        return cudaErrorInvalidConfiguration;      // grid.y limit
-    const dim3 grid((unsigned)(pair_heads ? qtiles : (qtiles + 1) / 2), (unsigned)heads);
-    auto kernel = rope_attn_kernel<T, LAYOUT, D, STAGED>;
-    const size_t smem = attn_smem_bytes(D);
+    const int64_t ytiles = pair_heads ? qtiles : (qtiles + 1) / 2;
+    if (ytiles > 65535 || heads > 0x7fffffff)
+        return cudaErrorInvalidConfiguration;      // grid.y / grid.x limits
+    const dim3 grid((unsigned)heads, (unsigned)ytiles);
     // the shared-memory limit is raised once per kernel instance and device
     static std::atomic<uint64_t> raised{0};       // bit d: done on device d (d < 64)
     int dev = 0;
@@ -996,25 +1331,40 @@ static cudaError_t launch_attn_kernel(const AttnArgs &a, const AttnMaps &maps, i
         return e;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (bit == 0 || !(raised.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
         raised.fetch_or(bit, std::memory_order_acq_rel);
     }
-    kernel<<<grid, kAttnThreads, smem, st>>>(a, maps, pair_heads);
+    Kernel<<<grid, threads, smem, st>>>(a, maps, pair_heads);
     return cudaGetLastError();
+}
+
+template <typename T, int LAYOUT, int D>
+static cudaError_t launch_attn_layout(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
+                                      cudaStream_t st)
+{
+    if (a.k_rot != nullptr) {
+        if (pp_staged_q(a, pair_heads))
+            return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true>>(
+                kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
+        return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, false>>(
+            kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
+    }
+    const size_t smem = attn_smem_bytes(D, false);
+    if (a.pos_k == nullptr && a.rotary_dim % 64 == 0)
+        return launch_attn<rope_attn_kernel<T, LAYOUT, D, true>>(kAttnThreads, smem, a, maps,
+                                                                 pair_heads, st);
+    return launch_attn<rope_attn_kernel<T, LAYOUT, D, false>>(kAttnThreads, smem, a, maps,
+                                                              pair_heads, st);
 }
 
 template <typename T, int D>
 static cudaError_t launch_attn_d(const AttnArgs &a, const AttnMaps &maps, int32_t layout,
                                  int pair_heads, cudaStream_t st)
 {
-    const bool staged = a.pos_k == nullptr && a.rotary_dim % 64 == 0;
-    if (layout == 0)
-        return staged ? launch_attn_kernel<T, 0, D, true>(a, maps, pair_heads, st)
-                      : launch_attn_kernel<T, 0, D, false>(a, maps, pair_heads, st);
-    return staged ? launch_attn_kernel<T, 1, D, true>(a, maps, pair_heads, st)
-                  : launch_attn_kernel<T, 1, D, false>(a, maps, pair_heads, st);
+    return layout == 0 ? launch_attn_layout<T, 0, D>(a, maps, pair_heads, st)
+                       : launch_attn_layout<T, 1, D>(a, maps, pair_heads, st);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
@@ -1022,6 +1372,9 @@ cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32
 {
     AttnMaps maps;
     memset(&maps, 0, sizeof maps);
+    // two heads of one GQA group per CTA when the group size is even, else
+    // two consecutive query tiles of one head
+    const int pair_heads = (a.Hq / a.Hk) % 2 == 0 ? 1 : 0;
     if (a.Sk > 0) {
         EncodeTiledFn enc = encode_tiled();
         if (enc == nullptr)
@@ -1029,17 +1382,22 @@ cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32
         const CUtensorMapDataType dt =
             dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const int64_t heads = a.B * a.Hk;
-        if (!encode_kv(enc, &maps.k, a.k, dt, heads, a.Sk, D) ||
-            !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D))
+        // keys rotated beforehand are read from the workspace, else from k;
+        // the query tiles arrive by TMA only in rope_attn_pp_kernel
+        if (!encode_kv(enc, &maps.k, a.k_rot != nullptr ? a.k_rot : a.k, dt, heads, a.Sk, D) ||
+            !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D) ||
+            (a.k_rot != nullptr && !encode_kv(enc, &maps.q, a.q, dt, a.B * a.Hq, a.Sq, D)))
             return cudaErrorInvalidValue;
-        if (a.pos_k == nullptr && a.rotary_dim % 64 == 0 &&
+        // the table boxes: of the key tiles (keys rotated in the kernel) or
+        // of the query tiles (keys rotated beforehand)
+        const bool stage_table = a.k_rot == nullptr
+                                     ? a.pos_k == nullptr && a.rotary_dim % 64 == 0
+                                     : pp_staged_q(a, pair_heads);
+        if (stage_table &&
             (!encode_table(enc, &maps.cos, a.cos, a.table_rows, a.rotary_dim / 2) ||
              !encode_table(enc, &maps.sin, a.sin, a.table_rows, a.rotary_dim / 2)))
             return cudaErrorInvalidValue;
     }
-    // two heads of one GQA group per CTA when the group size is even, else
-    // two consecutive query tiles of one head
-    const int pair_heads = (a.Hq / a.Hk) % 2 == 0 ? 1 : 0;
     if (dtype == 1)
         return D == 64 ? launch_attn_d<__nv_bfloat16, 64>(a, maps, layout, pair_heads, st)
                        : launch_attn_d<__nv_bfloat16, 128>(a, maps, layout, pair_heads, st);

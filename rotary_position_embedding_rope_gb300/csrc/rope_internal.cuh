@@ -91,6 +91,7 @@ constexpr int kMaxVectorsPerHalf = kVecThreads;
 // Attention with rotary Q/K (rope_attention.cu).
 struct AttnArgs {
     const void *q, *k, *v;
+    const void *k_rot;               // k rotated beforehand (rot(K), same layout), or nullptr
     void *o;
     const float *cos, *sin;
     const int32_t *pos_q, *pos_k;    // [Sq], [Sk] or nullptr (-1 = not rotated)

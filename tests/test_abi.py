@@ -243,11 +243,11 @@ def test_apply_out_empty_is_noop(lib):
 def attn_args(**over):
     a = dict(q=A16 * 1, k=A16 * 100, v=A16 * 200, o=A16 * 300, cos=A16 * 400, sin=A16 * 500,
              pq=None, pk=None, B=1, Hq=4, Hk=2, Sq=64, Sk=64, D=128, rd=128, layout=0, causal=1,
-             scale=-1.0, dtype=1, rows=64)
+             scale=-1.0, dtype=1, rows=64, ws=None, ws_bytes=0)
     a.update(over)
     return (a["q"], a["k"], a["v"], a["o"], a["cos"], a["sin"], a["pq"], a["pk"], a["B"], a["Hq"],
             a["Hk"], a["Sq"], a["Sk"], a["D"], a["rd"], a["layout"], a["causal"], a["scale"],
-            a["dtype"], a["rows"], None)
+            a["dtype"], a["rows"], a["ws"], a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("over,status", [
@@ -265,6 +265,12 @@ def attn_args(**over):
     (dict(rows=32), R.ROPE_ERR_INVALID_ARG),            # positions past the table
     (dict(q=A16 + 8), R.ROPE_ERR_UNSUPPORTED),          # not 16-byte aligned
     (dict(scale=float("nan")), R.ROPE_ERR_INVALID_ARG),
+    # key workspace: B * Hk * Sk * D * 2 = 32768 bytes, aligned, disjoint
+    (dict(ws=A16 * 600, ws_bytes=32767), R.ROPE_ERR_INVALID_ARG),       # too small
+    (dict(ws=A16 * 600 + 8, ws_bytes=32768), R.ROPE_ERR_UNSUPPORTED),   # not 16-byte aligned
+    (dict(ws=A16 * 100 + 16, ws_bytes=32768), R.ROPE_ERR_INVALID_ARG),  # over k
+    (dict(ws=A16 * 300 + 16, ws_bytes=32768), R.ROPE_ERR_INVALID_ARG),  # over o
+    (dict(ws=A16 * 400, ws_bytes=32768), R.ROPE_ERR_INVALID_ARG),       # over the cos table
 ])
 def test_attention_rejects_bad_arguments(lib, over, status):
     assert lib.rope_attention_fwd(*attn_args(**over)) == status

@@ -1,5 +1,7 @@
 """Attention with the rotation fused into the Q/K tile loads (tcgen05) against
-the fp64 rotary-attention oracle.
+the fp64 rotary-attention oracle, on both key paths: keys rotated inside the
+attention kernel (no workspace) and keys rotated once into a workspace by the
+rotation kernel.  The two paths give the same bits.
 
 Tolerance: the kernel rounds P to the element type before the P.V product and
 rounds O once; each is within half a unit in the last place, so per element
@@ -58,9 +60,13 @@ CASES = [
 ]
 
 
+WS = {"ws": "auto", "inkernel": None}     # key workspace, or keys rotated in the kernel
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
 @pytest.mark.parametrize("c", CASES, ids=lambda c: "Sq%d_Sk%d_D%d_rd%d_%s_%s_c%d" % (
     c["Sq"], c["Sk"], c["D"], c["rd"], c["dtype"], c["layout"], c["causal"]))
-def test_attention_against_oracle(c):
+def test_attention_against_oracle(c, ws):
     require_gpu()
     R = lib()
     q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], 31)
@@ -68,13 +74,14 @@ def test_attention_against_oracle(c):
     c32, s32 = oracle_tables(1e4, c["rd"], rows)
     cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
     o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, rotary_dim=c["rd"], layout=c["layout"],
-                    causal=c["causal"])
+                    causal=c["causal"], k_workspace=WS[ws])
     assert R.rope_check_errors() == R.ROPE_OK
     _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, None, None,
            c["causal"], str(c))
 
 
-def test_pages_example_cls_tokens_unrotated():
+@pytest.mark.parametrize("ws", sorted(WS))
+def test_pages_example_cls_tokens_unrotated(ws):
     """q, k, v [1, 8, 1024 + 2, 64], rotary dim 32, the first 2 tokens not
     rotated and the rest at positions 0..1023 ("rotary-embedding-torch",
     flash_attn_with_rotary example), causal."""
@@ -87,7 +94,7 @@ def test_pages_example_cls_tokens_unrotated():
     cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
     pg = torch.from_numpy(pos).cuda()
     o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=pg, pos_k=pg, rotary_dim=32,
-                    causal=True)
+                    causal=True, k_workspace=WS[ws])
     assert R.rope_check_errors() == R.ROPE_OK
     _check(o, q, k, v, "bf16", 32, O.SPLIT_HALF, c32, s32, pos, pos, True, "pages example")
 
@@ -109,7 +116,8 @@ def test_attention_with_no_keys_is_zero_and_shift_invariant():
     assert float((a.float() - b.float()).abs().max()) < 0.05
 
 
-def test_attention_gathered_positions_interleaved():
+@pytest.mark.parametrize("ws", sorted(WS))
+def test_attention_gathered_positions_interleaved(ws):
     """Per-token positions (a shuffled set, some -1) with the interleaved
     layout: the key rotation reads each row's table row by its position."""
     require_gpu()
@@ -124,7 +132,7 @@ def test_attention_gathered_positions_interleaved():
     cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
     o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, pos_q=torch.from_numpy(pq).cuda(),
                     pos_k=torch.from_numpy(pk).cuda(), rotary_dim=64, layout="interleaved",
-                    causal=False)
+                    causal=False, k_workspace=WS[ws])
     assert R.rope_check_errors() == R.ROPE_OK
     _check(o, q, k, v, "f16", 64, O.INTERLEAVED, c32, s32, pq, pk, False, "gathered positions")
 
@@ -146,7 +154,9 @@ def _fuzz_cases(n=24, seed=2024):
 
 @pytest.mark.parametrize("c", _fuzz_cases(), ids=lambda c: "fuzz%02d" % c["i"])
 def test_attention_fuzz(c):
-    """Seeded random shapes, spans, layouts, types, masks and positions."""
+    """Seeded random shapes, spans, layouts, types, masks and positions; the
+    workspace path against the oracle, the in-kernel key path bit for bit
+    against it."""
     require_gpu()
     R = lib()
     q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], c["seed"])
@@ -158,10 +168,13 @@ def test_attention_fuzz(c):
         pk = g.integers(-1, rows, c["Sk"]).astype(np.int32)
     c32, s32 = oracle_tables(1e4, c["rd"], rows)
     cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
-    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg,
-                    pos_q=None if pq is None else torch.from_numpy(pq).cuda(),
-                    pos_k=None if pk is None else torch.from_numpy(pk).cuda(),
-                    rotary_dim=c["rd"], layout=c["layout"], causal=c["causal"])
+    args = (q.cuda(), k.cuda(), v.cuda(), cg, sg)
+    kw = dict(pos_q=None if pq is None else torch.from_numpy(pq).cuda(),
+              pos_k=None if pk is None else torch.from_numpy(pk).cuda(),
+              rotary_dim=c["rd"], layout=c["layout"], causal=c["causal"])
+    o = R.attention(*args, **kw)
+    o_in = R.attention(*args, k_workspace=None, **kw)
     assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(o.view(torch.int16), o_in.view(torch.int16)), "key paths differ"
     _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, pq, pk, c["causal"],
            str(c))
