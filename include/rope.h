@@ -252,6 +252,36 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
                                void *stream);
 
 /*
+ * rope_attention_fwd_noalloc -- rope_attention_fwd with the key workspace
+ * taken from a fixed device array inside this library (32 MiB), for callers
+ * that cannot allocate device memory at call time: an engine that has
+ * reserved the device's memory for its own pool, plugin code limited to the
+ * buffers its host framework hands it, or a latency-critical path that
+ * cannot afford cudaMalloc.  The pages have no counterpart of this entry
+ * point; it is an addition of this library.
+ *
+ * Arguments, result and errors: as rope_attention_fwd with k_workspace set,
+ * except that rot(K) goes to the library's array.  ROPE_ERR_UNSUPPORTED when
+ * B * Hk * Sk * D * 2 bytes exceed 32 MiB (33554432 bytes), before anything
+ * touches the device.  Nothing is allocated or freed, and no allocating
+ * library routine is called.
+ * Set-up: the first call on a device (with that device current) looks up the
+ *    array's device address once (cudaGetSymbolAddress) and caches it; make
+ *    that first call before any stream capture.
+ * Sharing: every device that loads the library holds the 32 MiB array until
+ *    the process exits.  All calls on a device share it; each call rewrites
+ *    the part it uses before reading it (nothing needs to start at zero), and
+ *    calls whose work overlaps on the GPU (on streams not ordered with each
+ *    other) race on it.
+ */
+rope_status rope_attention_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
+                                       const float *cos, const float *sin, const int32_t *pos_q,
+                                       const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk,
+                                       int64_t Sq, int64_t Sk, int32_t D, int32_t rotary_dim,
+                                       int32_t layout, int32_t causal, float softmax_scale,
+                                       int32_t dtype, int64_t table_rows, void *stream);
+
+/*
  * rope_check_errors -- synchronise `stream`, then report and clear the
  * current device's error flag.
  * Returns ROPE_ERR_CUDA if the stream reports an error, else

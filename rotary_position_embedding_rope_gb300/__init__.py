@@ -34,7 +34,7 @@ __all__ = [
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
     "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
-    "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
+    "rope_attention_fwd_noalloc", "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
     "build_tables_ex", "apply_qk_xpos",
 ]
 
@@ -106,6 +106,11 @@ def load_library() -> ctypes.CDLL:
                                        c.c_int32, c.c_float, c.c_int32, c.c_int64, P,
                                        c.c_int64, P]
     lib.rope_attention_fwd.restype = c.c_int
+    lib.rope_attention_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, c.c_int64, c.c_int32,
+                                               c.c_int32, c.c_int64, c.c_int64, c.c_int32,
+                                               c.c_int32, c.c_int32, c.c_int32, c.c_float,
+                                               c.c_int32, c.c_int64, P]
+    lib.rope_attention_fwd_noalloc.restype = c.c_int
     lib.rope_force_kernel_variant.argtypes = [c.c_int32]
     lib.rope_force_kernel_variant.restype = c.c_int
     _lib = lib
@@ -399,6 +404,24 @@ def rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D,
                                 _addr(k_workspace, "k_workspace"), int(workspace_bytes),
                                 _stream(stream))
     _check(st, "rope_attention_fwd")
+
+
+def rope_attention_fwd_noalloc(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D,
+                               rotary_dim, layout, causal, softmax_scale, dtype, table_rows,
+                               stream=None):
+    """rope_attention_fwd with the rot(K) buffer taken from the library's own
+    32 MiB device array: for callers that cannot allocate device memory when
+    they call (their memory is all reserved by their own pool, or they may
+    only use buffers their host framework gives them).  Allocates nothing."""
+    lib = load_library()
+    st = lib.rope_attention_fwd_noalloc(_addr(q, "q"), _addr(k, "k"), _addr(v, "v"),
+                                        _addr(o, "o"), _addr(cos, "cos"), _addr(sin, "sin"),
+                                        _addr(pos_q, "pos_q"), _addr(pos_k, "pos_k"), int(B),
+                                        int(Hq), int(Hk), int(Sq), int(Sk), int(D),
+                                        int(rotary_dim), int(layout), int(causal),
+                                        float(softmax_scale), int(dtype), int(table_rows),
+                                        _stream(stream))
+    _check(st, "rope_attention_fwd_noalloc")
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor,
