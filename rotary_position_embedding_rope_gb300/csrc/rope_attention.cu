@@ -510,11 +510,11 @@ __device__ __forceinline__ void rotate_tile(uint8_t *sK, const uint8_t *sT, int6
         KeyItem x[NF];
 #pragma unroll
         for (int f = 0; f < NF; ++f)
-            if (i + f * NT < items)
+            if (f == 0 || i + f * NT < items)
                 load_key_item<T, LAYOUT, STAGED>(x[f], i + f * NT, sK, sT, k0, pos, S, a);
 #pragma unroll
         for (int f = 0; f < NF; ++f)
-            if (i + f * NT < items)
+            if (f == 0 || i + f * NT < items)
                 store_key_item<T, LAYOUT>(x[f], sK);
     }
 }
@@ -597,6 +597,42 @@ __device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_he
     return w;
 }
 
+// Packed pairs of fp32 values (Blackwell's f32x2 arithmetic: one instruction
+// for two lanes' worth of fma or add, each rounded as its scalar form).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_split(uint64_t r, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // One online-softmax step of query row qi on the key tile at k0.  The row's
 // S = Q K^T sits in TMEM columns [acc, acc + 128) of its lane and its O in
 // [acc + 128, acc + 128 + D).  The 128 S values are read once and held in
@@ -608,7 +644,13 @@ __device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_he
 // partial results, so no long chain of dependent instructions sets the
 // latency.  Warp-collective; the caller waits for the TMEM stores before
 // signalling that P is ready.
-template <typename T, int D>
+//
+// PACKED: the scale-and-subtract and the partial sums use f32x2 pairs (one
+// instruction per two keys); otherwise the same operations one lane at a
+// time, in the same order, so both forms give the same bits (the scalar one
+// needs fewer registers: rope_attn_kernel, whose key rotation holds more
+// values live, would spill with the pairs).
+template <typename T, int D, bool PACKED>
 __device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int64_t k0,
                                              int64_t shift, const AttnArgs &a, bool not_first,
                                              float &m_ref, float &l_run)
@@ -635,10 +677,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int6
     for (int r = 0; r < 8; ++r)
         m8[r] = sv[r];
 #pragma unroll
-    for (int i = 8; i < kAttnKeys; ++i)
-        m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
-    float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    for (int i = 8; i < kAttnKeys; i += 2)
+        m8[(i >> 1) & 7] = fmax3(m8[(i >> 1) & 7], sv[i], sv[i + 1]);
+    float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
     mx *= a.scale_log2;                    // scale > 0: max commutes with it
     // The exponentials use a reference max m_ref that only moves when the
     // row max exceeds it by more than 8 (factor 256): P stays <= 256, exact
@@ -651,14 +692,41 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int6
     // m_ref is -inf only while the row has seen no visible key; every key
     // of this tile is then masked (-inf) and gives 2^-inf = 0
     const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
-    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // s * scale - m and the partial sums of the even and the odd keys,
+    // four of each
     uint32_t w[kAttnKeys / 2];
+    float s4[4];
+    if constexpr (PACKED) {
+        const uint64_t scale2 = f32x2(a.scale_log2, a.scale_log2), neg_m2 = f32x2(neg_m, neg_m);
+        uint64_t sum2[4] = {0, 0, 0, 0};           // (even, odd) pairs of +0.0f
 #pragma unroll
-    for (int i = 0; i < kAttnKeys; i += 2) {
-        const float p0 = fast_exp2(fmaf(sv[i], a.scale_log2, neg_m));
-        const float p1 = fast_exp2(fmaf(sv[i + 1], a.scale_log2, neg_m));
-        s4[(i >> 1) & 3] += p0 + p1;
-        w[i >> 1] = Elt<T>::f2_to_word(p0, p1);
+        for (int i = 0; i < kAttnKeys; i += 2) {
+            float t0, t1;
+            f32x2_split(fma_f32x2(f32x2(sv[i], sv[i + 1]), scale2, neg_m2), t0, t1);
+            const float p0 = fast_exp2(t0);
+            const float p1 = fast_exp2(t1);
+            sum2[(i >> 1) & 3] = add_f32x2(sum2[(i >> 1) & 3], f32x2(p0, p1));
+            w[i >> 1] = Elt<T>::f2_to_word(p0, p1);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float e, o;
+            f32x2_split(sum2[r], e, o);
+            s4[r] = e + o;
+        }
+    } else {
+        float se[4] = {0.0f, 0.0f, 0.0f, 0.0f}, so[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < kAttnKeys; i += 2) {
+            const float p0 = fast_exp2(fmaf(sv[i], a.scale_log2, neg_m));
+            const float p1 = fast_exp2(fmaf(sv[i + 1], a.scale_log2, neg_m));
+            se[(i >> 1) & 3] += p0;
+            so[(i >> 1) & 3] += p1;
+            w[i >> 1] = Elt<T>::f2_to_word(p0, p1);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            s4[r] = se[r] + so[r];
     }
     // keys 2c, 2c + 1 -> column c (the even key in the low half)
 #pragma unroll
@@ -795,7 +863,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = __all_sync(0xffffffffu, attn_wait(&bar_k, ph, abort));
             if (!ok)
                 break;
-            rotate_tile<T, LAYOUT, STAGED, kMathThreads, 2>(sK, sT, k0, a.pos_k, a.Sk, a, tid);
+            // one item at a time: with the softmax's 128 S values this
+            // kernel has no registers left for a second item in flight
+            rotate_tile<T, LAYOUT, STAGED, kMathThreads, 1>(sK, sT, k0, a.pos_k, a.Sk, a, tid);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(&bar_krot);
             // 2. this block's S = Q K^T is ready; its O += P V of the previous
@@ -806,7 +876,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // 3. online softmax; P goes back into TMEM over S
-            softmax_tile<T, D>(acc_base, qi, k0, shift, a, kt > 0, m_ref, l_run);
+            softmax_tile<T, D, false>(acc_base, qi, k0, shift, a, kt > 0, m_ref, l_run);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
@@ -988,7 +1058,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
     // 128 threads), per block
     __shared__ __align__(8) uint64_t bar_kfull[kPpStages], bar_kfree[kPpStages],
         bar_vfull[kPpStages], bar_vfree[kPpStages], bar_s[kAttnBlocks], bar_o[kAttnBlocks],
-        bar_p[kAttnBlocks], bar_q;
+        bar_p[kAttnBlocks], bar_q, bar_sm[kAttnBlocks];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -1022,6 +1092,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
             mbar_init(&bar_s[blk], 1);
             mbar_init(&bar_o[blk], 1);
             mbar_init(&bar_p[blk], kAttnRows);
+            mbar_init(&bar_sm[blk], kAttnRows);
         }
         mbar_init(&bar_q, 1);
         abort_flag = 0;
@@ -1080,12 +1151,22 @@ __global__ void __launch_bounds__(kPpThreads, 1)
         float m_ref = -INFINITY, l_run = 0.0f;
         for (int64_t kt = 0; kt < n_tiles; ++kt) {
             // S of this block is ready (its previous O += P V has finished:
-            // the MMA warp waited for it before issuing S)
-            ok = __all_sync(0xffffffffu, attn_wait(&bar_s[j], (uint32_t)(kt & 1), abort));
+            // the issuer waited for it before issuing S), and it is this
+            // block's turn: the softmax steps alternate between the blocks
+            // (block 0 on tile kt after block 1 on tile kt - 1, block 1 after
+            // block 0 on the same tile), so each has the exponential unit to
+            // itself while the tensor cores run the other block's products
+            ok = __all_sync(0xffffffffu,
+                            attn_wait(&bar_s[j], (uint32_t)(kt & 1), abort) &&
+                                (j == 0 ? kt == 0 || attn_wait(&bar_sm[1], (uint32_t)((kt - 1) & 1),
+                                                               abort)
+                                        : attn_wait(&bar_sm[0], (uint32_t)(kt & 1), abort)));
             if (!ok)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            softmax_tile<T, D>(acc_base, qi, kt * kAttnKeys, shift, a, kt > 0, m_ref, l_run);
+            softmax_tile<T, D, true>(acc_base, qi, kt * kAttnKeys, shift, a, kt > 0, m_ref,
+                                     l_run);
+            mbar_arrive(&bar_sm[j]);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
