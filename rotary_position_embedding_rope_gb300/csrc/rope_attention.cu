@@ -552,34 +552,36 @@ __device__ __forceinline__ void issue_value_tile(const AttnMaps &m, uint8_t *sV,
         tma_load_3d(sV + lane * kBoxBytes, &m.v, lane * 64, k0, zkv, bar);
 }
 
-// The work of one CTA: batch b and key/value head zkv = b * Hk + hk; row
+// The work of one CTA (or CTA pair) on query tile qtile of (batch, head)
+// unit `unit`: batch b and key/value head zkv = b * Hk + hk; row
 // block j holds query head hq_first + j * hq_step, rows q0_first + j * q_step
 // .. + 127 (two query heads of one GQA group when pair_heads, else two
 // consecutive query tiles of one head); n_tiles = the key tiles those rows
-// can see.  blockIdx.x is the (batch, head) unit and blockIdx.y the query
-// tile, last tile first: the hardware hands out blocks x fastest, so under a
-// causal mask every CTA of the longest query tiles starts before any of the
-// shorter ones (longest job first; the short ones fill the end).
+// can see.  The one-unit-per-CTA kernels take unit = blockIdx.x and the query
+// tiles last first along blockIdx.y: the hardware hands out blocks x fastest,
+// so under a causal mask every CTA of the longest query tiles starts before
+// any of the shorter ones (longest job first; the short ones fill the end).
 struct AttnWork {
     int64_t b, q0_first, q_step, n_tiles;
     int32_t hq_first, hq_step, zkv;
 };
 
-__device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_heads)
+__device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_heads,
+                                              uint32_t unit, int64_t qtile)
 {
     AttnWork w;
     if (pair_heads) {
         const int32_t pairs = a.Hq / 2;
-        w.b = blockIdx.x / pairs;
-        w.hq_first = (int32_t)(blockIdx.x - w.b * pairs) * 2;
+        w.b = unit / pairs;
+        w.hq_first = (int32_t)(unit - w.b * pairs) * 2;
         w.hq_step = 1;
-        w.q0_first = (int64_t)(gridDim.y - 1 - blockIdx.y) * kAttnRows;
+        w.q0_first = qtile * kAttnRows;
         w.q_step = 0;
     } else {
-        w.b = blockIdx.x / a.Hq;
-        w.hq_first = (int32_t)(blockIdx.x - w.b * a.Hq);
+        w.b = unit / a.Hq;
+        w.hq_first = (int32_t)(unit - w.b * a.Hq);
         w.hq_step = 0;
-        w.q0_first = (int64_t)(gridDim.y - 1 - blockIdx.y) * 2 * kAttnRows;
+        w.q0_first = qtile * 2 * kAttnRows;
         w.q_step = kAttnRows;
     }
     w.zkv = (int32_t)(w.b * a.Hk + w.hq_first / (a.Hq / a.Hk));
@@ -635,7 +637,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
 
 // One online-softmax step of query row qi on the key tile at k0.  The row's
 // S = Q K^T sits in TMEM columns [acc, acc + 128) of its lane and its O in
-// [acc + 128, acc + 128 + D).  The 128 S values are read once and held in
+// [o_base, o_base + D).  The 128 S values are read once and held in
 // registers.  Computes the row max over the visible keys, moves the lazy
 // reference max m_ref when needed, writes P = 2^(s * scale * log2(e) -
 // m_ref) as packed 16-bit values over the first 64 columns of S, updates the
@@ -650,10 +652,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
 // time, in the same order, so both forms give the same bits (the scalar one
 // needs fewer registers: rope_attn_kernel, whose key rotation holds more
 // values live, would spill with the pairs).
-template <typename T, int D, bool PACKED>
-__device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int64_t k0,
-                                             int64_t shift, const AttnArgs &a, bool not_first,
-                                             float &m_ref, float &l_run)
+struct ONoWait {
+    __device__ __forceinline__ bool operator()() const { return true; }
+};
+
+template <typename T, int D, bool PACKED, typename OReady = ONoWait>
+__device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base, int64_t qi,
+                                             int64_t k0, int64_t shift, const AttnArgs &a,
+                                             bool not_first, float &m_ref, float &l_run,
+                                             const OReady &o_ready = OReady())
 {
     // columns of this tile visible to this row: [0, nvis)
     int64_t vis_end = a.Sk;                // first invisible key
@@ -733,24 +740,27 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, int64_t qi, int6
     for (int c = 0; c < kAttnKeys / 2; c += 16)
         tmem_st16(acc_base + c, *reinterpret_cast<const uint32_t(*)[16]>(w + c));
     l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-    if (not_first && __any_sync(0xffffffffu, alpha != 1.0f)) {   // rescale O rows of this warp
+    // rescale O rows of this warp; o_ready() waits until no product still
+    // writes O (a warp-uniform false, its wait expired, skips the rescale)
+    if (not_first && __any_sync(0xffffffffu, alpha != 1.0f) && o_ready()) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
             float ov[32];
-            tmem_ld32(acc_base + kAttnKeys + c0, ov);
+            tmem_ld32(o_base + c0, ov);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 ov[i] *= alpha;
-            tmem_st32(acc_base + kAttnKeys + c0, ov);
+            tmem_st32(o_base + c0, ov);
         }
     }
 }
 
-// Epilogue of query row qi: O / l from TMEM columns [acc + 128, acc + 128 +
-// D), rounded once, to the row of O (zeros when the row saw no key).  TMEM
+// Epilogue of query row qi: O / l from TMEM columns [o_base, o_base + D),
+// rounded once, to the row of O (zeros when the row saw no key).  TMEM
 // loads are warp-wide; rows at or past Sq store nothing.
 template <typename T, int D>
-__device__ __forceinline__ void store_o_row(uint32_t acc_base, T *O, int64_t qi, int64_t Sq,
+__device__ __forceinline__ void store_o_row(uint32_t o_base, T *O, int64_t qi, int64_t Sq,
                                             bool any_key, float l_run)
 {
     const float inv = (any_key && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
@@ -759,7 +769,7 @@ __device__ __forceinline__ void store_o_row(uint32_t acc_base, T *O, int64_t qi,
     for (int c0 = 0; c0 < D; c0 += 32) {
         float ov[32];
         if (any_key) {
-            tmem_ld32(acc_base + kAttnKeys + c0, ov);
+            tmem_ld32(o_base + c0, ov);
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -803,7 +813,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int j = math ? warp >> 2 : 0;            // row block of this warp
     const int wq = warp & 3;                       // TMEM lane quarter
     const int row = tid & (kAttnRows - 1);
-    const AttnWork w = attn_work(a, pair_heads);
+    const AttnWork w = attn_work(a, pair_heads, blockIdx.x, gridDim.y - 1 - blockIdx.y);
     const int32_t hq = w.hq_first + j * w.hq_step;
     const int zkv = w.zkv;
     const int64_t q0 = w.q0_first + j * w.q_step;
@@ -876,7 +886,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // 3. online softmax; P goes back into TMEM over S
-            softmax_tile<T, D, false>(acc_base, qi, k0, shift, a, kt > 0, m_ref, l_run);
+            softmax_tile<T, D, false>(acc_base, acc_base + kAttnKeys, qi, k0, shift, a, kt > 0,
+                                      m_ref, l_run);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
@@ -889,7 +900,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             *abort = 1;
         } else {
             // epilogue: O / l for this row
-            store_o_row<T, D>(acc_base, O, qi, a.Sq, n_tiles > 0, l_run);
+            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, n_tiles > 0, l_run);
         }
     } else {
         // ---- issue warp: TMA copies one tile ahead, the MMAs (lane 0)
@@ -1067,7 +1078,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
     const int j = math ? warp >> 2 : 0;
     const int wq = warp & 3;
     const int row = tid & (kAttnRows - 1);
-    const AttnWork w = attn_work(a, pair_heads);
+    const AttnWork w = attn_work(a, pair_heads, blockIdx.x, gridDim.y - 1 - blockIdx.y);
     const int32_t hq = w.hq_first + j * w.hq_step;
     const int64_t q0 = w.q0_first + j * w.q_step;
     const int64_t qi = q0 + row;
@@ -1164,8 +1175,8 @@ __global__ void __launch_bounds__(kPpThreads, 1)
             if (!ok)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            softmax_tile<T, D, true>(acc_base, qi, kt * kAttnKeys, shift, a, kt > 0, m_ref,
-                                     l_run);
+            softmax_tile<T, D, true>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
+                                     kt > 0, m_ref, l_run);
             mbar_arrive(&bar_sm[j]);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1179,7 +1190,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
         if (!ok)
             *abort = 1;
         else
-            store_o_row<T, D>(acc_base, O, qi, a.Sq, n_tiles > 0, l_run);
+            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, n_tiles > 0, l_run);
     } else if (warp < kPpTmaWarp) {
         // ---- MMA issue of row block jb (lane 0 issues; the waits are warp-wide)
         const int jb = warp - kPpMmaWarp;
@@ -1317,6 +1328,483 @@ __global__ void __launch_bounds__(kPpThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Attention over keys rotated beforehand, on pairs of SMs (a cluster of two
+// CTAs and tcgen05 MMAs with cta_group::2: M = 256, the two CTAs' row blocks
+// stacked).  Each CTA owns one 128-row block (two heads of a GQA group, or
+// two consecutive query tiles of one head, as the row blocks of
+// rope_attn_pp_kernel) and holds half of every key tile (64 keys) and half of
+// every value tile (64 of the 128 feature columns); the leader CTA (rank 0)
+// issues the MMAs of both.  One instruction now covers 256 rows, half as
+// many per flop as with M = 128, and with one row block per CTA its TMEM has
+// room for three S buffers: S(kt + 1) and S(kt + 2) are computed while the
+// softmax of S(kt) runs, and no S waits for the previous O += P V.
+//
+// 224 threads per CTA: warps 0-3 the row block (thread t = row t), warp 4 the
+// leader's S issue, warp 5 the leader's O += P V issue, warp 6 the TMA copies
+// of its CTA (the follower's count their bytes on the leader's barriers).
+// TMEM columns: S buffers at 0, 128 and 256, O at 384.  Shared memory: the query
+// tile, three stages of (key half, value half), the query tile's table rows.
+// The CTAs meet through mbarriers: multicast MMA commits reach both, the
+// follower's arrivals and copies reach the leader's barriers.  Every wait is
+// bounded; a role whose wait expires raises the abort flag of both CTAs.
+// ---------------------------------------------------------------------------
+constexpr int k2Stages = 3;
+constexpr int k2SIssueWarp = 4;                    // leader: S issue
+constexpr int k2PVIssueWarp = 5;
+constexpr int k2TmaWarp = 6;
+constexpr int k2Threads = 7 * 32;
+constexpr int k2SBufs = 3;                         // S buffers in TMEM
+constexpr uint32_t k2OCol = k2SBufs * kAttnKeys;   // TMEM column of O (384)
+constexpr uint32_t k2Half = 16384;                 // bytes of a CTA's half key or value tile
+
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t cta)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(attn_smem_u32(p)), "r"(cta));
+    return r;
+}
+
+// Arrival on a barrier of the peer CTA, without a cluster-scope release
+// fence (that fence costs ~1.4 k cycles inside this kernel).  Used after
+// tcgen05.wait::st and tcgen05.fence::before_thread_sync: the tensor-memory
+// stores it announces have completed before the arrival is issued.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion (bytes) is
+// counted on a barrier of the CTA pair's leader (cluster address).
+__device__ __forceinline__ void tma_load_3d_to_leader(void *dst, const CUtensorMap *map, int x, int y,
+                                                      int z, uint32_t leader_bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::"
+                 "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                 ::"r"(attn_smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(leader_bar)
+                 : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (the barrier may be completed by
+// the peer CTA); false on expiry or once *abort is raised.
+__device__ __forceinline__ bool attn_wait_cl(uint64_t *bar, uint32_t parity,
+                                             const volatile int *abort = nullptr)
+{
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(attn_smem_u32(bar)), "r"(parity)
+                     : "memory");
+        if (done)
+            return true;
+        if ((abort != nullptr && *abort) || clock64() - t0 > kAttnWaitCycles)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void umma2_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Commit of the issuing thread's earlier MMAs to the barrier at the same
+// shared-memory offset in every CTA of cta_mask.
+__device__ __forceinline__ void umma2_commit(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::"
+                 "cluster.b64 [%0], %1;"
+                 ::"r"(attn_smem_u32(bar)), "h"(cta_mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <typename T, int LAYOUT, bool STAGED_Q>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
+    rope_attn_2sm_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps,
+                         const int32_t pair_heads)
+{
+    constexpr int D = 128;
+    constexpr uint32_t kTile = kAttnRows * D * 2;  // the query tile
+    constexpr uint32_t ab_format = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *sQ = smem;
+    uint8_t *sStages = sQ + kTile;
+    uint8_t *sT = sStages + k2Stages * 2 * k2Half;     // the query tile's table rows
+    auto sK = [&](int st) { return sStages + st * 2 * k2Half; };
+    auto sV = [&](int st) { return sStages + st * 2 * k2Half + k2Half; };
+    // both CTAs' key / value halves landed (leader only: TMA bytes of both),
+    // stage released (multicast commits); S buffer ready (multicast); P
+    // ready (leader only: each row warp of both CTAs arrives); the O += P V
+    // that read P from S buffer b done (multicast); query tile landed; both
+    // query tiles rotated (leader only: each row warp arrives); every MMA of
+    // the S / the P V issuer finished (leader, once at the end).
+    // A parity wait is only sound for the phase right after the last one
+    // known to have completed (a barrier two phases away from the awaited one
+    // reads as complete, or as never completing): every barrier below is
+    // waited for that way, which is why O += P V completes one barrier per S
+    // buffer.
+    __shared__ __align__(8) uint64_t bar_kfull[k2Stages], bar_vfull[k2Stages],
+        bar_kfree[k2Stages], bar_vfree[k2Stages], bar_s[k2SBufs], bar_p[k2SBufs], bar_o[k2SBufs],
+        bar_q, bar_qr, bar_drain[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const bool leader = rank == 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool math = warp < 4;
+    // the work units, longest query tile first: unit L is query tile
+    // ytiles - 1 - L / heads_units of (batch, head) unit L mod heads_units;
+    // cluster c takes units c, c + clusters, ...
+    const int64_t qtiles = (a.Sq + kAttnRows - 1) / kAttnRows;
+    const int64_t heads_units = a.B * (pair_heads ? a.Hq / 2 : a.Hq);
+    const int64_t ytiles = pair_heads ? qtiles : (qtiles + 1) / 2;
+    const int64_t n_units = heads_units * ytiles;
+    const int64_t clusters = gridDim.x >> 1, cid = blockIdx.x >> 1;
+    auto unit_work = [&](int64_t L) {
+        return attn_work(a, pair_heads, (uint32_t)(L % heads_units), ytiles - 1 - L / heads_units);
+    };
+    const int64_t shift = a.Sk - a.Sq;
+    const int tboxes = a.rotary_dim / 64;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(attn_smem_u32(&tmem_base)), "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int s = 0; s < k2Stages; ++s) {
+            mbar_init(&bar_kfull[s], 1);
+            mbar_init(&bar_vfull[s], 1);
+            mbar_init(&bar_kfree[s], 1);
+            mbar_init(&bar_vfree[s], 1);
+        }
+        for (int b = 0; b < k2SBufs; ++b) {
+            mbar_init(&bar_s[b], 1);
+            mbar_init(&bar_p[b], 2 * (kAttnRows / 32));
+            mbar_init(&bar_o[b], 1);
+        }
+        mbar_init(&bar_q, 1);
+        mbar_init(&bar_qr, 2 * (kAttnRows / 32));
+        mbar_init(&bar_drain[0], 1);
+        mbar_init(&bar_drain[1], 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync_all();                            // barriers and TMEM of both CTAs ready
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base;
+    volatile int *abort = &abort_flag;
+    const uint32_t peer_abort = peer_addr(&abort_flag, rank ^ 1u);
+    auto raise_abort = [&]() {
+        *abort = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+    };
+    bool ok = true;
+
+    if (math) {
+        // ---- the row block: per unit, rotate the query tile, then the
+        // softmax of row qi on S buffer g mod 3 (g counts this CTA's tiles)
+        const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+        const uint32_t o_base = tmem + k2OCol + lanes;
+        int64_t g = 0;
+        uint32_t qn = 0;                           // units with key tiles so far
+        for (int64_t L = cid; ok && L < n_units; L += clusters) {
+            const AttnWork w = unit_work(L);
+            const int32_t hq = w.hq_first + (int32_t)rank * w.hq_step;
+            const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
+            const int64_t qi = q0 + tid;
+            T *O = static_cast<T *>(a.o) + ((w.b * a.Hq + hq) * a.Sq) * D;
+            const int64_t n_tiles = w.n_tiles;     // the same in both CTAs
+            float m_ref = -INFINITY, l_run = 0.0f;
+            if (n_tiles > 0) {
+                ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_q, qn & 1u, abort));
+                if (!ok)
+                    break;
+                rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(sQ, sT, q0, a.pos_q, a.Sq, a, tid);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // this warp's rows are rotated: one arrival per row warp of
+                // both CTAs on the leader's barrier (once per unit, with a
+                // cluster-scope release for the shared-memory stores)
+                __syncwarp();
+                if (lane == 0)
+                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                                 ::"r"(peer_addr(&bar_qr, 0))
+                                 : "memory");
+                ++qn;
+            }
+            for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
+                const int b = (int)(g % k2SBufs);
+                ok = __all_sync(0xffffffffu,
+                                attn_wait_cl(&bar_s[b], (uint32_t)((g / k2SBufs) & 1), abort));
+                if (!ok)
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                // O may still be updated by the products of tiles g - 2 and
+                // g - 1 (that of g - 3 had finished before S(g) was issued): a
+                // rescale waits for the later one, which finishes after the
+                // earlier (rare: the row max moved by more than 8)
+                bool o_ok = true;
+                auto o_ready = [&]() {
+                    const int64_t gp = g - 1;
+                    o_ok = __all_sync(0xffffffffu,
+                                      attn_wait_cl(&bar_o[gp % k2SBufs],
+                                                   (uint32_t)((gp / k2SBufs) & 1), abort));
+                    return o_ok;
+                };
+                softmax_tile<T, D, true>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
+                                         kt * kAttnKeys, shift, a, kt > 0, m_ref, l_run, o_ready);
+                ok = o_ok;
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                // this warp's P rows are in TMEM: one arrival per row warp of
+                // both CTAs on the leader's barrier
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(&bar_p[b]);
+                    else
+                        mbar_arrive_remote(peer_addr(&bar_p[b], 0));
+                }
+                if (!ok)
+                    break;
+            }
+            if (!ok)
+                break;
+            // the unit's last O += P V (products finish in order), then O / l
+            if (n_tiles > 0) {
+                const int64_t gp = g - 1;
+                ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_o[gp % k2SBufs],
+                                                          (uint32_t)((gp / k2SBufs) & 1), abort));
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (!ok)
+                break;
+            store_o_row<T, D>(o_base, O, qi, a.Sq, n_tiles > 0, l_run);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        }
+        if (!ok)
+            raise_abort();
+    } else if (warp == k2SIssueWarp && leader) {
+        // ---- S = Q K^T for both CTAs into S buffer g mod 3
+        const uint32_t idesc = umma_idesc(256, kAttnKeys, ab_format, 0);
+        const uint32_t q_addr = attn_smem_u32(sQ);
+        int64_t g = 0;
+        uint32_t qn = 0;
+        for (int64_t L = cid; ok && L < n_units; L += clusters) {
+            const int64_t n_tiles = unit_work(L).n_tiles;
+            if (n_tiles == 0)
+                continue;
+            // both CTAs' query tiles of this unit are rotated
+            ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_qr, qn & 1u, abort));
+            ++qn;
+            for (int64_t kt = 0; ok && kt < n_tiles; ++kt, ++g) {
+                const int st = (int)(g % k2Stages), b = (int)(g % k2SBufs);
+                // both key halves landed; the product that read P from this S
+                // buffer (tile g - 3) has finished
+                ok = __all_sync(0xffffffffu,
+                                attn_wait_cl(&bar_kfull[st], (uint32_t)((g / k2Stages) & 1), abort) &&
+                                    (g < k2SBufs ||
+                                     attn_wait_cl(&bar_o[b], (uint32_t)(((g / k2SBufs) - 1) & 1),
+                                                  abort)));
+                if (!ok)
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (lane == 0) {
+                    const uint32_t k_addr = attn_smem_u32(sK(st));
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma2_ss(tmem + (uint32_t)b * kAttnKeys,
+                                 umma_desc(q_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32u, 16u,
+                                           1024u, kSwizzle128),
+                                 umma_desc(k_addr + (kk >> 2) * (k2Half / 2) + (kk & 3) * 32u, 16u,
+                                           1024u, kSwizzle128),
+                                 idesc, kk > 0);
+                    umma2_commit(&bar_s[b], 3);
+                    umma2_commit(&bar_kfree[st], 3);
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA this thread issued has finished (one commit, phase 0)
+        if (lane == 0)
+            umma2_commit(&bar_drain[0], 1);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, attn_wait_cl(&bar_drain[0], 0u)))
+            ok = false;
+        if (!ok)
+            raise_abort();
+    } else if (warp == k2PVIssueWarp && leader) {
+        // ---- O += P V for both CTAs once both P are in TMEM
+        const uint32_t idesc = umma_idesc(256, D, ab_format, 1);
+        int64_t g = 0;
+        for (int64_t L = cid; ok && L < n_units; L += clusters) {
+            const int64_t n_tiles = unit_work(L).n_tiles;
+            for (int64_t kt = 0; ok && kt < n_tiles; ++kt, ++g) {
+                const int st = (int)(g % k2Stages), b = (int)(g % k2SBufs);
+                ok = __all_sync(0xffffffffu,
+                                attn_wait_cl(&bar_p[b], (uint32_t)((g / k2SBufs) & 1), abort) &&
+                                    attn_wait_cl(&bar_vfull[st], (uint32_t)((g / k2Stages) & 1),
+                                                 abort));
+                if (!ok)
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (lane == 0) {
+                    const uint32_t v_addr = attn_smem_u32(sV(st));
+#pragma unroll
+                    for (int kk = 0; kk < kAttnKeys / 16; ++kk)
+                        umma2_ts(tmem + k2OCol, tmem + (uint32_t)b * kAttnKeys + kk * 8,
+                                 umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128),
+                                 idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    umma2_commit(&bar_o[b], 3);
+                    umma2_commit(&bar_vfree[st], 3);
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA this thread issued has finished (one commit, phase 0)
+        if (lane == 0)
+            umma2_commit(&bar_drain[1], 1);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, attn_wait_cl(&bar_drain[1], 0u)))
+            ok = false;
+        if (!ok)
+            raise_abort();
+    } else if (warp == k2TmaWarp) {
+        // ---- per unit: the query tile (and its table rows) once the
+        // previous unit's last S has read the old one (its key stage's
+        // release: S products finish in order, and that stage's previous
+        // release, of tile g - 3, has been waited for), then this CTA's halves
+        // of key and value tile g into stage g mod 3 once tile g - 3 released it
+        int64_t k_last[k2Stages], v_last[k2Stages];
+#pragma unroll
+        for (int s = 0; s < k2Stages; ++s)
+            k_last[s] = v_last[s] = -1;
+        bool q_pending = false;
+        int64_t g = 0, g_prev = -1;                // g_prev: the previous unit's last tile
+        for (int64_t L = cid; ok && L < n_units; L += clusters) {
+            const AttnWork w = unit_work(L);
+            const int64_t n_tiles = w.n_tiles;
+            if (n_tiles == 0)
+                continue;
+            const int32_t hq = w.hq_first + (int32_t)rank * w.hq_step;
+            const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
+            if (g_prev >= 0)
+                ok = __all_sync(0xffffffffu,
+                                attn_wait_cl(&bar_kfree[g_prev % k2Stages],
+                                             (uint32_t)((g_prev / k2Stages) & 1), abort));
+            if (!ok)
+                break;
+            if (lane == 0)
+                mbar_expect_tx(&bar_q,
+                               (uint32_t)(D / 64 + (STAGED_Q ? 2 * tboxes : 0)) * kBoxBytes);
+            __syncwarp();
+            if (lane < D / 64)
+                tma_load_3d(sQ + lane * kBoxBytes, &maps.q, lane * 64, (int)q0,
+                            (int)(w.b * a.Hq + hq), &bar_q);
+            if (STAGED_Q && lane >= 8 && lane < 8 + 2 * tboxes) {
+                const int t = lane - 8;
+                const bool is_cos = t < tboxes;
+                tma_load_2d(sT + t * kBoxBytes, is_cos ? &maps.cos : &maps.sin,
+                            (is_cos ? t : t - tboxes) * 32, (int)q0, &bar_q);
+            }
+            q_pending = true;
+            for (int64_t kt = 0; ok && kt < n_tiles; ++kt, ++g) {
+                const int st = (int)(g % k2Stages);
+                const int k0 = (int)(kt * kAttnKeys);
+                const uint32_t free_ph = (uint32_t)(((g / k2Stages) - 1) & 1);
+                if (g >= k2Stages)
+                    ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_kfree[st], free_ph, abort));
+                if (!ok)
+                    break;
+                // this CTA's half of key tile k0: keys k0 + 64 rank .. + 63;
+                // both CTAs' bytes complete the leader's barrier
+                if (leader && lane == 0)
+                    mbar_expect_tx(&bar_kfull[st], 2 * k2Half);
+                __syncwarp();
+                if (lane < D / 64) {
+                    if (leader)
+                        tma_load_3d(sK(st) + lane * (k2Half / 2), &maps.k, lane * 64, k0, w.zkv,
+                                    &bar_kfull[st]);
+                    else
+                        tma_load_3d_to_leader(sK(st) + lane * (k2Half / 2), &maps.k, lane * 64,
+                                              k0 + 64, w.zkv, peer_addr(&bar_kfull[st], 0));
+                }
+                k_last[st] = g;
+                if (g >= k2Stages)
+                    ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_vfree[st], free_ph, abort));
+                if (!ok)
+                    break;
+                // this CTA's half of value tile k0: feature columns 64 rank ..
+                // + 63 of its 128 keys
+                if (lane == 0) {
+                    if (leader) {
+                        mbar_expect_tx(&bar_vfull[st], 2 * k2Half);
+                        tma_load_3d(sV(st), &maps.v, 0, k0, w.zkv, &bar_vfull[st]);
+                    } else {
+                        tma_load_3d_to_leader(sV(st), &maps.v, 64, k0, w.zkv,
+                                              peer_addr(&bar_vfull[st], 0));
+                    }
+                }
+                __syncwarp();
+                v_last[st] = g;
+            }
+            g_prev = g - 1;
+        }
+        if (!ok) {
+            raise_abort();
+            // one more bounded wait for the last query tile and, in the
+            // leader, the last copies into each stage (its barriers count both
+            // CTAs' bytes; the follower's memory stays valid until the pair's
+            // final barrier below, which the leader reaches after these waits)
+            (void)q_pending;
+#pragma unroll
+            for (int s = 0; s < k2Stages; ++s) {
+                if (leader && k_last[s] >= 0)
+                    (void)attn_wait_cl(&bar_kfull[s], (uint32_t)((k_last[s] / k2Stages) & 1));
+                if (leader && v_last[s] >= 0)
+                    (void)attn_wait_cl(&bar_vfull[s], (uint32_t)((v_last[s] / k2Stages) & 1));
+            }
+        }
+    }
+    // every role has left its loops; the pair meets once more before TMEM is
+    // freed, so no MMA of the leader still reads the follower's memory
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync_all();
+    if (tid == 0 && *abort)
+        atomicOr(a.flag, 2);
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1342,14 +1830,14 @@ static EncodeTiledFn encode_tiled()
     return f;
 }
 
-// [heads][rows][D] 16-bit elements; box 64 elements x 128 rows x 1 head,
-// 128-byte swizzle.
+// [heads][rows][D] 16-bit elements; box 64 elements x box_rows rows x 1
+// head, 128-byte swizzle.
 static bool encode_kv(EncodeTiledFn enc, CUtensorMap *m, const void *base, CUtensorMapDataType dt,
-                      int64_t heads, int64_t rows, int32_t D)
+                      int64_t heads, int64_t rows, int32_t D, uint32_t box_rows = kAttnKeys)
 {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kAttnKeys, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1375,6 +1863,13 @@ static bool encode_table(EncodeTiledFn enc, CUtensorMap *m, const float *base, i
 // fp32 blocks at most); rope_attn_pp_kernel: two query tiles and two stages
 // of key and value tiles.  With D = 64 the request is raised so that one CTA
 // holds an SM (its 512 TMEM columns are the whole SM's).
+// rope_attn_2sm_kernel (D = 128): the query tile, three stages of a key
+// half and a value half, the query tile's table rows.
+static size_t attn_2sm_smem_bytes()
+{
+    return (size_t)kAttnRows * 128 * 2 + (size_t)k2Stages * 2 * k2Half + 4 * (size_t)kBoxBytes;
+}
+
 static size_t attn_smem_bytes(int D, bool prerotated)
 {
     const size_t tile = (size_t)kAttnRows * D * 2;
@@ -1393,7 +1888,7 @@ static bool pp_staged_q(const AttnArgs &a, int pair_heads)
     return pair_heads && a.pos_q == nullptr && a.rotary_dim % 64 == 0;
 }
 
-// Launches one attention kernel instance over (query tiles, head units).
+// Launches one attention kernel instance over (head units, query tiles).
 template <auto Kernel>
 static cudaError_t launch_attn(int threads, size_t smem, const AttnArgs &a, const AttnMaps &maps,
                                int pair_heads, cudaStream_t st)
@@ -1421,10 +1916,54 @@ static cudaError_t launch_attn(int threads, size_t smem, const AttnArgs &a, cons
     return cudaGetLastError();
 }
 
+// Launches the persistent rope_attn_2sm_kernel: one cluster of two CTAs per
+// pair of SMs (at most one per work unit).
+template <auto Kernel>
+static cudaError_t launch_attn_2sm(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
+                                   cudaStream_t st)
+{
+    static std::atomic<uint64_t> raised{0};       // bit d: shared-memory limit raised on device d
+    static std::atomic<int> sm_count[64];         // multiprocessors of device d (0: not read yet)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    int sms = sm_count[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        sm_count[dev].store(sms, std::memory_order_release);
+    }
+    const uint64_t bit = (uint64_t)1 << dev;
+    if (!(raised.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_2sm_smem_bytes());
+        if (e != cudaSuccess)
+            return e;
+        raised.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const int64_t qtiles = (a.Sq + kAttnRows - 1) / kAttnRows;
+    const int64_t units = a.B * (pair_heads ? a.Hq / 2 : a.Hq) * (pair_heads ? qtiles : (qtiles + 1) / 2);
+    const int64_t clusters = units < sms / 2 ? units : sms / 2;
+    if (clusters < 1)
+        return cudaSuccess;
+    Kernel<<<dim3((unsigned)(2 * clusters)), k2Threads, attn_2sm_smem_bytes(), st>>>(a, maps,
+                                                                                      pair_heads);
+    return cudaGetLastError();
+}
+
 template <typename T, int LAYOUT, int D>
 static cudaError_t launch_attn_layout(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
                                       cudaStream_t st)
 {
+    if (a.k_rot != nullptr && D == 128) {
+        if (a.pos_q == nullptr && a.rotary_dim % 64 == 0)
+            return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, true>>(a, maps, pair_heads, st);
+        return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, false>>(a, maps, pair_heads, st);
+    }
     if (a.k_rot != nullptr) {
         if (pp_staged_q(a, pair_heads))
             return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true>>(
@@ -1463,17 +2002,21 @@ cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32
         const CUtensorMapDataType dt =
             dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const int64_t heads = a.B * a.Hk;
-        // keys rotated beforehand are read from the workspace, else from k;
-        // the query tiles arrive by TMA only in rope_attn_pp_kernel
-        if (!encode_kv(enc, &maps.k, a.k_rot != nullptr ? a.k_rot : a.k, dt, heads, a.Sk, D) ||
+        // keys rotated beforehand are read from the workspace (by
+        // rope_attn_2sm_kernel in halves of 64 keys), else from k; the query
+        // tiles arrive by TMA only when the keys were rotated beforehand
+        const bool two_sm = a.k_rot != nullptr && D == 128;
+        if (!encode_kv(enc, &maps.k, a.k_rot != nullptr ? a.k_rot : a.k, dt, heads, a.Sk, D,
+                       two_sm ? 64u : (uint32_t)kAttnKeys) ||
             !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D) ||
             (a.k_rot != nullptr && !encode_kv(enc, &maps.q, a.q, dt, a.B * a.Hq, a.Sq, D)))
             return cudaErrorInvalidValue;
         // the table boxes: of the key tiles (keys rotated in the kernel) or
         // of the query tiles (keys rotated beforehand)
-        const bool stage_table = a.k_rot == nullptr
-                                     ? a.pos_k == nullptr && a.rotary_dim % 64 == 0
-                                     : pp_staged_q(a, pair_heads);
+        const bool stage_table =
+            a.k_rot == nullptr ? a.pos_k == nullptr && a.rotary_dim % 64 == 0
+                               : (two_sm ? a.pos_q == nullptr && a.rotary_dim % 64 == 0
+                                         : pp_staged_q(a, pair_heads));
         if (stage_table &&
             (!encode_table(enc, &maps.cos, a.cos, a.table_rows, a.rotary_dim / 2) ||
              !encode_table(enc, &maps.sin, a.sin, a.table_rows, a.rotary_dim / 2)))

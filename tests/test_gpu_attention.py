@@ -57,6 +57,10 @@ CASES = [
     dict(B=1, Hq=3, Hk=1, Sq=257, Sk=390, D=128, rd=64, dtype="bf16", layout="interleaved", causal=True),
     # interleaved, full rotary span: table chunks from the second staged table box
     dict(B=1, Hq=4, Hk=1, Sq=300, Sk=300, D=128, rd=128, dtype="bf16", layout="interleaved", causal=True),
+    # more work units than pairs of SMs (144 and 180): the persistent kernel of
+    # the workspace path runs several units per cluster, back to back
+    dict(B=24, Hq=4, Hk=2, Sq=300, Sk=400, D=128, rd=128, dtype="bf16", layout="split_half", causal=False),
+    dict(B=30, Hq=3, Hk=1, Sq=260, Sk=260, D=128, rd=64, dtype="f16", layout="interleaved", causal=True),
 ]
 
 
