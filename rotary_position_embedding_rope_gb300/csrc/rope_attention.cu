@@ -1364,14 +1364,14 @@ __device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t cta)
     return r;
 }
 
-// Arrival on a barrier of the peer CTA, without a cluster-scope release
-// fence (that fence costs ~1.4 k cycles inside this kernel).  Used after
-// tcgen05.wait::st and tcgen05.fence::before_thread_sync: the tensor-memory
-// stores it announces have completed before the arrival is issued.
+// Arrival on a barrier of the peer CTA (default semantics: release at CTA
+// scope; a cluster-scope release fence costs ~1.4 k cycles inside this
+// kernel).  Used after tcgen05.wait::st and tcgen05.fence::before_thread_sync
+// (the tensor-memory stores it announces have completed) or after
+// fence.proxy.async (the shared-memory stores are visible to the tensor cores).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion (bytes) is
@@ -1383,27 +1383,6 @@ __device__ __forceinline__ void tma_load_3d_to_leader(void *dst, const CUtensorM
                  "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
                  ::"r"(attn_smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(leader_bar)
                  : "memory");
-}
-
-// Bounded wait with cluster-scope acquire (the barrier may be completed by
-// the peer CTA); false on expiry or once *abort is raised.
-__device__ __forceinline__ bool attn_wait_cl(uint64_t *bar, uint32_t parity,
-                                             const volatile int *abort = nullptr)
-{
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(attn_smem_u32(bar)), "r"(parity)
-                     : "memory");
-        if (done)
-            return true;
-        if ((abort != nullptr && *abort) || clock64() - t0 > kAttnWaitCycles)
-            return false;
-    }
 }
 
 __device__ __forceinline__ void umma2_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -1543,25 +1522,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             const int64_t n_tiles = w.n_tiles;     // the same in both CTAs
             float m_ref = -INFINITY, l_run = 0.0f;
             if (n_tiles > 0) {
-                ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_q, qn & 1u, abort));
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_q, qn & 1u, abort));
                 if (!ok)
                     break;
                 rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(sQ, sT, q0, a.pos_q, a.Sq, a, tid);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 // this warp's rows are rotated: one arrival per row warp of
-                // both CTAs on the leader's barrier (once per unit, with a
-                // cluster-scope release for the shared-memory stores)
+                // both CTAs on the leader's barrier (once per unit)
                 __syncwarp();
                 if (lane == 0)
-                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-                                 ::"r"(peer_addr(&bar_qr, 0))
-                                 : "memory");
+                    mbar_arrive_remote(peer_addr(&bar_qr, 0));
                 ++qn;
             }
             for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
                 const int b = (int)(g % k2SBufs);
                 ok = __all_sync(0xffffffffu,
-                                attn_wait_cl(&bar_s[b], (uint32_t)((g / k2SBufs) & 1), abort));
+                                attn_wait(&bar_s[b], (uint32_t)((g / k2SBufs) & 1), abort));
                 if (!ok)
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -1573,7 +1549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 auto o_ready = [&]() {
                     const int64_t gp = g - 1;
                     o_ok = __all_sync(0xffffffffu,
-                                      attn_wait_cl(&bar_o[gp % k2SBufs],
+                                      attn_wait(&bar_o[gp % k2SBufs],
                                                    (uint32_t)((gp / k2SBufs) & 1), abort));
                     return o_ok;
                 };
@@ -1599,7 +1575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             // the unit's last O += P V (products finish in order), then O / l
             if (n_tiles > 0) {
                 const int64_t gp = g - 1;
-                ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_o[gp % k2SBufs],
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_o[gp % k2SBufs],
                                                           (uint32_t)((gp / k2SBufs) & 1), abort));
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -1621,16 +1597,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             if (n_tiles == 0)
                 continue;
             // both CTAs' query tiles of this unit are rotated
-            ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_qr, qn & 1u, abort));
+            ok = __all_sync(0xffffffffu, attn_wait(&bar_qr, qn & 1u, abort));
             ++qn;
             for (int64_t kt = 0; ok && kt < n_tiles; ++kt, ++g) {
                 const int st = (int)(g % k2Stages), b = (int)(g % k2SBufs);
                 // both key halves landed; the product that read P from this S
                 // buffer (tile g - 3) has finished
                 ok = __all_sync(0xffffffffu,
-                                attn_wait_cl(&bar_kfull[st], (uint32_t)((g / k2Stages) & 1), abort) &&
+                                attn_wait(&bar_kfull[st], (uint32_t)((g / k2Stages) & 1), abort) &&
                                     (g < k2SBufs ||
-                                     attn_wait_cl(&bar_o[b], (uint32_t)(((g / k2SBufs) - 1) & 1),
+                                     attn_wait(&bar_o[b], (uint32_t)(((g / k2SBufs) - 1) & 1),
                                                   abort)));
                 if (!ok)
                     break;
@@ -1655,7 +1631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         if (lane == 0)
             umma2_commit(&bar_drain[0], 1);
         __syncwarp();
-        if (!__all_sync(0xffffffffu, attn_wait_cl(&bar_drain[0], 0u)))
+        if (!__all_sync(0xffffffffu, attn_wait(&bar_drain[0], 0u)))
             ok = false;
         if (!ok)
             raise_abort();
@@ -1668,8 +1644,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             for (int64_t kt = 0; ok && kt < n_tiles; ++kt, ++g) {
                 const int st = (int)(g % k2Stages), b = (int)(g % k2SBufs);
                 ok = __all_sync(0xffffffffu,
-                                attn_wait_cl(&bar_p[b], (uint32_t)((g / k2SBufs) & 1), abort) &&
-                                    attn_wait_cl(&bar_vfull[st], (uint32_t)((g / k2Stages) & 1),
+                                attn_wait(&bar_p[b], (uint32_t)((g / k2SBufs) & 1), abort) &&
+                                    attn_wait(&bar_vfull[st], (uint32_t)((g / k2Stages) & 1),
                                                  abort));
                 if (!ok)
                     break;
@@ -1691,7 +1667,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         if (lane == 0)
             umma2_commit(&bar_drain[1], 1);
         __syncwarp();
-        if (!__all_sync(0xffffffffu, attn_wait_cl(&bar_drain[1], 0u)))
+        if (!__all_sync(0xffffffffu, attn_wait(&bar_drain[1], 0u)))
             ok = false;
         if (!ok)
             raise_abort();
@@ -1716,7 +1692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
             if (g_prev >= 0)
                 ok = __all_sync(0xffffffffu,
-                                attn_wait_cl(&bar_kfree[g_prev % k2Stages],
+                                attn_wait(&bar_kfree[g_prev % k2Stages],
                                              (uint32_t)((g_prev / k2Stages) & 1), abort));
             if (!ok)
                 break;
@@ -1739,7 +1715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 const int k0 = (int)(kt * kAttnKeys);
                 const uint32_t free_ph = (uint32_t)(((g / k2Stages) - 1) & 1);
                 if (g >= k2Stages)
-                    ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_kfree[st], free_ph, abort));
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_kfree[st], free_ph, abort));
                 if (!ok)
                     break;
                 // this CTA's half of key tile k0: keys k0 + 64 rank .. + 63;
@@ -1757,7 +1733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 }
                 k_last[st] = g;
                 if (g >= k2Stages)
-                    ok = __all_sync(0xffffffffu, attn_wait_cl(&bar_vfree[st], free_ph, abort));
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_vfree[st], free_ph, abort));
                 if (!ok)
                     break;
                 // this CTA's half of value tile k0: feature columns 64 rank ..
@@ -1786,9 +1762,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
 #pragma unroll
             for (int s = 0; s < k2Stages; ++s) {
                 if (leader && k_last[s] >= 0)
-                    (void)attn_wait_cl(&bar_kfull[s], (uint32_t)((k_last[s] / k2Stages) & 1));
+                    (void)attn_wait(&bar_kfull[s], (uint32_t)((k_last[s] / k2Stages) & 1));
                 if (leader && v_last[s] >= 0)
-                    (void)attn_wait_cl(&bar_vfull[s], (uint32_t)((v_last[s] / k2Stages) & 1));
+                    (void)attn_wait(&bar_vfull[s], (uint32_t)((v_last[s] / k2Stages) & 1));
             }
         }
     }
