@@ -477,9 +477,9 @@ def attention_arm(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "peak_source": "%s bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
-                         "traffic": profiled_traffic("rope_attn_pp_kernel", a["name"],
+                         "traffic": profiled_traffic("rope_attn_2sm_kernel", a["name"],
                                                      ATTN_SOURCES),
-                         "kernel": "rope_attn_pp_kernel",
+                         "kernel": "rope_attn_2sm_kernel",
                          "note": "achieved = flops per call / the call's time, which also holds "
                                  "the launch that rotates K into the workspace"},
             "inkernel_keys_context": inkernel,

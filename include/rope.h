@@ -227,8 +227,8 @@ rope_status rope_apply_q(void *x, const float *cos, const float *sin, const int3
  *    reads in shared memory, and rot(K) is never written.  Given: rot(K) is
  *    written there once per call by the rotation kernel (rope_apply_qk's
  *    arithmetic, so the same bits), then the attention kernel reads the
- *    rotated keys, and its two row blocks no longer wait for a joint key
- *    rotation.  Under GQA every key tile is read by many CTAs, so for long
+ *    rotated keys (for D = 128 on pairs of SMs, with no CTA rotating key
+ *    tiles).  Under GQA every key tile is read by many CTAs, so for long
  *    sequences the workspace path is the faster one; both give the same
  *    result bit for bit.  Q is rotated inside the attention kernel either way.
  * Arithmetic: the rotated q and k rows are rounded to `dtype`, S = q k^T is

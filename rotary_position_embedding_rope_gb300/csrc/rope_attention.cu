@@ -9,7 +9,14 @@
 //
 //   O = softmax(scale * rot(Q) rot(K)^T + mask) V
 //
-// One CTA = two row blocks of 128 query rows that read the same key/value
+// Three kernels share the helpers of this file:
+//   * rope_attn_kernel (described here): the key tiles are rotated in shared
+//     memory by every CTA that reads them (no key workspace);
+//   * rope_attn_pp_kernel and rope_attn_2sm_kernel (described at their
+//     definitions): the keys were rotated once beforehand into a workspace
+//     by the rotation kernel; D = 64 and D = 128 (pairs of SMs).
+//
+// rope_attn_kernel: one CTA = two row blocks of 128 query rows that read the same key/value
 // head: two query heads of one GQA group (same rows), or, when the group
 // size is odd, two consecutive query tiles of one head.  288 threads: warps
 // 4j .. 4j+3 own row block j (thread t: row t mod 128, which is also TMEM lane
