@@ -1942,17 +1942,22 @@ template <typename T, int LAYOUT, int D>
 static cudaError_t launch_attn_layout(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
                                       cudaStream_t st)
 {
-    if (a.k_rot != nullptr && D == 128) {
-        if (a.pos_q == nullptr && a.rotary_dim % 64 == 0)
-            return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, true>>(a, maps, pair_heads, st);
-        return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, false>>(a, maps, pair_heads, st);
-    }
-    if (a.k_rot != nullptr) {
-        if (pp_staged_q(a, pair_heads))
-            return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true>>(
+    // keys rotated beforehand: pairs of SMs for D = 128, one SM for D = 64
+    if constexpr (D == 128) {
+        if (a.k_rot != nullptr) {
+            if (a.pos_q == nullptr && a.rotary_dim % 64 == 0)
+                return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, true>>(a, maps, pair_heads,
+                                                                              st);
+            return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, false>>(a, maps, pair_heads, st);
+        }
+    } else {
+        if (a.k_rot != nullptr) {
+            if (pp_staged_q(a, pair_heads))
+                return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true>>(
+                    kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
+            return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, false>>(
                 kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
-        return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, false>>(
-            kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
+        }
     }
     const size_t smem = attn_smem_bytes(D, false);
     if (a.pos_k == nullptr && a.rotary_dim % 64 == 0)
