@@ -182,3 +182,34 @@ def test_attention_fuzz(c):
     assert torch.equal(o.view(torch.int16), o_in.view(torch.int16)), "key paths differ"
     _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, pq, pk, c["causal"],
            str(c))
+
+
+def test_attention_full_size_sampled_rows():
+    """The bench's attention workload at full size (Q [4,32,4096,128], K/V
+    [4,8,4096,128] bf16, causal, theta 5e5) through the workspace path, in
+    the configuration the bench times (2048 work units on the persistent
+    clusters).  Sampled query rows against the oracle: row i at its own
+    position, against the keys 0..i it can see, is exactly that row of the
+    causal attention."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, S, D, rd = 4, 32, 8, 4096, 128, 128
+    q, k, v = _inputs(B, Hq, Hk, S, S, D, "bf16", 6)
+    c32, s32 = oracle_tables(5e5, rd, S)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, causal=True).cpu()
+    assert R.rope_check_errors() == R.ROPE_OK
+    rng = np.random.default_rng(11)
+    rows = [(0, 0, 0), (3, 31, S - 1), (1, 5, 127), (2, 17, 128), (0, 30, 2047), (3, 2, 4095)]
+    rows += [(int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(S))) for _ in range(18)]
+    group = Hq // Hk
+    for b, h, i in rows:
+        kv = h // group
+        ref = OA.attention(W.bits(q[b:b + 1, h:h + 1, i:i + 1]), W.bits(k[b:b + 1, kv:kv + 1, :i + 1]),
+                           W.bits(v[b:b + 1, kv:kv + 1, :i + 1]), O.BF16, rd, O.SPLIT_HALF, c32, s32,
+                           np.array([i], dtype=np.int32), None, True)
+        got = o[b:b + 1, h:h + 1, i:i + 1].float().numpy().astype(np.float64)
+        vmax = float(v[b, kv, :i + 1].float().abs().max())
+        tol = U["bf16"] * (vmax + np.abs(ref))
+        assert np.all(np.abs(got - ref) <= tol), "row (%d, %d, %d): max err %.3g" % (
+            b, h, i, np.abs(got - ref).max())
