@@ -1519,6 +1519,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
         const uint32_t o_base = tmem + k2OCol + lanes;
         int64_t g = 0;
+        uint32_t sb = 0, s_ph = 0;                 // S buffer g mod 3 and its phase parity
+        uint32_t ob = 0, o_ph = 0;                 // the same for tile g - 1 (O barriers)
         uint32_t qn = 0;                           // units with key tiles so far
         for (int64_t L = cid; ok && L < n_units; L += clusters) {
             const AttnWork w = unit_work(L);
@@ -1542,9 +1544,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 ++qn;
             }
             for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
-                const int b = (int)(g % k2SBufs);
-                ok = __all_sync(0xffffffffu,
-                                attn_wait(&bar_s[b], (uint32_t)((g / k2SBufs) & 1), abort));
+                const uint32_t b = sb;
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_s[b], s_ph, abort));
                 if (!ok)
                     break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -1554,10 +1555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 // earlier (rare: the row max moved by more than 8)
                 bool o_ok = true;
                 auto o_ready = [&]() {
-                    const int64_t gp = g - 1;
-                    o_ok = __all_sync(0xffffffffu,
-                                      attn_wait(&bar_o[gp % k2SBufs],
-                                                   (uint32_t)((gp / k2SBufs) & 1), abort));
+                    o_ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
                     return o_ok;
                 };
                 softmax_tile<T, D, true>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
@@ -1574,17 +1572,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                     else
                         mbar_arrive_remote(peer_addr(&bar_p[b], 0));
                 }
+                // tile g becomes the "previous" tile; advance to g + 1
+                ob = sb;
+                o_ph = s_ph;
+                if (++sb == k2SBufs) {
+                    sb = 0;
+                    s_ph ^= 1u;
+                }
                 if (!ok)
                     break;
             }
             if (!ok)
                 break;
             // the unit's last O += P V (products finish in order), then O / l
-            if (n_tiles > 0) {
-                const int64_t gp = g - 1;
-                ok = __all_sync(0xffffffffu, attn_wait(&bar_o[gp % k2SBufs],
-                                                          (uint32_t)((gp / k2SBufs) & 1), abort));
-            }
+            if (n_tiles > 0)
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ok)
                 break;
