@@ -445,6 +445,42 @@ def attention_arm(args):
     except Exception as exc:  # noqa: BLE001 - context only
         unfused = {"unavailable": str(exc)[:200]}
 
+    # end to end through the public API with host buffers: every step copies
+    # Q, K, V from pinned host memory and O back to pinned host memory, one
+    # batch chunk at a time, with the copies overlapping the calls
+    from rotary_position_embedding_rope_gb300.host import HostAttention
+
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty_like(hq).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    hat = HostAttention(device, chunks=a["B"])
+
+    def e2e_step(after):
+        return hat.forward(hq, hk, hv, ho, cos, sin, rotary_dim=a["rotary_dim"],
+                           causal=a["causal"], after=after)
+
+    for _ in range(2):
+        stream.wait_event(e2e_step(None))
+    torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    last = x0
+    for i in range(args.e2e_steps):
+        last = e2e_step(x0 if i == 0 else None)
+    stream.wait_event(last)
+    x1.record(stream)
+    torch.cuda.synchronize(device)
+    assert R.rope_check_errors(stream) == R.ROPE_OK
+    e2e_ms, e2e_flops = aggregate(dist, device, x0.elapsed_time(x1), flops * args.e2e_steps)
+    e2e = {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+           "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
+           "what": "pinned host Q, K, V in and O out; %d batch chunks, copies overlapping the "
+                   "calls" % a["B"]}
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         from oracle import attention as OA
@@ -482,6 +518,7 @@ def attention_arm(args):
                          "kernel": "rope_attn_2sm_kernel",
                          "note": "achieved = flops per call / the call's time, which also holds "
                                  "the launch that rotates K into the workspace"},
+            "e2e": e2e,
             "inkernel_keys_context": inkernel,
             "unfused_context": unfused,
             "gpu_launches": 2 * steps,

@@ -1,18 +1,19 @@
-"""Rotation of Q and K that live in pinned host memory.
+"""Rotation of Q and K, and attention with rotary Q and K, on tensors that
+live in pinned host memory.
 
 The tensors are split along the batch dimension into chunks.  Chunk i is
-copied host->device on one stream, rotated by the CUDA library on a second
+copied host->device on one stream, processed by the CUDA library on a second
 and copied device->host on a third, so the copies in both directions and the
 kernels of neighbouring chunks overlap.  Device staging buffers (two chunks
 per tensor) are allocated once per shape and reused.  Only argument
-marshalling and stream ordering happen here; the rotation is one library call
+marshalling and stream ordering happen here; the work is one library call
 per chunk.
 """
 from __future__ import annotations
 
 import torch
 
-from . import _DTYPE_CODE, _LAYOUT_CODE, _shape4, rope_apply_qk_out
+from . import _DTYPE_CODE, _LAYOUT_CODE, _shape4, rope_apply_qk_out, rope_attention_fwd
 
 
 class HostRotator:
@@ -87,6 +88,90 @@ class HostRotator:
                 q_out[b0:b1].copy_(dq, non_blocking=True)
                 if k is not None:
                     k_out[b0:b1].copy_(dk, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(self.s_out)
+            self._free[slot] = done
+        return done
+
+
+class HostAttention:
+    """softmax(scale * rot(q) rot(k)^T + mask) v for pinned host q, k, v into
+    a pinned host o, through rope_attention_fwd with a key workspace, one call
+    per batch chunk.  Each chunk's copies of q, k, v in, the call, and the
+    copy of o out run on three streams, so neighbouring chunks overlap."""
+
+    def __init__(self, device=None, chunks: int = 4):
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.chunks = chunks
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_run = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
+        self._key = None
+        self._slots = None
+        self._ws = None
+        self._free = [None, None]
+
+    def _staging(self, q, k, per):
+        key = (tuple(q.shape), tuple(k.shape), q.dtype, per)
+        if key != self._key:
+            def dev(t):
+                return torch.empty((per,) + tuple(t.shape[1:]), dtype=t.dtype, device=self.device)
+            self._slots = [(dev(q), dev(k), dev(k), dev(q)) for _ in range(2)]
+            # the calls all run on s_run, one after another: one workspace serves them
+            self._ws = dev(k)
+            self._key = key
+            self._free = [None, None]
+        return self._slots, self._ws
+
+    def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                cos: torch.Tensor, sin: torch.Tensor, pos_q: torch.Tensor | None = None,
+                pos_k: torch.Tensor | None = None, rotary_dim: int | None = None,
+                layout: str = "split_half", causal: bool = False, scale: float | None = None,
+                after: torch.cuda.Event | None = None):
+        """q [B,Hq,Sq,D], k and v [B,Hk,Sk,D], o like q: contiguous pinned CPU
+        tensors.  cos, sin and pos_q [Sq], pos_k [Sk] (int32) are device
+        tensors.  Work is ordered after the event `after` (if given).  Returns
+        the event recorded when the last copy of o to the host is done."""
+        for t in (q, k, v, o):
+            if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+                raise ValueError("host tensors must be contiguous pinned CPU memory")
+        B, Hq, Sq, D = q.shape
+        _, Hk, Sk, _ = k.shape
+        if v.shape != k.shape or o.shape != q.shape:
+            raise ValueError("v must have k's shape and o q's shape")
+        rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+        n = max(1, min(self.chunks, B))
+        per = (B + n - 1) // n
+        slots, ws = self._staging(q, k, per)
+        ws_bytes = ws.numel() * ws.element_size()
+        for s in (self.s_in, self.s_run, self.s_out):
+            if after is not None:
+                s.wait_event(after)
+        done = None
+        for c in range(n):
+            b0, b1 = c * per, min(B, (c + 1) * per)
+            if b0 >= b1:
+                break
+            slot = c % 2
+            dq, dk, dv, do = (t[: b1 - b0] for t in slots[slot])
+            if self._free[slot] is not None:
+                self.s_in.wait_event(self._free[slot])
+            with torch.cuda.stream(self.s_in):
+                dq.copy_(q[b0:b1], non_blocking=True)
+                dk.copy_(k[b0:b1], non_blocking=True)
+                dv.copy_(v[b0:b1], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(self.s_in)
+            self.s_run.wait_event(ready)
+            rope_attention_fwd(dq, dk, dv, do, cos, sin, pos_q, pos_k, b1 - b0, Hq, Hk, Sq, Sk, D,
+                               rd, _LAYOUT_CODE[layout], int(causal),
+                               -1.0 if scale is None else scale, _DTYPE_CODE[q.dtype],
+                               cos.shape[0], ws, ws_bytes, self.s_run)
+            computed = torch.cuda.Event()
+            computed.record(self.s_run)
+            self.s_out.wait_event(computed)
+            with torch.cuda.stream(self.s_out):
+                o[b0:b1].copy_(do, non_blocking=True)
                 done = torch.cuda.Event()
                 done.record(self.s_out)
             self._free[slot] = done

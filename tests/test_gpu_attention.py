@@ -213,3 +213,25 @@ def test_attention_full_size_sampled_rows():
         tol = U["bf16"] * (vmax + np.abs(ref))
         assert np.all(np.abs(got - ref) <= tol), "row (%d, %d, %d): max err %.3g" % (
             b, h, i, np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3])
+def test_host_attention_pipeline_matches_device_call(chunks):
+    """Pinned host Q, K, V through the chunked copy/attend/copy pipeline give
+    the device call's bits, and leave the host inputs untouched."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostAttention
+
+    q, k, v = _inputs(3, 4, 2, 200, 230, 128, "bf16", seed=17)
+    cos, sin = R.build_tables(10000.0, 128, 256)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.full_like(q, float("nan")).pin_memory()
+    hat = HostAttention(chunks=chunks)
+    for causal in (True, False):
+        hat.forward(hq, hk, hv, ho, cos, sin, causal=causal).synchronize()
+        want = R.attention(q.cuda(), k.cuda(), v.cuda(), cos, sin, causal=causal)
+        torch.cuda.synchronize()
+        assert R.rope_check_errors() == R.ROPE_OK
+        assert torch.equal(ho, want.cpu())
+    assert torch.equal(hq, q) and torch.equal(hk, k) and torch.equal(hv, v)
