@@ -1363,6 +1363,10 @@ constexpr int k2Threads = 7 * 32;
 constexpr int k2SBufs = 3;                         // S buffers in TMEM
 constexpr uint32_t k2OCol = k2SBufs * kAttnKeys;   // TMEM column of O (384)
 constexpr uint32_t k2Half = 16384;                 // bytes of a CTA's half key or value tile
+// Key / value stage g mod 3 is released by the commits that complete S
+// buffer g mod 3 (S(g) has read the key half) and its O barrier (O += P V
+// has read the value half): one commit per issuing thread and tile.
+static_assert(k2Stages == k2SBufs, "stages and S buffers advance together");
 
 __device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t cta)
 {
@@ -1440,10 +1444,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     uint8_t *sT = sStages + k2Stages * 2 * k2Half;     // the query tile's table rows
     auto sK = [&](int st) { return sStages + st * 2 * k2Half; };
     auto sV = [&](int st) { return sStages + st * 2 * k2Half + k2Half; };
-    // both CTAs' key / value halves landed (leader only: TMA bytes of both),
-    // stage released (multicast commits); S buffer ready (multicast); P
+    // both CTAs' key / value halves landed (leader only: TMA bytes of both);
+    // S buffer ready, which also releases key stage b (multicast); P
     // ready (leader only: each row warp of both CTAs arrives); the O += P V
-    // that read P from S buffer b done (multicast); query tile landed; both
+    // that read P from S buffer b done, which also releases value stage b
+    // (multicast); query tile landed; both
     // query tiles rotated (leader only: each row warp arrives); every MMA of
     // the S / the P V issuer finished (leader, once at the end).
     // A parity wait is only sound for the phase right after the last one
@@ -1451,9 +1456,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     // reads as complete, or as never completing): every barrier below is
     // waited for that way, which is why O += P V completes one barrier per S
     // buffer.
-    __shared__ __align__(8) uint64_t bar_kfull[k2Stages], bar_vfull[k2Stages],
-        bar_kfree[k2Stages], bar_vfree[k2Stages], bar_s[k2SBufs], bar_p[k2SBufs], bar_o[k2SBufs],
-        bar_q, bar_qr, bar_drain[2];
+    __shared__ __align__(8) uint64_t bar_kfull[k2Stages], bar_vfull[k2Stages], bar_s[k2SBufs],
+        bar_p[k2SBufs], bar_o[k2SBufs], bar_q, bar_qr, bar_drain[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -1486,8 +1490,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         for (int s = 0; s < k2Stages; ++s) {
             mbar_init(&bar_kfull[s], 1);
             mbar_init(&bar_vfull[s], 1);
-            mbar_init(&bar_kfree[s], 1);
-            mbar_init(&bar_vfree[s], 1);
         }
         for (int b = 0; b < k2SBufs; ++b) {
             mbar_init(&bar_s[b], 1);
@@ -1631,7 +1633,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                                            1024u, kSwizzle128),
                                  idesc, kk > 0);
                     umma2_commit(&bar_s[b], 3);
-                    umma2_commit(&bar_kfree[st], 3);
                 }
                 __syncwarp();
             }
@@ -1667,7 +1668,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                                  umma_desc(v_addr + kk * 2048u, kBoxBytes, 1024u, kSwizzle128),
                                  idesc, (kt > 0 || kk > 0) ? 1u : 0u);
                     umma2_commit(&bar_o[b], 3);
-                    umma2_commit(&bar_vfree[st], 3);
                 }
                 __syncwarp();
             }
@@ -1701,7 +1701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
             if (g_prev >= 0)
                 ok = __all_sync(0xffffffffu,
-                                attn_wait(&bar_kfree[g_prev % k2Stages],
+                                attn_wait(&bar_s[g_prev % k2Stages],
                                              (uint32_t)((g_prev / k2Stages) & 1), abort));
             if (!ok)
                 break;
@@ -1724,7 +1724,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 const int k0 = (int)(kt * kAttnKeys);
                 const uint32_t free_ph = (uint32_t)(((g / k2Stages) - 1) & 1);
                 if (g >= k2Stages)
-                    ok = __all_sync(0xffffffffu, attn_wait(&bar_kfree[st], free_ph, abort));
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_s[st], free_ph, abort));
                 if (!ok)
                     break;
                 // this CTA's half of key tile k0: keys k0 + 64 rank .. + 63;
@@ -1742,7 +1742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 }
                 k_last[st] = g;
                 if (g >= k2Stages)
-                    ok = __all_sync(0xffffffffu, attn_wait(&bar_vfree[st], free_ph, abort));
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_o[st], free_ph, abort));
                 if (!ok)
                     break;
                 // this CTA's half of value tile k0: feature columns 64 rank ..
