@@ -281,11 +281,19 @@ def reference_arm(args, w):
     dq, dk, _ = W.make_inputs(w, seed_offset=100)
     xs = [(q, w.Hq), (k, w.Hk), (dq, w.Hq), (dk, w.Hk)]
     cos32, sin32 = o.tables(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, "f32")
-    # size one step to ~0.25 s of CPU work
-    t0 = time.perf_counter()
-    oracle_sample_step(o, w, xs, pos, cos32, sin32, 8)
-    per_tok = (time.perf_counter() - t0) / 8
-    n_tok = int(max(1, min(w.S, 0.25 / max(per_tok, 1e-9))))
+    # the oracle is single-threaded; so is the slicing around it from here on
+    torch.set_num_threads(1)
+    # size one step so the whole run stays near two minutes of CPU work
+    budget = reference_step_seconds(args)
+    # a step costs about c0 + c1 * tokens: fit both from two sizes
+    times = []
+    for n in (8, 64):
+        t0 = time.perf_counter()
+        oracle_sample_step(o, w, xs, pos, cos32, sin32, min(n, w.S))
+        times.append(time.perf_counter() - t0)
+    c1 = max((times[1] - times[0]) / 56, 1e-9)
+    c0 = max(times[0] - 8 * c1, 0.0)
+    n_tok = int(max(1, min(w.S, (budget - c0) / c1)))
     for _ in range(args.warmup):
         oracle_sample_step(o, w, xs, pos, cos32, sin32, n_tok)
     t0 = time.perf_counter()
@@ -311,6 +319,12 @@ def reference_arm(args, w):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def reference_step_seconds(args) -> float:
+    """CPU seconds of one reference-arm step: at most 0.25 s, and about two
+    minutes for all warm-up and timed steps together."""
+    return min(0.25, 120.0 / max(1, args.steps + args.warmup))
 
 
 def config_of(w):
@@ -340,6 +354,86 @@ def attention_flops(B, Hq, Sq, Sk, D, causal):
     return 4.0 * B * Hq * D * pairs
 
 
+def attention_inputs(a):
+    """Seeded Q, K, V of the attention workload, on the CPU."""
+    g = torch.Generator().manual_seed(6)
+    q = W.draw((a["B"], a["Hq"], a["S"], a["D"]), a["dtype"], g)
+    k = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g)
+    v = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g)
+    return q, k, v
+
+
+def oracle_attention_rows(a, q, k, v, head, nq, c32, s32):
+    """The oracle on the last nq query rows of (batch 0, head), at their own
+    positions, against every key of its key/value head.  q, k, v may live on
+    any device; only those rows and heads are copied.  Returns the flops of
+    the visible pairs."""
+    import oracle as O
+    from oracle import attention as OA
+
+    S = a["S"]
+    hk = head // (a["Hq"] // a["Hk"])
+    pos_q = np.arange(S - nq, S, dtype=np.int32)
+    OA.attention(W.bits(q[:1, head:head + 1, S - nq:].cpu()), W.bits(k[:1, hk:hk + 1].cpu()),
+                 W.bits(v[:1, hk:hk + 1].cpu()), O.BF16, a["rotary_dim"], O.SPLIT_HALF, c32, s32,
+                 pos_q=pos_q, causal=True)
+    return attention_flops(1, 1, nq, S, a["D"], True)
+
+
+def attention_config(a, flops):
+    return {"workload": a["name"], "q_shape": [a["B"], a["Hq"], a["S"], a["D"]],
+            "kv_shape": [a["B"], a["Hk"], a["S"], a["D"]], "causal": a["causal"],
+            "rotary_dim": a["rotary_dim"], "flops_per_call": flops}
+
+
+def attention_reference_arm(args):
+    """The oracle on a bounded sample of the attention workload: per step the
+    last rows of one query head (heads taken in turn) against all keys."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0                               # rank 0 alone times the CPU oracle
+    import oracle as O
+
+    a = ATTN_WORKLOAD
+    q, k, v = attention_inputs(a)
+    c32, s32 = O.load().tables(a["theta"], a["rotary_dim"], a["S"], 1.0, "f32")
+    budget = reference_step_seconds(args)
+    # a step costs about c0 + c1 * rows: fit both from two sizes
+    times = []
+    for n in (16, 128):
+        t0 = time.perf_counter()
+        oracle_attention_rows(a, q, k, v, 0, n, c32, s32)
+        times.append(time.perf_counter() - t0)
+    c1 = max((times[1] - times[0]) / 112, 1e-9)
+    c0 = max(times[0] - 16 * c1, 0.0)
+    nq = int(max(1, min(a["S"], (budget - c0) / c1)))
+    for i in range(args.warmup):
+        oracle_attention_rows(a, q, k, v, i % a["Hq"], nq, c32, s32)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += oracle_attention_rows(a, q, k, v, i % a["Hq"], nq, c32, s32)
+    el = time.perf_counter() - t0
+    tflops = flops / el / 1e12
+    sample = ("batch 0, one query head per step (heads in turn), its last %d of %d query rows "
+              "against all keys (numpy fp64; threads as numpy uses them)" % (nq, a["S"]))
+    line = {
+        "impl": "reference", "metric": "fused rotary attention forward TFLOP/s", "op": "attention",
+        "value": round(tflops, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": a["dtype"],
+        "data": "synthetic", "config": attention_config(a, flops_of(a)),
+        "cpu_baseline": {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": os.cpu_count() or 0,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(tflops, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "the pages publish no runnable implementation; the reference arm is the fp64 "
+                "CPU oracle on this host",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def tensor_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -366,10 +460,7 @@ def attention_arm(args):
     import rotary_position_embedding_rope_gb300 as R
 
     a = ATTN_WORKLOAD
-    g = torch.Generator().manual_seed(6)
-    q = W.draw((a["B"], a["Hq"], a["S"], a["D"]), a["dtype"], g).to(device)
-    k = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g).to(device)
-    v = W.draw((a["B"], a["Hk"], a["S"], a["D"]), a["dtype"], g).to(device)
+    q, k, v = (t.to(device) for t in attention_inputs(a))
     cos, sin = R.build_tables(a["theta"], a["rotary_dim"], a["S"], device=device)
     stream = torch.cuda.current_stream(device)
     o = torch.empty_like(q)
@@ -483,22 +574,20 @@ def attention_arm(args):
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        from oracle import attention as OA
         import oracle as O
 
         c32, s32 = O.load().tables(a["theta"], a["rotary_dim"], a["S"], 1.0, "f32")
-        nq = 64
+        # the last nq query rows of heads 0, 1, ... of batch 0 until cpu_seconds are spent
+        nq, heads, sf = 64, 0, 0.0
         t0 = time.perf_counter()
-        # the last nq query rows (at their own positions) against every key
-        pos_q = np.arange(a["S"] - nq, a["S"], dtype=np.int32)
-        OA.attention(W.bits(q[:1, :1, a["S"] - nq:].cpu()), W.bits(k[:1, :1].cpu()),
-                     W.bits(v[:1, :1].cpu()), O.BF16, a["rotary_dim"], O.SPLIT_HALF, c32, s32,
-                     pos_q=pos_q, causal=True)
+        while heads < a["Hq"] and (heads == 0 or time.perf_counter() - t0 < args.cpu_seconds):
+            sf += oracle_attention_rows(a, q, k, v, heads, nq, c32, s32)
+            heads += 1
         el = time.perf_counter() - t0
-        sf = attention_flops(1, 1, nq, a["S"], a["D"], True)
         cpu = {"value": round(sf / el / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count() or 0,
-               "kind": "oracle", "sample": "1 head, the last %d of %d query rows against all keys "
-               "(numpy fp64; threads as numpy uses them)" % (nq, a["S"])}
+               "kind": "oracle", "sample": "batch 0, query heads 0-%d, the last %d of %d query rows "
+               "of each against all keys (numpy fp64; threads as numpy uses them)"
+               % (heads - 1, nq, a["S"])}
 
     peak, peak_kind = tensor_peak()
     if rank == 0:
@@ -507,9 +596,7 @@ def attention_arm(args):
             "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
             "warmup": warmup, "ms_per_step": round(max_ms / steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": a["dtype"], "data": "synthetic",
-            "config": {"workload": a["name"], "q_shape": [a["B"], a["Hq"], a["S"], a["D"]],
-                       "kv_shape": [a["B"], a["Hk"], a["S"], a["D"]], "causal": a["causal"],
-                       "rotary_dim": a["rotary_dim"], "flops_per_call": flops},
+            "config": attention_config(a, flops),
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "peak_source": "%s bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
@@ -648,9 +735,7 @@ def main():
         return xpos_arm(args)
     if args.op == "attention":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": "attention",
-                              "unavailable": "the reference arm times the rotation only"}))
-            return 0
+            return attention_reference_arm(args)
         return attention_arm(args)
     w = W.BY_NAME[args.workload]
     if args.impl == "reference":
@@ -803,8 +888,12 @@ def main():
 
         o = O.load()
         cos32, sin32 = o.tables(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, "f32")
+        # the oracle is single-threaded; so is the slicing around it while it is timed
+        threads = torch.get_num_threads()
+        torch.set_num_threads(1)
         nb, el, toks = time_oracle(w, args.cpu_seconds, [(q, w.Hq), (k, w.Hk), (dq, w.Hq),
                                                          (dk, w.Hk)], pos, cos32, sin32)
+        torch.set_num_threads(threads)
         cpu = {"value": round(nb / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "batch 0, growing prefixes of the %d tokens (%d token-steps in %.1f s), "
                          "all heads, forward on Q,K + backward on dQ,dK; host has %d cores, "
