@@ -74,3 +74,21 @@ def test_reference_arm_other_ranks_exit_quietly():
     p = _run_bench(["--impl", "reference", "--workload", "tiny_f32_split_half", "--steps", "1",
                     "--warmup", "1"], {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+def test_attention_reference_arm_prints_one_line():
+    p = _run_bench(["--impl", "reference", "--op", "attention", "--steps", "1", "--warmup", "0"])
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["op"] == "attention" and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "llama3_8b_prefill_attention_bf16"
+
+
+def test_attention_reference_arm_other_ranks_exit_quietly():
+    p = _run_bench(["--impl", "reference", "--op", "attention", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert p.returncode == 0 and p.stdout.strip() == ""
