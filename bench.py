@@ -545,7 +545,8 @@ def attention_arm(args):
     ho = torch.empty_like(hq).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size()
-    hat = HostAttention(device, chunks=a["B"])
+    pieces = a["B"]                    # one batch entry per call (more pieces measured slower)
+    hat = HostAttention(device, chunks=pieces)
 
     def e2e_step(after):
         return hat.forward(hq, hk, hv, ho, cos, sin, rotary_dim=a["rotary_dim"],
@@ -569,8 +570,8 @@ def attention_arm(args):
     e2e = {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
            "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
-           "what": "pinned host Q, K, V in and O out; %d batch chunks, copies overlapping the "
-                   "calls" % a["B"]}
+           "what": "pinned host Q, K, V in and O out; %d pieces (batch entry x group of "
+                   "key/value heads), copies overlapping the calls" % pieces}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

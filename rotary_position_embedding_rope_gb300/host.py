@@ -97,8 +97,13 @@ class HostRotator:
 class HostAttention:
     """softmax(scale * rot(q) rot(k)^T + mask) v for pinned host q, k, v into
     a pinned host o, through rope_attention_fwd with a key workspace, one call
-    per batch chunk.  Each chunk's copies of q, k, v in, the call, and the
-    copy of o out run on three streams, so neighbouring chunks overlap."""
+    per piece.  A piece is a run of whole batch entries, or, with more pieces
+    than batch entries, one batch entry's key/value heads split into equal
+    groups (with their query heads).  Each output row depends only on its own
+    query row and its key/value head, so every split gives the same bits.  Each
+    piece's copies of q, k, v in, the call, and the copy of o out run on three
+    streams, so neighbouring pieces overlap; more pieces leave less of the
+    first copy in and the last copy out exposed."""
 
     def __init__(self, device=None, chunks: int = 4):
         self.device = torch.device("cuda") if device is None else torch.device(device)
@@ -111,14 +116,28 @@ class HostAttention:
         self._ws = None
         self._free = [None, None]
 
-    def _staging(self, q, k, per):
-        key = (tuple(q.shape), tuple(k.shape), q.dtype, per)
+    def _pieces(self, B: int, Hk: int):
+        """(b0, b1, kv0, kv1) ranges covering [0, B) x [0, Hk)."""
+        if self.chunks <= B:
+            n = max(1, self.chunks)
+            per = (B + n - 1) // n
+            return [(b0, min(B, b0 + per), 0, Hk) for b0 in range(0, B, per)]
+        groups = 1
+        while B * groups * 2 <= self.chunks and Hk % (groups * 2) == 0:
+            groups *= 2
+        kv = Hk // groups
+        return [(b, b + 1, g * kv, (g + 1) * kv) for b in range(B) for g in range(groups)]
+
+    def _staging(self, q, k, nb, nkv, grp):
+        key = (tuple(q.shape), tuple(k.shape), q.dtype, nb, nkv)
         if key != self._key:
-            def dev(t):
-                return torch.empty((per,) + tuple(t.shape[1:]), dtype=t.dtype, device=self.device)
-            self._slots = [(dev(q), dev(k), dev(k), dev(q)) for _ in range(2)]
+            def dev(t, heads):
+                return torch.empty((nb, heads) + tuple(t.shape[2:]), dtype=t.dtype,
+                                   device=self.device)
+            self._slots = [(dev(q, nkv * grp), dev(k, nkv), dev(k, nkv), dev(q, nkv * grp))
+                           for _ in range(2)]
             # the calls all run on s_run, one after another: one workspace serves them
-            self._ws = dev(k)
+            self._ws = dev(k, nkv)
             self._key = key
             self._free = [None, None]
         return self._slots, self._ws
@@ -139,39 +158,44 @@ class HostAttention:
         _, Hk, Sk, _ = k.shape
         if v.shape != k.shape or o.shape != q.shape:
             raise ValueError("v must have k's shape and o q's shape")
+        if Hk < 1 or Hq % Hk:
+            raise ValueError("Hq must be a multiple of Hk")
+        grp = Hq // Hk
         rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
-        n = max(1, min(self.chunks, B))
-        per = (B + n - 1) // n
-        slots, ws = self._staging(q, k, per)
+        pieces = self._pieces(B, Hk)
+        nb = max(p[1] - p[0] for p in pieces)
+        nkv = max(p[3] - p[2] for p in pieces)
+        slots, ws = self._staging(q, k, nb, nkv, grp)
         ws_bytes = ws.numel() * ws.element_size()
         for s in (self.s_in, self.s_run, self.s_out):
             if after is not None:
                 s.wait_event(after)
         done = None
-        for c in range(n):
-            b0, b1 = c * per, min(B, (c + 1) * per)
-            if b0 >= b1:
-                break
+        for c, (b0, b1, kv0, kv1) in enumerate(pieces):
             slot = c % 2
-            dq, dk, dv, do = (t[: b1 - b0] for t in slots[slot])
+            hq0, hq1 = kv0 * grp, kv1 * grp
+            # a piece is whole batch entries or one entry's heads: contiguous either way
+            dq, dk, dv, do = slots[slot]
+            dq, do = dq[: b1 - b0, : hq1 - hq0], do[: b1 - b0, : hq1 - hq0]
+            dk, dv = dk[: b1 - b0, : kv1 - kv0], dv[: b1 - b0, : kv1 - kv0]
             if self._free[slot] is not None:
                 self.s_in.wait_event(self._free[slot])
             with torch.cuda.stream(self.s_in):
-                dq.copy_(q[b0:b1], non_blocking=True)
-                dk.copy_(k[b0:b1], non_blocking=True)
-                dv.copy_(v[b0:b1], non_blocking=True)
+                dq.copy_(q[b0:b1, hq0:hq1], non_blocking=True)
+                dk.copy_(k[b0:b1, kv0:kv1], non_blocking=True)
+                dv.copy_(v[b0:b1, kv0:kv1], non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(self.s_in)
             self.s_run.wait_event(ready)
-            rope_attention_fwd(dq, dk, dv, do, cos, sin, pos_q, pos_k, b1 - b0, Hq, Hk, Sq, Sk, D,
-                               rd, _LAYOUT_CODE[layout], int(causal),
+            rope_attention_fwd(dq, dk, dv, do, cos, sin, pos_q, pos_k, b1 - b0, hq1 - hq0,
+                               kv1 - kv0, Sq, Sk, D, rd, _LAYOUT_CODE[layout], int(causal),
                                -1.0 if scale is None else scale, _DTYPE_CODE[q.dtype],
                                cos.shape[0], ws, ws_bytes, self.s_run)
             computed = torch.cuda.Event()
             computed.record(self.s_run)
             self.s_out.wait_event(computed)
             with torch.cuda.stream(self.s_out):
-                o[b0:b1].copy_(do, non_blocking=True)
+                o[b0:b1, hq0:hq1].copy_(do, non_blocking=True)
                 done = torch.cuda.Event()
                 done.record(self.s_out)
             self._free[slot] = done

@@ -215,10 +215,11 @@ def test_attention_full_size_sampled_rows():
             b, h, i, np.abs(got - ref).max())
 
 
-@pytest.mark.parametrize("chunks", [1, 2, 3])
+@pytest.mark.parametrize("chunks", [1, 2, 3, 6])
 def test_host_attention_pipeline_matches_device_call(chunks):
     """Pinned host Q, K, V through the chunked copy/attend/copy pipeline give
-    the device call's bits, and leave the host inputs untouched."""
+    the device call's bits, and leave the host inputs untouched (6 pieces:
+    each batch entry's two key/value heads apart)."""
     require_gpu()
     R = lib()
     from rotary_position_embedding_rope_gb300.host import HostAttention
