@@ -294,6 +294,22 @@ rope_status rope_attention_fwd_noalloc(const void *q, const void *k, const void 
  */
 rope_status rope_check_errors(void *stream);
 
+/*
+ * rope_probe_wait_expiry -- diagnostic: exercise the path an expired wait
+ * takes, without stalling any real kernel.  One thread of one CTA waits,
+ * with the bounded mbarrier wait that the attention and bulk-staged kernels
+ * use, on a barrier that nothing arrives at; after `cycles` SM clock cycles
+ * (1 .. 4e9; 2e6 is about a millisecond) the wait gives up and sets the
+ * timeout bit of the device error flag, as an expired wait inside those
+ * kernels does.  The next rope_check_errors then returns
+ * ROPE_ERR_KERNEL_TIMEOUT and clears the flag.  The pages have no
+ * counterpart; this is an addition of this library, for tests and for
+ * callers that want to check their error handling.
+ * Errors: ROPE_ERR_INVALID_ARG for cycles outside 1 .. 4e9 (nothing is
+ *    launched); ROPE_ERR_CUDA if the launch fails.  Asynchronous on `stream`.
+ */
+rope_status rope_probe_wait_expiry(int64_t cycles, void *stream);
+
 /* rope_status_string -- static, NUL-terminated name of a status value. */
 const char *rope_status_string(rope_status status);
 

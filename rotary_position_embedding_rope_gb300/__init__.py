@@ -35,7 +35,7 @@ __all__ = [
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
     "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
     "rope_attention_fwd_noalloc", "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
-    "build_tables_ex", "apply_qk_xpos",
+    "build_tables_ex", "apply_qk_xpos", "rope_probe_wait_expiry",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
@@ -91,6 +91,8 @@ def load_library() -> ctypes.CDLL:
     lib.rope_apply_q.restype = c.c_int
     lib.rope_check_errors.argtypes = [P]
     lib.rope_check_errors.restype = c.c_int
+    lib.rope_probe_wait_expiry.argtypes = [c.c_int64, P]
+    lib.rope_probe_wait_expiry.restype = c.c_int
     lib.rope_status_string.argtypes = [c.c_int]
     lib.rope_status_string.restype = c.c_char_p
     lib.rope_qk_kernel_variant.argtypes = [P, P, P, P, P, c.c_int64, c.c_int32, c.c_int32,
@@ -216,6 +218,13 @@ def rope_apply_q(x, cos, sin, pos_idx, B, H, S, D, rotary_dim, layout, seq_befor
 def rope_check_errors(stream=None) -> int:
     """Synchronise the stream; returns the status (does not raise)."""
     return load_library().rope_check_errors(_stream(stream))
+
+
+def rope_probe_wait_expiry(cycles: int, stream=None) -> int:
+    """Launch one bounded wait that expires after `cycles` clock cycles and
+    sets the timeout bit of the device flag (the next rope_check_errors
+    returns ROPE_ERR_KERNEL_TIMEOUT).  Returns the launch status."""
+    return load_library().rope_probe_wait_expiry(int(cycles), _stream(stream))
 
 
 def rope_status_string(status: int) -> str:

@@ -516,6 +516,22 @@ rope_status rope_check_errors(void *stream)
     return value ? ROPE_ERR_POS_OUT_OF_RANGE : ROPE_OK;
 }
 
+// Longest wait the probe may take: the kernels' own bound (~2 s of clock).
+static constexpr int64_t kMaxProbeCycles = 4000000000LL;
+
+rope_status rope_probe_wait_expiry(int64_t cycles, void *stream)
+{
+    if (cycles <= 0 || cycles > kMaxProbeCycles)
+        return ROPE_ERR_INVALID_ARG;
+    int32_t *flag = nullptr, *taken = nullptr;
+    if (flag_addresses(&flag, &taken) != cudaSuccess)
+        return ROPE_ERR_CUDA;
+    return launch_wait_probe(flag, (long long)cycles, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? ROPE_OK
+               : ROPE_ERR_CUDA;
+}
+
 rope_status rope_force_kernel_variant(int32_t variant)
 {
     if (variant < 0 || variant > 3)

@@ -180,10 +180,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
                  : "memory");
 }
 
-// Bounded wait for the phase of the given parity; false on expiry (~2 s of
-// clock) or once another thread of the CTA has raised *abort.
+// Bounded wait for the phase of the given parity; false on expiry (after
+// `limit` clock cycles, ~2 s by default) or once another thread of the CTA
+// has raised *abort.
 __device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity,
-                                          const volatile int *abort = nullptr)
+                                          const volatile int *abort = nullptr,
+                                          long long limit = kAttnWaitCycles)
 {
     const long long t0 = clock64();
     while (true) {
@@ -196,7 +198,7 @@ __device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity,
                      : "memory");
         if (done)
             return true;
-        if ((abort != nullptr && *abort) || clock64() - t0 > kAttnWaitCycles)
+        if ((abort != nullptr && *abort) || clock64() - t0 > limit)
             return false;
     }
 }
@@ -1975,6 +1977,26 @@ static cudaError_t launch_attn_d(const AttnArgs &a, const AttnMaps &maps, int32_
 {
     return layout == 0 ? launch_attn_layout<T, 0, D>(a, maps, pair_heads, st)
                        : launch_attn_layout<T, 1, D>(a, maps, pair_heads, st);
+}
+
+// Probe of the expiry path: one thread waits, with the attention kernels'
+// bounded wait, on a barrier that nothing arrives at; after `cycles` clock
+// cycles the wait gives up and the thread records the expiry as those kernels
+// do (bit 1 of the device flag).  Nothing else runs, so nothing stalls.
+__global__ void rope_wait_probe_kernel(int32_t *flag, long long cycles)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0)
+        mbar_init(&bar, 1);
+    __syncthreads();
+    if (threadIdx.x == 0 && !attn_wait(&bar, 0u, nullptr, cycles))
+        atomicOr(flag, 2);
+}
+
+cudaError_t launch_wait_probe(int32_t *flag, long long cycles, cudaStream_t st)
+{
+    rope_wait_probe_kernel<<<1, 32, 0, st>>>(flag, cycles);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,

@@ -106,6 +106,9 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
                              cudaStream_t st);
+// One bounded mbarrier wait that expires after `cycles` clock cycles and sets
+// bit 1 of *flag (rope_probe_wait_expiry).
+cudaError_t launch_wait_probe(int32_t *flag, long long cycles, cudaStream_t st);
 
 // Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).
 cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);

@@ -279,3 +279,9 @@ def test_attention_rejects_bad_arguments(lib, over, status):
 def test_attention_empty_is_noop(lib):
     assert lib.rope_attention_fwd(*attn_args(Sq=0, q=None, o=None)) == R.ROPE_OK
     assert lib.rope_attention_fwd(*attn_args(B=0)) == R.ROPE_OK
+
+
+@pytest.mark.parametrize("cycles", [0, -5, 4000000001])
+def test_wait_probe_rejects_cycles_out_of_range(lib, cycles):
+    # checked before any CUDA call: nothing is launched
+    assert lib.rope_probe_wait_expiry(cycles, None) == R.ROPE_ERR_INVALID_ARG
