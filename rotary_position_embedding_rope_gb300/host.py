@@ -16,27 +16,42 @@ import torch
 from . import _DTYPE_CODE, _LAYOUT_CODE, _shape4, rope_apply_qk_out, rope_attention_fwd
 
 
+def _head_groups(B: int, heads: tuple, chunks: int) -> int:
+    """Groups per batch entry when a call is cut into more pieces than batch
+    entries: the largest power of two with B * groups <= chunks that divides
+    every head count (1: batch pieces only)."""
+    groups = 1
+    while B * groups * 2 <= chunks and all(h % (groups * 2) == 0 for h in heads if h):
+        groups *= 2
+    return groups
+
+
 class HostRotator:
+    """Rotation of pinned host Q and K into pinned host outputs.  A piece is a
+    run of whole batch entries or, with more pieces than batch entries and
+    the [B,H,S,D] layout (each entry's heads contiguous), one entry's heads
+    split into equal groups of Q heads and of K heads.  Every head is rotated
+    on its own, so every split gives the same bits."""
+
     def __init__(self, device=None, chunks: int = 4):
         self.device = torch.device("cuda") if device is None else torch.device(device)
         self.chunks = chunks
         self.s_in = torch.cuda.Stream(self.device)
         self.s_run = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
-        self._staging = {}
+        self._key = None
+        self._slots = None
         self._free = [None, None]          # event: staging slot's device->host copy done
 
-    def _slots(self, shape_q, shape_k, dtype, rows_q, rows_k):
-        key = (shape_q, shape_k, dtype)
-        if key not in self._staging:
-            self._staging = {key: [(torch.empty((rows_q,) + tuple(shape_q[1:]), dtype=dtype,
-                                                device=self.device),
-                                    None if shape_k is None else
-                                    torch.empty((rows_k,) + tuple(shape_k[1:]), dtype=dtype,
-                                                device=self.device))
-                                   for _ in range(2)]}
+    def _staging(self, q, k, dims_q, dims_k):
+        key = (tuple(q.shape), None if k is None else tuple(k.shape), q.dtype, dims_q, dims_k)
+        if key != self._key:
+            def dev(dims):
+                return torch.empty(dims, dtype=q.dtype, device=self.device)
+            self._slots = [(dev(dims_q), None if k is None else dev(dims_k)) for _ in range(2)]
+            self._key = key
             self._free = [None, None]
-        return self._staging[key]
+        return self._slots
 
     def apply_qk(self, q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor,
                  sin: torch.Tensor, q_out: torch.Tensor, k_out: torch.Tensor | None,
@@ -55,39 +70,54 @@ class HostRotator:
             if t is not None and (t.is_cuda or not t.is_pinned() or not t.is_contiguous()):
                 raise ValueError("host tensors must be contiguous pinned CPU memory")
         rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
-        n = max(1, min(self.chunks, B))
-        per = (B + n - 1) // n
-        slots = self._slots(q.shape, None if k is None else k.shape, q.dtype, per, per)
+        groups = 1 if seq_before_head else _head_groups(B, (Hq, Hk), self.chunks)
+        if groups == 1:
+            n = max(1, min(self.chunks, B))
+            per = (B + n - 1) // n
+            pieces = [(b0, min(B, b0 + per), 0, 1) for b0 in range(0, B, per)]
+        else:
+            per = 1
+            pieces = [(b, b + 1, g, groups) for b in range(B) for g in range(groups)]
+        hq_c, hk_c = Hq // groups, Hk // groups
+        slots = self._staging(q, k, (per,) + tuple(q.shape[1:]) if groups == 1 else (1, hq_c, S, D),
+                              None if k is None else
+                              ((per,) + tuple(k.shape[1:]) if groups == 1 else (1, hk_c, S, D)))
         for s in (self.s_in, self.s_run, self.s_out):
             if after is not None:
                 s.wait_event(after)
         done = None
-        for c in range(n):
-            b0, b1 = c * per, min(B, (c + 1) * per)
-            if b0 >= b1:
-                break
+        for c, (b0, b1, g, ng) in enumerate(pieces):
             slot = c % 2
             dq, dk = slots[slot]
             dq, dk = dq[: b1 - b0], None if dk is None else dk[: b1 - b0]
+            if ng == 1:                    # whole batch entries
+                src_q, src_k = q[b0:b1], None if k is None else k[b0:b1]
+                dst_q, dst_k = q_out[b0:b1], None if k is None else k_out[b0:b1]
+            else:                          # heads of one entry ([B,H,S,D]: contiguous)
+                src_q, dst_q = q[b0, g * hq_c:(g + 1) * hq_c], q_out[b0, g * hq_c:(g + 1) * hq_c]
+                src_k = None if k is None else k[b0, g * hk_c:(g + 1) * hk_c]
+                dst_k = None if k is None else k_out[b0, g * hk_c:(g + 1) * hk_c]
+                dq = dq[0]
+                dk = None if dk is None else dk[0]
             if self._free[slot] is not None:
                 self.s_in.wait_event(self._free[slot])
             with torch.cuda.stream(self.s_in):
-                dq.copy_(q[b0:b1], non_blocking=True)
+                dq.copy_(src_q, non_blocking=True)
                 if k is not None:
-                    dk.copy_(k[b0:b1], non_blocking=True)
+                    dk.copy_(src_k, non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(self.s_in)
             self.s_run.wait_event(ready)
-            rope_apply_qk_out(dq, dk, dq, dk, cos, sin, pos_idx, 0, b1 - b0, Hq, Hk, S, D, rd,
-                              _LAYOUT_CODE[layout], int(seq_before_head), int(backward),
+            rope_apply_qk_out(dq, dk, dq, dk, cos, sin, pos_idx, 0, b1 - b0, Hq // ng, Hk // ng,
+                              S, D, rd, _LAYOUT_CODE[layout], int(seq_before_head), int(backward),
                               _DTYPE_CODE[q.dtype], cos.shape[0], self.s_run)
             rotated = torch.cuda.Event()
             rotated.record(self.s_run)
             self.s_out.wait_event(rotated)
             with torch.cuda.stream(self.s_out):
-                q_out[b0:b1].copy_(dq, non_blocking=True)
+                dst_q.copy_(dq, non_blocking=True)
                 if k is not None:
-                    k_out[b0:b1].copy_(dk, non_blocking=True)
+                    dst_k.copy_(dk, non_blocking=True)
                 done = torch.cuda.Event()
                 done.record(self.s_out)
             self._free[slot] = done
@@ -122,9 +152,7 @@ class HostAttention:
             n = max(1, self.chunks)
             per = (B + n - 1) // n
             return [(b0, min(B, b0 + per), 0, Hk) for b0 in range(0, B, per)]
-        groups = 1
-        while B * groups * 2 <= self.chunks and Hk % (groups * 2) == 0:
-            groups *= 2
+        groups = _head_groups(B, (Hk,), self.chunks)
         kv = Hk // groups
         return [(b, b + 1, g * kv, (g + 1) * kv) for b in range(B) for g in range(groups)]
 

@@ -139,10 +139,11 @@ def test_autograd_forward_and_backward(dtype):
     assert_matches(dtype, gpu_bits(qg2.grad), yb, y64)
 
 
-@pytest.mark.parametrize("chunks", [1, 2, 4])
+@pytest.mark.parametrize("chunks", [1, 2, 4, 10])
 def test_host_pipeline_matches_device_call(chunks):
     """Pinned host tensors rotated through the chunked copy/rotate/copy pipeline
-    give the same bits as the device call."""
+    give the same bits as the device call (10 pieces: each batch entry's heads
+    in two groups)."""
     require_gpu()
     R = lib()
     from rotary_position_embedding_rope_gb300.host import HostRotator
@@ -160,3 +161,29 @@ def test_host_pipeline_matches_device_call(chunks):
         R.apply_qk(dq, dk, cos, sin, backward=backward)
         assert torch.equal(oq, dq.cpu()) and torch.equal(ok_, dk.cpu())
         assert torch.equal(hq, q) and torch.equal(hk, k)
+
+
+@pytest.mark.parametrize("sbh,with_k", [(False, False), (True, True)])
+def test_host_pipeline_head_pieces_q_only_and_seq_first(sbh, with_k):
+    """More pieces than batch entries: Q alone is split by head groups; the
+    [B,S,H,D] layout (heads not contiguous per entry) falls back to batch
+    pieces.  Both give the device call's bits."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostRotator
+
+    w = case(3, 4, 2, 48, 64, 64, "f16", sbh=sbh, rows=48)
+    q, k, _ = W.make_inputs(w)
+    cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+    rot = HostRotator(chunks=12)
+    hq = q.pin_memory()
+    hk = k.pin_memory() if with_k else None
+    oq = torch.empty_like(q).pin_memory()
+    ok_ = torch.empty_like(k).pin_memory() if with_k else None
+    rot.apply_qk(hq, hk, cos, sin, oq, ok_, seq_before_head=sbh).synchronize()
+    dq = q.cuda()
+    dk = k.cuda() if with_k else None
+    R.apply_qk(dq, dk, cos, sin, seq_before_head=sbh)
+    assert torch.equal(oq, dq.cpu())
+    if with_k:
+        assert torch.equal(ok_, dk.cpu())
