@@ -16,7 +16,10 @@ torch.  ``autograd.rotary_qk`` wraps the out-of-place call in a
 'constant') at given positions, optionally XPOS-scaled; ``apply_qk_xpos``
 rotates Q and K with their own XPOS tables.  ``attention`` calls
 ``rope_attention_fwd``: attention with the rotation fused into the Q/K tile
-loads (or, with a key workspace, keys rotated once beforehand).  ``host.HostRotator`` rotates tensors that live in pinned host memory.
+loads (or, with a key workspace, keys rotated once beforehand).
+``host.HostRotator`` and ``host.HostAttention`` run the rotation and the
+attention on tensors that live in pinned host memory, overlapping the copies
+with the calls.
 """
 from __future__ import annotations
 
