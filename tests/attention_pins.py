@@ -14,7 +14,13 @@ runs them on mutants.  What fixes each expected value:
     oracle states);
   * GQA is the same as repeating each key/value head over its query group;
   * brute force: scalar Python loops on tiny cases, in fp64 and in bf16 with
-    the rotated rows rounded as the oracle's reading says.
+    the rotated rows rounded as the oracle's reading says;
+  * the attn_mask: an all-True mask is no mask, hiding a key is deleting it
+    (with its position), a per-query mask shaped like the causal pattern is
+    the causal mask, and a row whose keys are all hidden gives zeros;
+  * the bound weights W = sum p |v| / l and A = sum_vis |v| / l: constant
+    values give W = |c|, one visible key gives W = A = |v_0|, and always
+    |O| <= W <= A with W blind to the sign of V.
 """
 import math
 
@@ -196,6 +202,85 @@ def pin_default_scale_is_inverse_sqrt_d(A):
     assert np.max(np.abs(o - o3)) > 1e-6
 
 
+def pin_bound_weights_closed_forms(A):
+    B, H, Sq, Sk, D = 1, 2, 6, 9, 8
+    c, s = _tables(D, Sk)
+    q, k, v = _x((B, H, Sq, D), 31), _x((B, H, Sk, D), 32), _x((B, H, Sk, D), 33)
+    for causal in (False, True):
+        o, w, a = A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, None, None, causal,
+                              want_bounds=True)
+        assert np.array_equal(o, A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, None, None,
+                                             causal))
+        assert np.all(np.abs(o) <= w + 1e-12) and np.all(w <= a + 1e-12)
+        # the sign of V changes O's sign, not the weights
+        o2, w2, a2 = A.attention(q, k, -v, O.F64, D, O.SPLIT_HALF, c, s, None, None, causal,
+                                 want_bounds=True)
+        assert np.allclose(o2, -o, atol=1e-12) and np.allclose(w2, w, atol=1e-12)
+        assert np.allclose(a2, a, atol=1e-12)
+        # constant values: W is |c| whatever the weights, A is |c| times the
+        # visible keys over the softmax sum (>= |c|, = |c| for one key)
+        cv = np.broadcast_to(np.linspace(-2.0, 1.5, D), (B, H, Sk, D)).copy()
+        _, wc, ac = A.attention(q, k, cv, O.F64, D, O.SPLIT_HALF, c, s, None, None, causal,
+                                want_bounds=True)
+        assert np.allclose(wc, np.abs(cv[:, :, :Sq]), atol=1e-12)
+        assert np.all(ac >= np.abs(cv[:, :, :Sq]) - 1e-12)
+    # causal with Sq = Sk: the first query sees key 0 alone (p = 1, l = 1)
+    o, w, a = A.attention(q, k[:, :, :Sq], v[:, :, :Sq], O.F64, D, O.SPLIT_HALF, c, s, None, None,
+                          True, want_bounds=True)
+    assert np.array_equal(w[:, :, 0], np.abs(v[:, :, 0])) and np.array_equal(a[:, :, 0],
+                                                                             np.abs(v[:, :, 0]))
+
+
+def pin_attn_mask_hides_keys(A):
+    B, Hq, Hk, Sq, Sk, D = 2, 4, 2, 5, 11, 8
+    c, s = _tables(D, 32)
+    q, k, v = _x((B, Hq, Sq, D), 34), _x((B, Hk, Sk, D), 35), _x((B, Hk, Sk, D), 36)
+    pq = np.arange(Sk - Sq, Sk, dtype=np.int32)
+    pk = np.arange(Sk, dtype=np.int32)
+    for causal in (False, True):
+        base = A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, causal)
+        ones = np.ones((B, Sk), dtype=bool)
+        assert np.array_equal(base, A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk,
+                                                causal, attn_mask=ones))
+        # batch 0 hides keys 1 and 6, batch 1 hides its last three: the same as
+        # deleting those keys (with their positions) from each batch entry
+        mask = ones.copy()
+        mask[0, [1, 6]] = False
+        mask[1, Sk - 3:] = False
+        got = A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, causal, attn_mask=mask)
+        for b in range(B):
+            keep = np.flatnonzero(mask[b])
+            want = A.attention(q[b:b + 1], k[b:b + 1][:, :, keep], v[b:b + 1][:, :, keep], O.F64, D,
+                               O.SPLIT_HALF, c, s, pq, pk[keep].copy(), False,
+                               attn_mask=None if not causal else
+                               (keep[None, None, :] <= (np.arange(Sq)[None, :, None] + Sk - Sq)))
+            assert np.max(np.abs(got[b] - want[0])) <= 1e-12
+        # a [B, Sq, Sk] mask equal to the causal pattern is the causal mask; the
+        # same key mask broadcast over the queries is the key mask
+        pat = np.arange(Sk)[None, :] <= (np.arange(Sq)[:, None] + (Sk - Sq))
+        full = np.broadcast_to(pat, (B, Sq, Sk)).copy()
+        assert np.max(np.abs(A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, False,
+                                         attn_mask=full) -
+                             A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, True))) == 0
+        bcast = np.broadcast_to(mask[:, None, :], (B, Sq, Sk)).copy()
+        assert np.array_equal(got, A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk,
+                                               causal, attn_mask=bcast))
+    # every key of batch 1 hidden: zeros there, batch 0 unchanged
+    mask = np.ones((B, Sk), dtype=bool)
+    mask[1] = False
+    got = A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, False, attn_mask=mask)
+    assert np.array_equal(got[1], np.zeros_like(got[1]))
+    assert np.array_equal(got[0], A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk)[0])
+    # one query row of batch 0 with all its keys hidden
+    m3 = np.ones((B, Sq, Sk), dtype=bool)
+    m3[0, 2] = False
+    got = A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk, False, attn_mask=m3)
+    assert np.array_equal(got[0, :, 2], np.zeros((Hq, D)))
+    assert np.array_equal(np.delete(got, 2, axis=2)[0],
+                          np.delete(A.attention(q, k, v, O.F64, D, O.SPLIT_HALF, c, s, pq, pk), 2,
+                                    axis=2)[0])
+
+
 ALL_PINS = [
     pin_shifting_all_positions_leaves_attention_unchanged,
     pin_constant_values_give_the_constant,
@@ -207,4 +292,6 @@ ALL_PINS = [
     pin_brute_force_scalar_loops_tiny_case,
     pin_bf16_rotated_rows_are_rounded_before_the_products,
     pin_default_scale_is_inverse_sqrt_d,
+    pin_bound_weights_closed_forms,
+    pin_attn_mask_hides_keys,
 ]

@@ -43,6 +43,16 @@ MUTANTS = [
     ("scores_missing_scale", [("s = (q[b, h] @ k[b, kh].T) * scale", "s = q[b, h] @ k[b, kh].T")]),
     ("softmax_over_queries", [("m = s.max(axis=1, keepdims=True)", "m = s.max(axis=0, keepdims=True)"),
                               ("l = p.sum(axis=1, keepdims=True)", "l = p.sum(axis=0, keepdims=True)")]),
+    ("bound_w_signed", [("w_abs[b, h] = (p @ av) * inv_l", "w_abs[b, h] = (p @ v[b, kh]) * inv_l")]),
+    ("bound_w_unnormalised", [("w_abs[b, h] = (p @ av) * inv_l", "w_abs[b, h] = p @ av")]),
+    ("bound_a_all_keys", [("a_abs[b, h] = (visible.astype(np.float64) @ av) * inv_l",
+                           "a_abs[b, h] = av.sum(axis=0)[None, :] * inv_l")]),
+    ("mask_ignored", [("visible = visible & (mb[None, :] if mb.ndim == 1 else mb)", "pass")]),
+    ("mask_inverted", [("visible = visible & (mb[None, :] if mb.ndim == 1 else mb)",
+                        "visible = visible & ~(mb[None, :] if mb.ndim == 1 else mb)")]),
+    ("mask_replaces_causal", [("visible = visible & (mb[None, :] if mb.ndim == 1 else mb)",
+                               "visible = (mb[None, :] if mb.ndim == 1 else mb) | (visible & False)")]),
+    ("mask_of_first_batch", [("mb = attn_mask[b]", "mb = attn_mask[0]")]),
 ]
 
 
