@@ -53,6 +53,13 @@ typedef enum {
 
 typedef enum { ROPE_SPLIT_HALF = 0, ROPE_INTERLEAVED = 1 } rope_layout;
 typedef enum { ROPE_F32 = 0, ROPE_BF16 = 1, ROPE_F16 = 2 } rope_dtype;
+/* attention masks ("rotary-embedding-torch", flash_attn_with_rotary / Input
+ * Tensor Shapes: attn_mask (batch, seq_len_k) or (batch, seq_len_q, seq_len_k)) */
+typedef enum {
+    ROPE_MASK_NONE = 0,
+    ROPE_MASK_KEYS = 1,        /* uint8 [B, Sk]: one entry per key (key padding) */
+    ROPE_MASK_QUERY_KEYS = 2   /* uint8 [B, Sq, Sk]: one entry per query and key */
+} rope_mask_kind;
 /* frequency modes ("rotary-embedding-torch", RotaryEmbedding: freqs_for) */
 typedef enum { ROPE_FREQ_LANG = 0, ROPE_FREQ_PIXEL = 1, ROPE_FREQ_CONSTANT = 2 } rope_freq_mode;
 
@@ -178,9 +185,7 @@ rope_status rope_apply_qk(void *q, void *k, const float *cos, const float *sin,
  *     (b, s) uses pos_idx[b * pos_batch_stride + s] -- one position vector per
  *     sequence, e.g. sequences decoded at different offsets.
  * Other strides return ROPE_ERR_INVALID_ARG.  Everything else (sizes, flags,
- * errors, range flag) as for rope_apply_qk.  The bulk-copy kernel (variant 1)
- * rotates in place only: forcing it with an out-of-place output returns
- * ROPE_ERR_UNSUPPORTED.
+ * errors, range flag) as for rope_apply_qk.
  */
 rope_status rope_apply_qk_out(const void *q, const void *k, void *q_out, void *k_out,
                               const float *cos, const float *sin, const int32_t *pos_idx,
@@ -252,6 +257,40 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
                                void *stream);
 
 /*
+ * rope_attention_fwd_masked -- rope_attention_fwd with a boolean attention
+ * mask ("rotary-embedding-torch", flash_attn_with_rotary / Input Tensor
+ * Shapes: attn_mask, batch x seq_len_k or batch x seq_len_q x seq_len_k,
+ * whose False entries are excluded like masked scores):
+ *
+ *   o = softmax(scale * rot(q) rot(k)^T + causal mask + attn_mask) v
+ *
+ * attn_mask: device bytes, 0 = the key is hidden from the query (its score
+ *    becomes -inf), any other value = visible (torch.bool tensors qualify):
+ *      mask_kind ROPE_MASK_KEYS:       [B, Sk], the same for every query
+ *                                      (padded batches: key padding);
+ *      mask_kind ROPE_MASK_QUERY_KEYS: [B, Sq, Sk], one row per query (read
+ *                                      as 16-byte vectors when the pointer
+ *                                      is 16-byte aligned and Sk % 16 == 0,
+ *                                      else byte by byte);
+ *      mask_kind ROPE_MASK_NONE:       ignored (may be NULL): rope_attention_fwd.
+ *    Dense, contiguous, shared by all heads; it must not overlap o or the
+ *    workspace.  The mask applies together with `causal`; a query row that
+ *    sees no key gets zeros.
+ * Everything else as rope_attention_fwd.
+ * Errors: as rope_attention_fwd; also ROPE_ERR_UNSUPPORTED for a mask_kind
+ *    outside the enum and ROPE_ERR_INVALID_ARG for a NULL mask (with Sk > 0)
+ *    or one that overlaps o or the workspace.
+ */
+rope_status rope_attention_fwd_masked(const void *q, const void *k, const void *v, void *o,
+                                      const float *cos, const float *sin, const int32_t *pos_q,
+                                      const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk,
+                                      int64_t Sq, int64_t Sk, int32_t D, int32_t rotary_dim,
+                                      int32_t layout, int32_t causal, float softmax_scale,
+                                      int32_t dtype, int64_t table_rows, const uint8_t *attn_mask,
+                                      int32_t mask_kind, void *k_workspace,
+                                      int64_t workspace_bytes, void *stream);
+
+/*
  * rope_attention_fwd_noalloc -- rope_attention_fwd with the key workspace
  * taken from a fixed device array inside this library (32 MiB), for callers
  * that cannot allocate device memory at call time: an engine that has
@@ -261,13 +300,17 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
  * point; it is an addition of this library.
  *
  * Arguments, result and errors: as rope_attention_fwd with k_workspace set,
- * except that rot(K) goes to the library's array.  ROPE_ERR_UNSUPPORTED when
- * B * Hk * Sk * D * 2 bytes exceed 32 MiB (33554432 bytes), before anything
- * touches the device.  Nothing is allocated or freed, and no allocating
- * library routine is called.
+ * except that rot(K) goes to the library's array.  The arguments are checked
+ * first, exactly as rope_attention_fwd checks them (its error, if any, is
+ * returned); then ROPE_ERR_UNSUPPORTED when B * Hk * Sk * D * 2 bytes exceed
+ * 32 MiB (33554432 bytes).  Both happen before anything touches the device.
+ * Nothing is allocated or freed, and no allocating library routine is called.
  * Set-up: the first call on a device (with that device current) looks up the
  *    array's device address once (cudaGetSymbolAddress) and caches it; make
- *    that first call before any stream capture.
+ *    that first call before any stream capture.  The cached address belongs
+ *    to the device's context as it was then: after cudaDeviceReset (or any
+ *    reset of the primary context) the process must be restarted before this
+ *    entry point is called again.
  * Sharing: every device that loads the library holds the 32 MiB array until
  *    the process exits.  All calls on a device share it; each call rewrites
  *    the part it uses before reading it (nothing needs to start at zero), and
@@ -285,9 +328,8 @@ rope_status rope_attention_fwd_noalloc(const void *q, const void *k, const void 
  * rope_check_errors -- synchronise `stream`, then report and clear the
  * current device's error flag.
  * Returns ROPE_ERR_CUDA if the stream reports an error, else
- * ROPE_ERR_KERNEL_TIMEOUT if a wait inside the bulk-staged rotation kernel or
- * the attention kernel expired (about 2 s; that launch stopped early and its
- * output is incomplete), else
+ * ROPE_ERR_KERNEL_TIMEOUT if a wait inside an attention kernel expired
+ * (about 2 s; that launch stopped early and its output is incomplete), else
  * ROPE_ERR_POS_OUT_OF_RANGE if any launch since the last check met an
  * out-of-range position index, else ROPE_OK.  The flag is shared by all
  * streams of the device.
@@ -297,8 +339,7 @@ rope_status rope_check_errors(void *stream);
 /*
  * rope_probe_wait_expiry -- diagnostic: exercise the path an expired wait
  * takes, without stalling any real kernel.  One thread of one CTA waits,
- * with the bounded mbarrier wait that the attention and bulk-staged kernels
- * use, on a barrier that nothing arrives at; after `cycles` SM clock cycles
+ * with the bounded mbarrier wait that the attention kernels use, on a barrier that nothing arrives at; after `cycles` SM clock cycles
  * (1 .. 4e9; 2e6 is about a millisecond) the wait gives up and sets the
  * timeout bit of the device error flag, as an expired wait inside those
  * kernels does.  The next rope_check_errors then returns
@@ -317,10 +358,9 @@ const char *rope_status_string(rope_status status);
  * rope_qk_kernel_variant -- which kernel rope_apply_qk would launch for
  * these arguments, without launching anything or touching the device.
  * Returns 0 when nothing would be launched (error or empty problem),
- * 1 for the bulk-copy staged kernel (rows move between HBM and shared memory
- * through the copy engine; the default for 16-byte aligned shapes),
  * 2 for the element-wise kernel (any shape or alignment),
- * 3 for the register-staged 16-byte vector kernel.
+ * 3 for the register-staged 16-byte vector kernel (the automatic choice
+ * for 16-byte aligned shapes whose rotary span is whole pairs of vectors).
  * Useful for tests and for callers checking that their tensors are aligned.
  */
 int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, const float *sin,
@@ -331,13 +371,29 @@ int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, c
 
 /*
  * rope_force_kernel_variant -- process-wide choice of the rotation kernel,
- * for tests and tuning: 0 = automatic (default), 1, 2 or 3 as returned by
- * rope_qk_kernel_variant.  While 1 or 3 is forced, calls whose shapes or
- * pointers do not qualify for it return ROPE_ERR_UNSUPPORTED.  All three
- * kernels compute bit-identical results.  ROPE_ERR_INVALID_ARG for other
- * values.
+ * for tests and tuning: 0 = automatic (default), 2 or 3 as returned by
+ * rope_qk_kernel_variant.  While 3 is forced, calls whose shapes or pointers
+ * do not qualify for it return ROPE_ERR_UNSUPPORTED.  Both kernels compute
+ * bit-identical results.  ROPE_ERR_INVALID_ARG for other values.
  */
 rope_status rope_force_kernel_variant(int32_t variant);
+
+/*
+ * rope_tune_rotation_launch -- process-wide grid sizing of the vector
+ * rotation kernel, for tuning and measurement; the results do not depend on
+ * it.  The kernel splits its work, units of (TT consecutive tokens, one
+ * head), into balanced contiguous runs, one per lane group of TT rows.
+ *   ctas_per_sm: cap the grid at this many CTAs per SM (0 = as many as can
+ *     be resident at once, the default; 1 .. 64 otherwise);
+ *   min_units: the fewest units a run holds before the grid grows (0 = the
+ *     default, 1);
+ *   prefetch_next: 1 or 0 = while rotating a tile, prefetch the first heads
+ *     of the run's next tile into L2 (the default); -1 = do not.
+ * ROPE_ERR_INVALID_ARG for values outside these ranges (nothing changes).
+ * The pages have no counterpart; this is an addition of this library.
+ */
+rope_status rope_tune_rotation_launch(int32_t ctas_per_sm, int32_t min_units,
+                                      int32_t prefetch_next);
 
 #ifdef __cplusplus
 }

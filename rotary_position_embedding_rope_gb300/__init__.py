@@ -32,21 +32,23 @@ from . import _build
 
 __all__ = [
     "RopeError", "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
-    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_ERR_KERNEL_TIMEOUT", "VARIANT_BULK", "VARIANT_ELEMENTWISE",
-    "VARIANT_VECTOR", "rope_force_kernel_variant", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
+    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_ERR_KERNEL_TIMEOUT", "VARIANT_ELEMENTWISE",
+    "VARIANT_VECTOR", "rope_force_kernel_variant", "rope_tune_rotation_launch", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
     "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
     "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
     "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
     "rope_attention_fwd_noalloc", "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
-    "build_tables_ex", "apply_qk_xpos", "rope_probe_wait_expiry",
+    "build_tables_ex", "apply_qk_xpos", "rope_probe_wait_expiry", "rope_attention_fwd_masked",
+    "ROPE_MASK_NONE", "ROPE_MASK_KEYS", "ROPE_MASK_QUERY_KEYS", "PreparedApply",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
  ROPE_ERR_KERNEL_TIMEOUT) = range(6)
-VARIANT_BULK, VARIANT_ELEMENTWISE, VARIANT_VECTOR = 1, 2, 3
+VARIANT_ELEMENTWISE, VARIANT_VECTOR = 2, 3
 ROPE_SPLIT_HALF, ROPE_INTERLEAVED = 0, 1
 ROPE_F32, ROPE_BF16, ROPE_F16 = 0, 1, 2
 ROPE_FREQ_LANG, ROPE_FREQ_PIXEL, ROPE_FREQ_CONSTANT = 0, 1, 2
+ROPE_MASK_NONE, ROPE_MASK_KEYS, ROPE_MASK_QUERY_KEYS = 0, 1, 2
 _FREQ_CODE = {"lang": ROPE_FREQ_LANG, "pixel": ROPE_FREQ_PIXEL, "constant": ROPE_FREQ_CONSTANT}
 _DTYPE_CODE = {torch.float32: ROPE_F32, torch.bfloat16: ROPE_BF16, torch.float16: ROPE_F16}
 _LAYOUT_CODE = {"split_half": ROPE_SPLIT_HALF, "interleaved": ROPE_INTERLEAVED}
@@ -111,6 +113,11 @@ def load_library() -> ctypes.CDLL:
                                        c.c_int32, c.c_float, c.c_int32, c.c_int64, P,
                                        c.c_int64, P]
     lib.rope_attention_fwd.restype = c.c_int
+    lib.rope_attention_fwd_masked.argtypes = [P, P, P, P, P, P, P, P, c.c_int64, c.c_int32,
+                                              c.c_int32, c.c_int64, c.c_int64, c.c_int32,
+                                              c.c_int32, c.c_int32, c.c_int32, c.c_float,
+                                              c.c_int32, c.c_int64, P, c.c_int32, P, c.c_int64, P]
+    lib.rope_attention_fwd_masked.restype = c.c_int
     lib.rope_attention_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, c.c_int64, c.c_int32,
                                                c.c_int32, c.c_int64, c.c_int64, c.c_int32,
                                                c.c_int32, c.c_int32, c.c_int32, c.c_float,
@@ -118,6 +125,8 @@ def load_library() -> ctypes.CDLL:
     lib.rope_attention_fwd_noalloc.restype = c.c_int
     lib.rope_force_kernel_variant.argtypes = [c.c_int32]
     lib.rope_force_kernel_variant.restype = c.c_int
+    lib.rope_tune_rotation_launch.argtypes = [c.c_int32, c.c_int32, c.c_int32]
+    lib.rope_tune_rotation_launch.restype = c.c_int
     _lib = lib
     return lib
 
@@ -248,6 +257,14 @@ def rope_force_kernel_variant(variant: int):
     _check(load_library().rope_force_kernel_variant(int(variant)), "rope_force_kernel_variant")
 
 
+def rope_tune_rotation_launch(ctas_per_sm: int = 0, min_units: int = 0, prefetch_next: int = 0):
+    """Grid sizing of the vector rotation kernel (0 = defaults); results do
+    not depend on it."""
+    _check(load_library().rope_tune_rotation_launch(int(ctas_per_sm), int(min_units),
+                                                    int(prefetch_next)),
+           "rope_tune_rotation_launch")
+
+
 # --------------------------------------------------------------------------
 # conveniences
 # --------------------------------------------------------------------------
@@ -319,6 +336,68 @@ def apply_qk(q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor, sin: to
                   int(seq_before_head), int(backward), _DTYPE_CODE[q.dtype], cos.shape[0],
                   stream)
     return q, k
+
+
+class PreparedApply:
+    """rope_apply_qk with every argument but q and k checked and converted
+    once, for calls repeated on tensors of one shape (a model layer, a decode
+    loop): each call marshals two pointers and the fixed rest.
+
+        f = PreparedApply(q, k, cos, sin, stream=s)   # shapes, tables, layout
+        f(q, k)                  # forward, in place
+        f(dq, dk, backward=True)
+
+    q and k of later calls must have the shapes and dtype of the ones given
+    here (their element counts are checked; raw integer addresses are passed
+    as they are).  The stream is fixed here (None: torch's current stream at
+    this point).  Only marshalling: the library does the work."""
+
+    def __init__(self, q, k, cos, sin, pos_idx=None, rotary_dim=None, layout="split_half",
+                 seq_before_head=False, stream=None):
+        B, Hq, S, D = _shape4(q, seq_before_head)
+        Hk = 0
+        if k is not None:
+            Bk, Hk, Sk, Dk = _shape4(k, seq_before_head)
+            if (Bk, Sk, Dk) != (B, S, D) or k.dtype != q.dtype:
+                raise ValueError("q and k must agree in batch, sequence, head_dim and dtype")
+        if q.dtype not in _DTYPE_CODE:
+            raise TypeError("unsupported dtype %s" % q.dtype)
+        if cos.dtype != torch.float32 or sin.dtype != torch.float32 or cos.shape != sin.shape:
+            raise ValueError("cos and sin must be float32 tables of the same shape")
+        rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
+        if cos.shape[1] != rd // 2:
+            raise ValueError("table width %d does not match rotary_dim %d" % (cos.shape[1], rd))
+        if pos_idx is not None and (pos_idx.dtype != torch.int32 or pos_idx.numel() != S):
+            raise ValueError("pos_idx must be int32 with S elements")
+        c = ctypes
+        self._fn = load_library().rope_apply_qk
+        self._keep = (cos, sin, pos_idx)
+        self._nq, self._nk = q.numel(), 0 if k is None else k.numel()
+        head = [c.c_void_p(_addr(cos, "cos")), c.c_void_p(_addr(sin, "sin")),
+                c.c_void_p(_addr(pos_idx, "pos_idx")), c.c_int64(B), c.c_int32(Hq),
+                c.c_int32(Hk), c.c_int64(S), c.c_int32(D), c.c_int32(rd),
+                c.c_int32(_LAYOUT_CODE[layout]), c.c_int32(int(seq_before_head))]
+        tail = [c.c_int32(_DTYPE_CODE[q.dtype]), c.c_int64(cos.shape[0]),
+                c.c_void_p(_stream(stream))]
+        self._fwd = tuple(head + [c.c_int32(0)] + tail)
+        self._bwd = tuple(head + [c.c_int32(1)] + tail)
+
+    def __call__(self, q, k=None, backward: bool = False):
+        if isinstance(q, int):
+            qp = q
+        else:
+            if q.numel() != self._nq:
+                raise ValueError("q does not have the prepared shape")
+            qp = q.data_ptr()
+        if k is None or isinstance(k, int):
+            kp = k
+        else:
+            if k.numel() != self._nk:
+                raise ValueError("k does not have the prepared shape")
+            kp = k.data_ptr()
+        st = self._fn(qp, kp, *(self._bwd if backward else self._fwd))
+        if st != ROPE_OK:
+            raise RopeError(st, "rope_apply_qk")
 
 
 def apply_q(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
@@ -418,6 +497,21 @@ def rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D,
     _check(st, "rope_attention_fwd")
 
 
+def rope_attention_fwd_masked(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim,
+                              layout, causal, softmax_scale, dtype, table_rows, attn_mask,
+                              mask_kind, k_workspace=None, workspace_bytes=0, stream=None):
+    lib = load_library()
+    st = lib.rope_attention_fwd_masked(_addr(q, "q"), _addr(k, "k"), _addr(v, "v"), _addr(o, "o"),
+                                       _addr(cos, "cos"), _addr(sin, "sin"), _addr(pos_q, "pos_q"),
+                                       _addr(pos_k, "pos_k"), int(B), int(Hq), int(Hk), int(Sq),
+                                       int(Sk), int(D), int(rotary_dim), int(layout), int(causal),
+                                       float(softmax_scale), int(dtype), int(table_rows),
+                                       _addr(attn_mask, "attn_mask"), int(mask_kind),
+                                       _addr(k_workspace, "k_workspace"), int(workspace_bytes),
+                                       _stream(stream))
+    _check(st, "rope_attention_fwd_masked")
+
+
 def rope_attention_fwd_noalloc(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D,
                                rotary_dim, layout, causal, softmax_scale, dtype, table_rows,
                                stream=None):
@@ -440,7 +534,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
               sin: torch.Tensor, pos_q: torch.Tensor | None = None,
               pos_k: torch.Tensor | None = None, rotary_dim: int | None = None,
               layout: str = "split_half", causal: bool = False, scale: float | None = None,
-              out: torch.Tensor | None = None, k_workspace="auto", stream=None) -> torch.Tensor:
+              out: torch.Tensor | None = None, k_workspace="auto",
+              attn_mask: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """softmax(scale * rot(q) rot(k)^T + mask) v with q [B,Hq,Sq,D], k/v [B,Hk,Sk,D].
 
     k_workspace: "auto" allocates a buffer like k that receives rot(K) (the
@@ -448,6 +543,9 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
     tensor of k's size is used as that buffer; None rotates the key tiles
     inside the attention kernel instead (nothing extra is written).  The
     result is the same bit for bit.
+    attn_mask: None, or a bool (or uint8) CUDA tensor [B, Sk] (one entry per
+    key) or [B, Sq, Sk] (one per query and key); False hides the key from the
+    query, together with the causal mask.
     """
     B, Hq, Sq, D = q.shape
     _, Hk, Sk, _ = k.shape
@@ -460,7 +558,19 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
             raise ValueError("k_workspace must be 'auto', None or a tensor")
         k_workspace = torch.empty_like(k)
     ws_bytes = 0 if k_workspace is None else k_workspace.numel() * k_workspace.element_size()
-    rope_attention_fwd(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rd,
-                       _LAYOUT_CODE[layout], int(causal), -1.0 if scale is None else scale,
-                       _DTYPE_CODE[q.dtype], cos.shape[0], k_workspace, ws_bytes, stream)
+    args = (q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rd, _LAYOUT_CODE[layout],
+            int(causal), -1.0 if scale is None else scale, _DTYPE_CODE[q.dtype], cos.shape[0])
+    if attn_mask is None:
+        rope_attention_fwd(*args, k_workspace, ws_bytes, stream)
+        return o
+    if attn_mask.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("attn_mask must be bool or uint8")
+    if tuple(attn_mask.shape) == (B, Sk):
+        kind = ROPE_MASK_KEYS
+    elif tuple(attn_mask.shape) == (B, Sq, Sk):
+        kind = ROPE_MASK_QUERY_KEYS
+    else:
+        raise ValueError("attn_mask must be [B, Sk] or [B, Sq, Sk], got %s" %
+                         (tuple(attn_mask.shape),))
+    rope_attention_fwd_masked(*args, attn_mask, kind, k_workspace, ws_bytes, stream)
     return o

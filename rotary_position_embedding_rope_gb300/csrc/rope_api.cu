@@ -16,9 +16,9 @@ namespace rope {
 // ---------------------------------------------------------------------------
 // Device flag word: bit 0 is set (atomicOr) by the rotation kernels when a
 // position index is outside [0, table_rows) and not -1; bit 1 when a wait of
-// the bulk-staged kernel ran out of its time budget.  One word per device; the
-// kernels get its address as an argument.  g_flag_taken receives the value
-// read-and-cleared by rope_check_errors.
+// an attention kernel (or of rope_probe_wait_expiry) ran out of its time
+// budget.  One word per device; the kernels get its address as an argument.
+// g_flag_taken receives the value read-and-cleared by rope_check_errors.
 // ---------------------------------------------------------------------------
 __device__ int32_t g_range_flag;
 __device__ int32_t g_flag_taken;
@@ -141,6 +141,18 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Kernel variant forced by rope_force_kernel_variant (0 = automatic choice).
 static std::atomic<int32_t> g_forced_variant{0};
 
+// Grid sizing of the register kernel (rope_tune_rotation_launch).
+static std::atomic<int32_t> g_tune_ctas_per_sm{0}, g_tune_min_units{0}, g_tune_prefetch_next{0};
+
+VecLaunchTuning vec_launch_tuning()
+{
+    VecLaunchTuning t;
+    t.ctas_per_sm = g_tune_ctas_per_sm.load(std::memory_order_relaxed);
+    t.min_units = g_tune_min_units.load(std::memory_order_relaxed);
+    t.prefetch_next = g_tune_prefetch_next.load(std::memory_order_relaxed);
+    return t;
+}
+
 struct Plan {
     ApplyArgs args;
     int32_t layout;
@@ -261,18 +273,15 @@ static rope_status plan_apply(const CallArgs &c, Plan *plan)
     const int64_t span_bytes = c.rotary_dim * elt;
     bool vec = (span_bytes % 32) == 0 && ((int64_t)c.D * elt) % 16 == 0 && aligned16(c.cos) &&
                aligned16(c.sin) && span_bytes / 32 <= kMaxVectorsPerHalf;
-    bool copies = false;
-    for (int t = 0; t < n; ++t) {
+    for (int t = 0; t < n; ++t)
         vec = vec && aligned16(a.t[t].base) && aligned16(a.out[t]);
-        copies = copies || a.copy_through[t];
-    }
     const int32_t forced = g_forced_variant.load(std::memory_order_relaxed);
     if (forced == kScalar)
         plan->variant = kScalar;
-    else if (forced == kBulk || forced == kVector) {
-        if (!vec || (forced == kBulk && copies))       // the bulk kernel works in place only
+    else if (forced == kVector) {
+        if (!vec)
             return ROPE_ERR_UNSUPPORTED;
-        plan->variant = static_cast<Variant>(forced);
+        plan->variant = kVector;
     } else
         plan->variant = vec ? kVector : kScalar;
     return ROPE_OK;
@@ -414,6 +423,155 @@ int32_t rope_qk_kernel_variant(const void *q, const void *k, const float *cos, c
     return plan_apply(c, &plan) == ROPE_OK ? (int32_t)plan.variant : 0;
 }
 
+}  // extern "C"
+
+namespace rope {
+
+// All arguments of an attention call.
+struct AttnCall {
+    const void *q, *k, *v;
+    void *o;
+    const float *cos, *sin;
+    const int32_t *pos_q, *pos_k;
+    int64_t B;
+    int32_t Hq, Hk;
+    int64_t Sq, Sk;
+    int32_t D, rotary_dim, layout, causal;
+    float softmax_scale;
+    int32_t dtype;
+    int64_t table_rows;
+    const uint8_t *mask;
+    int32_t mask_kind;
+    void *k_workspace;
+    int64_t workspace_bytes;
+};
+
+// Host checks of an attention call, in order; *empty is set when the call
+// has no output rows (nothing to do).  No CUDA calls.
+static rope_status attention_check(const AttnCall &c, bool *empty, int64_t *kbytes)
+{
+    *empty = false;
+    if (c.dtype != ROPE_BF16 && c.dtype != ROPE_F16)
+        return ROPE_ERR_UNSUPPORTED;
+    if (c.layout != ROPE_SPLIT_HALF && c.layout != ROPE_INTERLEAVED)
+        return ROPE_ERR_UNSUPPORTED;
+    if (c.D != 64 && c.D != 128)
+        return ROPE_ERR_UNSUPPORTED;
+    if (c.rotary_dim < 16 || c.rotary_dim > c.D || (c.rotary_dim % 16) != 0)
+        return ROPE_ERR_UNSUPPORTED;
+    if (c.mask_kind < ROPE_MASK_NONE || c.mask_kind > ROPE_MASK_QUERY_KEYS)
+        return ROPE_ERR_UNSUPPORTED;
+    if ((c.causal != 0 && c.causal != 1) || c.B < 0 || c.Sq < 0 || c.Sk < 0 || c.Hq < 0 ||
+        c.Hk < 0 || c.table_rows < 0 || !(c.softmax_scale == c.softmax_scale))
+        return ROPE_ERR_INVALID_ARG;
+    if (c.Hq > 0 && (c.Hk == 0 || c.Hq % c.Hk != 0))
+        return ROPE_ERR_INVALID_ARG;
+    int64_t nq = 0, nk = 0, qb = 0, kb = 0, tab = 0, tabb = 0, mb = 0;
+    if (!mul_ok(c.B * (int64_t)c.Hq, c.Sq, &nq) || !mul_ok(nq, (int64_t)c.D * 2, &qb) ||
+        !mul_ok(c.B * (int64_t)c.Hk, c.Sk, &nk) || !mul_ok(nk, (int64_t)c.D * 2, &kb) ||
+        !mul_ok(c.table_rows, c.rotary_dim / 2, &tab) || !mul_ok(tab, 4, &tabb) ||
+        !mul_ok(c.B, c.Sk, &mb) ||
+        (c.mask_kind == ROPE_MASK_QUERY_KEYS && !mul_ok(mb, c.Sq, &mb)))
+        return ROPE_ERR_INVALID_ARG;
+    if (c.mask_kind == ROPE_MASK_NONE)
+        mb = 0;
+    *kbytes = kb;
+    if (c.B == 0 || c.Hq == 0 || c.Sq == 0) {
+        *empty = true;                                   // no output rows
+        return ROPE_OK;
+    }
+    if (!c.q || !c.o || !c.cos || !c.sin || (c.Sk > 0 && (!c.k || !c.v)) ||
+        (c.Sk > 0 && c.mask_kind != ROPE_MASK_NONE && !c.mask))
+        return ROPE_ERR_INVALID_ARG;
+    if (c.table_rows < 1 || (!c.pos_q && c.Sq > c.table_rows) || (!c.pos_k && c.Sk > c.table_rows))
+        return ROPE_ERR_INVALID_ARG;
+    if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.o) ||
+        !aligned16(c.cos) || !aligned16(c.sin))
+        return ROPE_ERR_UNSUPPORTED;
+    const void *o = c.o;
+    if (ranges_overlap(o, qb, c.q, qb) || ranges_overlap(o, qb, c.k, kb) ||
+        ranges_overlap(o, qb, c.v, kb) || ranges_overlap(o, qb, c.cos, tabb) ||
+        ranges_overlap(o, qb, c.sin, tabb) || ranges_overlap(o, qb, c.pos_q, c.Sq * 4) ||
+        ranges_overlap(o, qb, c.pos_k, c.Sk * 4) || ranges_overlap(o, qb, c.mask, mb))
+        return ROPE_ERR_INVALID_ARG;
+    // the key workspace receives rot(K): at least kb bytes, aligned, and
+    // disjoint from every other buffer of the call
+    const void *ws = c.Sk > 0 ? c.k_workspace : nullptr;
+    if (ws != nullptr) {
+        if (c.workspace_bytes < kb)
+            return ROPE_ERR_INVALID_ARG;
+        if (!aligned16(ws))
+            return ROPE_ERR_UNSUPPORTED;
+        if (ranges_overlap(ws, kb, c.q, qb) || ranges_overlap(ws, kb, c.k, kb) ||
+            ranges_overlap(ws, kb, c.v, kb) || ranges_overlap(ws, kb, o, qb) ||
+            ranges_overlap(ws, kb, c.cos, tabb) || ranges_overlap(ws, kb, c.sin, tabb) ||
+            ranges_overlap(ws, kb, c.pos_q, c.Sq * 4) || ranges_overlap(ws, kb, c.pos_k, c.Sk * 4) ||
+            ranges_overlap(ws, kb, c.mask, mb))
+            return ROPE_ERR_INVALID_ARG;
+    }
+    return ROPE_OK;
+}
+
+static rope_status attention_call(const AttnCall &c, void *stream)
+{
+    bool empty = false;
+    int64_t kb = 0;
+    const rope_status st = attention_check(c, &empty, &kb);
+    if (st != ROPE_OK || empty)
+        return st;
+    void *ws = c.Sk > 0 ? c.k_workspace : nullptr;
+    AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.q = c.q; a.k = c.k; a.v = c.v; a.o = c.o;
+    a.k_rot = ws;
+    a.cos = c.cos; a.sin = c.sin;
+    a.pos_q = c.pos_q; a.pos_k = c.pos_k;
+    a.B = c.B; a.Hq = c.Hq; a.Hk = c.Hk; a.Sq = c.Sq; a.Sk = c.Sk;
+    a.rotary_dim = c.rotary_dim;
+    a.table_rows = c.table_rows;
+    const double scale = c.softmax_scale > 0.0f ? c.softmax_scale : 1.0 / std::sqrt((double)c.D);
+    a.scale_log2 = (float)(scale * 1.4426950408889634);
+    a.causal = c.causal;
+    a.mask_kind = c.Sk > 0 ? c.mask_kind : ROPE_MASK_NONE;
+    a.mask = a.mask_kind != ROPE_MASK_NONE ? c.mask : nullptr;
+    a.mask_vec16 = a.mask_kind == ROPE_MASK_QUERY_KEYS && aligned16(c.mask) && c.Sk % 16 == 0;
+    int32_t *taken = nullptr;
+    if (flag_addresses(&a.flag, &taken) != cudaSuccess)
+        return ROPE_ERR_CUDA;
+    if (ws != nullptr) {
+        // rot(K) into the workspace, by the rotation kernel on the same stream
+        // (out of place: -1 and out-of-range positions copy the key unchanged)
+        const CallArgs r = {nullptr, c.k, nullptr, ws, c.cos, c.sin, c.pos_k, 0, c.B, 0, c.Hk, c.Sk,
+                            c.D, c.rotary_dim, c.layout, 0, 0, c.dtype, c.table_rows};
+        const rope_status s = apply_call(r, stream);
+        if (s != ROPE_OK)
+            return s;
+    }
+    return launch_attention(a, c.D, c.layout, c.dtype, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? ROPE_OK
+               : ROPE_ERR_CUDA;
+}
+
+rope_status attention_args_status(const void *q, const void *k, const void *v, void *o,
+                                  const float *cos, const float *sin, const int32_t *pos_q,
+                                  const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk,
+                                  int64_t Sq, int64_t Sk, int32_t D, int32_t rotary_dim,
+                                  int32_t layout, int32_t causal, float softmax_scale,
+                                  int32_t dtype, int64_t table_rows)
+{
+    const AttnCall c = {q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim, layout,
+                        causal, softmax_scale, dtype, table_rows, nullptr, ROPE_MASK_NONE, nullptr,
+                        0};
+    bool empty = false;
+    int64_t kb = 0;
+    return attention_check(c, &empty, &kb);
+}
+
+}  // namespace rope
+
+extern "C" {
+
 rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void *o,
                                const float *cos, const float *sin, const int32_t *pos_q,
                                const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
@@ -422,78 +580,25 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
                                int64_t table_rows, void *k_workspace, int64_t workspace_bytes,
                                void *stream)
 {
-    if (dtype != ROPE_BF16 && dtype != ROPE_F16)
-        return ROPE_ERR_UNSUPPORTED;
-    if (layout != ROPE_SPLIT_HALF && layout != ROPE_INTERLEAVED)
-        return ROPE_ERR_UNSUPPORTED;
-    if (D != 64 && D != 128)
-        return ROPE_ERR_UNSUPPORTED;
-    if (rotary_dim < 16 || rotary_dim > D || (rotary_dim % 16) != 0)
-        return ROPE_ERR_UNSUPPORTED;
-    if ((causal != 0 && causal != 1) || B < 0 || Sq < 0 || Sk < 0 || Hq < 0 || Hk < 0 ||
-        table_rows < 0 || !(softmax_scale == softmax_scale))
-        return ROPE_ERR_INVALID_ARG;
-    if (Hq > 0 && (Hk == 0 || Hq % Hk != 0))
-        return ROPE_ERR_INVALID_ARG;
-    int64_t nq = 0, nk = 0, qb = 0, kb = 0, tab = 0, tabb = 0;
-    if (!mul_ok(B * (int64_t)Hq, Sq, &nq) || !mul_ok(nq, (int64_t)D * 2, &qb) ||
-        !mul_ok(B * (int64_t)Hk, Sk, &nk) || !mul_ok(nk, (int64_t)D * 2, &kb) ||
-        !mul_ok(table_rows, rotary_dim / 2, &tab) || !mul_ok(tab, 4, &tabb))
-        return ROPE_ERR_INVALID_ARG;
-    if (B == 0 || Hq == 0 || Sq == 0)
-        return ROPE_OK;                                  // no output rows
-    if (!q || !o || !cos || !sin || (Sk > 0 && (!k || !v)))
-        return ROPE_ERR_INVALID_ARG;
-    if (table_rows < 1 || (!pos_q && Sq > table_rows) || (!pos_k && Sk > table_rows))
-        return ROPE_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(cos) ||
-        !aligned16(sin))
-        return ROPE_ERR_UNSUPPORTED;
-    if (ranges_overlap(o, qb, q, qb) || ranges_overlap(o, qb, k, kb) ||
-        ranges_overlap(o, qb, v, kb) || ranges_overlap(o, qb, cos, tabb) ||
-        ranges_overlap(o, qb, sin, tabb) || ranges_overlap(o, qb, pos_q, Sq * 4) ||
-        ranges_overlap(o, qb, pos_k, Sk * 4))
-        return ROPE_ERR_INVALID_ARG;
-    // the key workspace receives rot(K): at least kb bytes, aligned, and
-    // disjoint from every other buffer of the call
-    void *ws = Sk > 0 ? k_workspace : nullptr;
-    if (ws != nullptr) {
-        if (workspace_bytes < kb)
-            return ROPE_ERR_INVALID_ARG;
-        if (!aligned16(ws))
-            return ROPE_ERR_UNSUPPORTED;
-        if (ranges_overlap(ws, kb, q, qb) || ranges_overlap(ws, kb, k, kb) ||
-            ranges_overlap(ws, kb, v, kb) || ranges_overlap(ws, kb, o, qb) ||
-            ranges_overlap(ws, kb, cos, tabb) || ranges_overlap(ws, kb, sin, tabb) ||
-            ranges_overlap(ws, kb, pos_q, Sq * 4) || ranges_overlap(ws, kb, pos_k, Sk * 4))
-            return ROPE_ERR_INVALID_ARG;
-    }
-    AttnArgs a;
-    a.q = q; a.k = k; a.v = v; a.o = o;
-    a.k_rot = ws;
-    a.cos = cos; a.sin = sin;
-    a.pos_q = pos_q; a.pos_k = pos_k;
-    a.B = B; a.Hq = Hq; a.Hk = Hk; a.Sq = Sq; a.Sk = Sk;
-    a.rotary_dim = rotary_dim;
-    a.table_rows = table_rows;
-    const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt((double)D);
-    a.scale_log2 = (float)(scale * 1.4426950408889634);
-    a.causal = causal;
-    int32_t *taken = nullptr;
-    if (flag_addresses(&a.flag, &taken) != cudaSuccess)
-        return ROPE_ERR_CUDA;
-    if (ws != nullptr) {
-        // rot(K) into the workspace, by the rotation kernel on the same stream
-        // (out of place: -1 and out-of-range positions copy the key unchanged)
-        const CallArgs c = {nullptr, k, nullptr, ws, cos, sin, pos_k, 0, B, 0, Hk, Sk, D,
-                            rotary_dim, layout, 0, 0, dtype, table_rows};
-        const rope_status s = apply_call(c, stream);
-        if (s != ROPE_OK)
-            return s;
-    }
-    return launch_attention(a, D, layout, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? ROPE_OK
-               : ROPE_ERR_CUDA;
+    const AttnCall c = {q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim, layout,
+                        causal, softmax_scale, dtype, table_rows, nullptr, ROPE_MASK_NONE,
+                        k_workspace, workspace_bytes};
+    return attention_call(c, stream);
+}
+
+rope_status rope_attention_fwd_masked(const void *q, const void *k, const void *v, void *o,
+                                      const float *cos, const float *sin, const int32_t *pos_q,
+                                      const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk,
+                                      int64_t Sq, int64_t Sk, int32_t D, int32_t rotary_dim,
+                                      int32_t layout, int32_t causal, float softmax_scale,
+                                      int32_t dtype, int64_t table_rows, const uint8_t *attn_mask,
+                                      int32_t mask_kind, void *k_workspace,
+                                      int64_t workspace_bytes, void *stream)
+{
+    const AttnCall c = {q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rotary_dim, layout,
+                        causal, softmax_scale, dtype, table_rows, attn_mask, mask_kind,
+                        k_workspace, workspace_bytes};
+    return attention_call(c, stream);
 }
 
 rope_status rope_check_errors(void *stream)
@@ -534,9 +639,21 @@ rope_status rope_probe_wait_expiry(int64_t cycles, void *stream)
 
 rope_status rope_force_kernel_variant(int32_t variant)
 {
-    if (variant < 0 || variant > 3)
+    if (variant != kNone && variant != kScalar && variant != kVector)
         return ROPE_ERR_INVALID_ARG;
     g_forced_variant.store(variant, std::memory_order_relaxed);
+    return ROPE_OK;
+}
+
+rope_status rope_tune_rotation_launch(int32_t ctas_per_sm, int32_t min_units,
+                                      int32_t prefetch_next)
+{
+    if (ctas_per_sm < 0 || ctas_per_sm > 64 || min_units < 0 || prefetch_next < -1 ||
+        prefetch_next > 1)
+        return ROPE_ERR_INVALID_ARG;
+    g_tune_ctas_per_sm.store(ctas_per_sm, std::memory_order_relaxed);
+    g_tune_min_units.store(min_units, std::memory_order_relaxed);
+    g_tune_prefetch_next.store(prefetch_next, std::memory_order_relaxed);
     return ROPE_OK;
 }
 

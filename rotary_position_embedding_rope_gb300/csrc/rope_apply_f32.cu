@@ -1,13 +1,11 @@
 // rope_apply_f32.cu -- instantiates the rotation kernels for float elements.
 // One translation unit per element type so the library builds in parallel.
-#include "rope_bulk.cuh"
+#include "rope_kernels.cuh"
 
 namespace rope {
 
 cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st)
 {
-    if (v == kBulk)
-        return launch_bulk<float>(a, layout, st);
     return launch_apply<float>(a, layout, v, st);
 }
 

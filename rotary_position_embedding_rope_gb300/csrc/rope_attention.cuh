@@ -1,4 +1,4 @@
-// rope_attention.cu -- attention forward with the rotation fused into the
+// rope_attention.cuh -- attention forward with the rotation fused into the
 // loads of the Q and K tiles, on the sm_103a tensor cores (tcgen05, TMEM, TMA).
 //
 // "rotary-embedding-torch", flash_attn_with_rotary: the rotary transformation
@@ -47,6 +47,8 @@
 // a role whose wait expires raises a shared abort flag that ends the other
 // roles' waits; warp 8 then waits (bounded) for its copies and MMAs in
 // flight, TMEM is freed and the timeout flag is raised.
+#pragma once
+
 #include <atomic>
 #include <cstring>
 #include <type_traits>
@@ -665,11 +667,71 @@ struct ONoWait {
     __device__ __forceinline__ bool operator()() const { return true; }
 };
 
-template <typename T, int D, bool PACKED, typename OReady = ONoWait>
+// Bytes b0..b3 of x that are nonzero, as bits 0..3.
+__device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t x)
+{
+    // 0x80 in each nonzero byte, moved to bit 0 of its byte; one multiply
+    // then gathers bits 0, 8, 16, 24 into bits 21..24 (no two partial
+    // products overlap, so nothing carries)
+    const uint32_t t = (__vcmpne4(x, 0u) & 0x80808080u) >> 7;
+    return (t * 0x00204081u) >> 21 & 0xFu;
+}
+
+// attn_mask of the 128 keys k0 .. k0 + 127 for query row qi of batch b
+// (warp-collective): bit (i & 31) of vis[i >> 5] set when key k0 + i is
+// visible.  Keys at or past Sk, and rows at or past Sq, read as visible
+// (the tile's key count and the row's own bound hide them).
+//   a.mask_kind 1, [B, Sk]: lane l reads keys k0 + 32e + l (e = 0..3), four
+//     coalesced 32-byte reads shared by every row of the batch, and a ballot
+//     per e gives word e to all lanes;
+//   a.mask_kind 2, [B, Sq, Sk]: each row reads its own 128 bytes, as eight
+//     16-byte vectors when the rows are 16-byte aligned (a.mask_vec16), else
+//     byte by byte.
+__device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t qi, int64_t k0,
+                                          uint32_t (&vis)[4])
+{
+    if (a.mask_kind == 1) {
+        const int lane = threadIdx.x & 31;
+        const uint8_t *row = a.mask + b * a.Sk;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t kk = k0 + 32 * e + lane;
+            const bool on = kk >= a.Sk || __ldg(row + kk) != 0;
+            vis[e] = __ballot_sync(0xffffffffu, on);
+        }
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        vis[e] = 0xffffffffu;
+    if (qi >= a.Sq)
+        return;
+    const uint8_t *row = a.mask + (b * a.Sq + qi) * a.Sk + k0;
+    const int64_t nk = a.Sk - k0;                   // keys of this row from k0 on
+    if (a.mask_vec16) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {               // chunk c: keys 16c .. 16c + 15
+            if (16 * c < nk) {
+                const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row) + c);
+                const uint32_t m16 = nonzero_bytes4(x.x) | nonzero_bytes4(x.y) << 4 |
+                                     nonzero_bytes4(x.z) << 8 | nonzero_bytes4(x.w) << 12;
+                vis[c >> 1] &= ~(0xFFFFu << (16 * (c & 1))) | (m16 << (16 * (c & 1)));
+            }
+        }
+    } else {
+#pragma unroll 8
+        for (int i = 0; i < kAttnKeys; ++i) {
+            if (i < nk && row[i] == 0)
+                vis[i >> 5] &= ~(1u << (i & 31));
+        }
+    }
+}
+
+template <typename T, int D, bool PACKED, bool MASK, typename OReady = ONoWait>
 __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base, int64_t qi,
                                              int64_t k0, int64_t shift, const AttnArgs &a,
-                                             bool not_first, float &m_ref, float &l_run,
-                                             const OReady &o_ready = OReady())
+                                             int64_t b, bool not_first, float &m_ref,
+                                             float &l_run, const OReady &o_ready = OReady())
 {
     // columns of this tile visible to this row: [0, nvis)
     int64_t vis_end = a.Sk;                // first invisible key
@@ -677,7 +739,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base,
         vis_end = qi + shift + 1;
     const int64_t nv = vis_end - k0;
     const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
-    const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no mask in this tile
+    // the attn_mask of this tile, if any (before S is read: its loads do not
+    // wait behind the tensor-memory loads)
+    uint32_t vis[4];
+    bool unmasked = true;                  // no attn_mask bit clear in this tile
+    if constexpr (MASK) {
+        mask_bits(a, b, qi, k0, vis);
+        unmasked = __all_sync(0xffffffffu, (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu);
+    }
+    const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no causal/length mask
     float sv[kAttnKeys];
 #pragma unroll
     for (int c0 = 0; c0 < kAttnKeys; c0 += 32)
@@ -687,6 +757,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base,
 #pragma unroll
         for (int i = 0; i < kAttnKeys; ++i)
             sv[i] = i < nvis ? sv[i] : -INFINITY;  // masked keys: 2^-inf = 0 below
+    }
+    if constexpr (MASK) {
+        if (!unmasked) {
+#pragma unroll
+            for (int i = 0; i < kAttnKeys; ++i)
+                sv[i] = (vis[i >> 5] >> (i & 31)) & 1u ? sv[i] : -INFINITY;
+        }
     }
     float m8[8];
 #pragma unroll
@@ -797,7 +874,7 @@ __device__ __forceinline__ void store_o_row(uint32_t o_base, T *O, int64_t qi, i
     }
 }
 
-template <typename T, int LAYOUT, int D, bool STAGED>
+template <typename T, int LAYOUT, int D, bool STAGED, bool MASK>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     rope_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps, const int32_t pair_heads)
 {
@@ -895,8 +972,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // 3. online softmax; P goes back into TMEM over S
-            softmax_tile<T, D, false>(acc_base, acc_base + kAttnKeys, qi, k0, shift, a, kt > 0,
-                                      m_ref, l_run);
+            softmax_tile<T, D, false, MASK>(acc_base, acc_base + kAttnKeys, qi, k0, shift, a, w.b,
+                                      kt > 0, m_ref, l_run);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
@@ -1056,7 +1133,7 @@ constexpr int kPpTmaWarp = kPpMmaWarp + kAttnBlocks;   // warp 10
 constexpr int kPpThreads = kMathThreads + 32 * (kAttnBlocks + 1);
 constexpr int kPpStages = 2;                       // key and value stages
 
-template <typename T, int LAYOUT, int D, bool STAGED_Q>
+template <typename T, int LAYOUT, int D, bool STAGED_Q, bool MASK>
 __global__ void __launch_bounds__(kPpThreads, 1)
     rope_attn_pp_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps,
                         const int32_t pair_heads)
@@ -1184,8 +1261,8 @@ __global__ void __launch_bounds__(kPpThreads, 1)
             if (!ok)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            softmax_tile<T, D, true>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
-                                     kt > 0, m_ref, l_run);
+            softmax_tile<T, D, true, MASK>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
+                                     w.b, kt > 0, m_ref, l_run);
             mbar_arrive(&bar_sm[j]);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1432,7 +1509,7 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <typename T, int LAYOUT, bool STAGED_Q>
+template <typename T, int LAYOUT, bool STAGED_Q, bool MASK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     rope_attn_2sm_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps,
                          const int32_t pair_heads)
@@ -1562,8 +1639,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                     o_ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
                     return o_ok;
                 };
-                softmax_tile<T, D, true>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
-                                         kt * kAttnKeys, shift, a, kt > 0, m_ref, l_run, o_ready);
+                softmax_tile<T, D, true, MASK>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
+                                         kt * kAttnKeys, shift, a, w.b, kt > 0, m_ref, l_run,
+                                         o_ready);
                 ok = o_ok;
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1942,7 +2020,7 @@ static cudaError_t launch_attn_2sm(const AttnArgs &a, const AttnMaps &maps, int 
     return cudaGetLastError();
 }
 
-template <typename T, int LAYOUT, int D>
+template <typename T, int LAYOUT, int D, bool MASK>
 static cudaError_t launch_attn_layout(const AttnArgs &a, const AttnMaps &maps, int pair_heads,
                                       cudaStream_t st)
 {
@@ -1950,57 +2028,40 @@ static cudaError_t launch_attn_layout(const AttnArgs &a, const AttnMaps &maps, i
     if constexpr (D == 128) {
         if (a.k_rot != nullptr) {
             if (a.pos_q == nullptr && a.rotary_dim % 64 == 0)
-                return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, true>>(a, maps, pair_heads,
+                return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, true, MASK>>(a, maps, pair_heads,
                                                                               st);
-            return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, false>>(a, maps, pair_heads, st);
+            return launch_attn_2sm<rope_attn_2sm_kernel<T, LAYOUT, false, MASK>>(a, maps, pair_heads, st);
         }
     } else {
         if (a.k_rot != nullptr) {
             if (pp_staged_q(a, pair_heads))
-                return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true>>(
+                return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, true, MASK>>(
                     kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
-            return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, false>>(
+            return launch_attn<rope_attn_pp_kernel<T, LAYOUT, D, false, MASK>>(
                 kPpThreads, attn_smem_bytes(D, true), a, maps, pair_heads, st);
         }
     }
     const size_t smem = attn_smem_bytes(D, false);
     if (a.pos_k == nullptr && a.rotary_dim % 64 == 0)
-        return launch_attn<rope_attn_kernel<T, LAYOUT, D, true>>(kAttnThreads, smem, a, maps,
+        return launch_attn<rope_attn_kernel<T, LAYOUT, D, true, MASK>>(kAttnThreads, smem, a, maps,
                                                                  pair_heads, st);
-    return launch_attn<rope_attn_kernel<T, LAYOUT, D, false>>(kAttnThreads, smem, a, maps,
+    return launch_attn<rope_attn_kernel<T, LAYOUT, D, false, MASK>>(kAttnThreads, smem, a, maps,
                                                               pair_heads, st);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool MASK>
 static cudaError_t launch_attn_d(const AttnArgs &a, const AttnMaps &maps, int32_t layout,
                                  int pair_heads, cudaStream_t st)
 {
-    return layout == 0 ? launch_attn_layout<T, 0, D>(a, maps, pair_heads, st)
-                       : launch_attn_layout<T, 1, D>(a, maps, pair_heads, st);
+    return layout == 0 ? launch_attn_layout<T, 0, D, MASK>(a, maps, pair_heads, st)
+                       : launch_attn_layout<T, 1, D, MASK>(a, maps, pair_heads, st);
 }
 
-// Probe of the expiry path: one thread waits, with the attention kernels'
-// bounded wait, on a barrier that nothing arrives at; after `cycles` clock
-// cycles the wait gives up and the thread records the expiry as those kernels
-// do (bit 1 of the device flag).  Nothing else runs, so nothing stalls.
-__global__ void rope_wait_probe_kernel(int32_t *flag, long long cycles)
-{
-    __shared__ __align__(8) uint64_t bar;
-    if (threadIdx.x == 0)
-        mbar_init(&bar, 1);
-    __syncthreads();
-    if (threadIdx.x == 0 && !attn_wait(&bar, 0u, nullptr, cycles))
-        atomicOr(flag, 2);
-}
-
-cudaError_t launch_wait_probe(int32_t *flag, long long cycles, cudaStream_t st)
-{
-    rope_wait_probe_kernel<<<1, 32, 0, st>>>(flag, cycles);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
-                             cudaStream_t st)
+// Tensor maps of the call, then the kernel for its shape, element type and
+// key path; MASK: the kernels that apply an attn_mask.
+template <bool MASK>
+cudaError_t launch_attention_t(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
+                               cudaStream_t st)
 {
     AttnMaps maps;
     memset(&maps, 0, sizeof maps);
@@ -2035,10 +2096,10 @@ cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32
             return cudaErrorInvalidValue;
     }
     if (dtype == 1)
-        return D == 64 ? launch_attn_d<__nv_bfloat16, 64>(a, maps, layout, pair_heads, st)
-                       : launch_attn_d<__nv_bfloat16, 128>(a, maps, layout, pair_heads, st);
-    return D == 64 ? launch_attn_d<__half, 64>(a, maps, layout, pair_heads, st)
-                   : launch_attn_d<__half, 128>(a, maps, layout, pair_heads, st);
+        return D == 64 ? launch_attn_d<__nv_bfloat16, 64, MASK>(a, maps, layout, pair_heads, st)
+                       : launch_attn_d<__nv_bfloat16, 128, MASK>(a, maps, layout, pair_heads, st);
+    return D == 64 ? launch_attn_d<__half, 64, MASK>(a, maps, layout, pair_heads, st)
+                   : launch_attn_d<__half, 128, MASK>(a, maps, layout, pair_heads, st);
 }
 
 }  // namespace rope

@@ -37,7 +37,9 @@ void *g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mutex;
 
 // Device address of g_key_scratch on the current device, looked up once per
-// device (with that device current) and then cached.
+// device (with that device current) and then cached.  The cache is never
+// invalidated: a process that resets a device must restart before calling
+// rope_attention_fwd_noalloc again.
 cudaError_t scratch_address(void **out)
 {
     int dev = 0;
@@ -60,17 +62,34 @@ cudaError_t scratch_address(void **out)
 
 }  // namespace
 
+namespace rope {
+// rope_attention_fwd's host checks (rope_api.cu), without a workspace.
+rope_status attention_args_status(const void *q, const void *k, const void *v, void *o,
+                                  const float *cos, const float *sin, const int32_t *pos_q,
+                                  const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk,
+                                  int64_t Sq, int64_t Sk, int32_t D, int32_t rotary_dim,
+                                  int32_t layout, int32_t causal, float softmax_scale,
+                                  int32_t dtype, int64_t table_rows);
+}  // namespace rope
+
 extern "C" rope_status rope_attention_fwd_noalloc(
     const void *q, const void *k, const void *v, void *o, const float *cos, const float *sin,
     const int32_t *pos_q, const int32_t *pos_k, int64_t B, int32_t Hq, int32_t Hk, int64_t Sq,
     int64_t Sk, int32_t D, int32_t rotary_dim, int32_t layout, int32_t causal,
     float softmax_scale, int32_t dtype, int64_t table_rows, void *stream)
 {
+    // the arguments first, as rope_attention_fwd checks them (an empty call
+    // is accepted there and needs nothing of the array)
+    const rope_status st =
+        rope::attention_args_status(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D,
+                                    rotary_dim, layout, causal, softmax_scale, dtype, table_rows);
+    if (st != ROPE_OK)
+        return st;
     // rot(K) needs B * Hk * Sk * D elements of 2 bytes; larger calls do not
-    // fit the array (checked before anything else touches the device)
+    // fit the array (checked before anything touches the device)
     int64_t n = 0, bytes = 0;
-    if (B < 0 || Hk < 0 || Sk < 0 || D < 0 || __builtin_mul_overflow(B, (int64_t)Hk, &n) ||
-        __builtin_mul_overflow(n, Sk, &n) || __builtin_mul_overflow(n, (int64_t)D * 2, &bytes))
+    if (__builtin_mul_overflow(B, (int64_t)Hk, &n) || __builtin_mul_overflow(n, Sk, &n) ||
+        __builtin_mul_overflow(n, (int64_t)D * 2, &bytes))
         return ROPE_ERR_INVALID_ARG;
     if (bytes > kKeyScratchBytes)
         return ROPE_ERR_UNSUPPORTED;

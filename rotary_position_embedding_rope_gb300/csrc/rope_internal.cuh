@@ -37,10 +37,9 @@ struct ApplyArgs {
 };
 
 // Kernel variants: kVector moves 16-byte vectors through registers (the
-// automatic choice for aligned shapes), kBulk stages rows through shared
-// memory with bulk copies (in place only, chosen only when forced), kScalar
-// handles any shape one pair at a time.
-enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
+// automatic choice for aligned shapes), kScalar handles any shape one pair at
+// a time.  The values are those rope_qk_kernel_variant reports.
+enum Variant : int32_t { kNone = 0, kScalar = 2, kVector = 3 };
 
 // Threads per CTA of the vectorised kernel and heads in flight per thread.
 #ifndef ROPE_VEC_THREADS
@@ -52,11 +51,6 @@ enum Variant : int32_t { kNone = 0, kBulk = 1, kScalar = 2, kVector = 3 };
 // Resident CTAs per SM the register allocation must allow (launch bounds).
 #ifndef ROPE_VEC_MIN_BLOCKS
 #define ROPE_VEC_MIN_BLOCKS 4
-#endif
-// Threads the register kernel aims to run at once; below that, a token's
-// heads are split into groups handled by separate thread rows.
-#ifndef ROPE_VEC_TARGET_THREADS
-#define ROPE_VEC_TARGET_THREADS (152 * 128)
 #endif
 // Launch the hot kernels with programmatic dependent launch.
 #ifndef ROPE_PDL
@@ -73,22 +67,34 @@ constexpr bool kVecPipeline = ROPE_VEC_PIPELINE != 0;
 #define ROPE_VEC_LOAD_MODE 2
 #endif
 constexpr int kVecLoadMode = ROPE_VEC_LOAD_MODE;
-constexpr int64_t kVecTargetThreads = ROPE_VEC_TARGET_THREADS;
+// Loads of rotary spans that are not whole 256-byte rows: 0 = ld.global.cs,
+// 1 = ld.global.cs.L2::64B.
+#ifndef ROPE_VEC_PART_HINT
+#define ROPE_VEC_PART_HINT 1
+#endif
+constexpr int kVecPartHint = ROPE_VEC_PART_HINT;
 constexpr bool kPdl = ROPE_PDL != 0;
-// Head rows of its first item each thread row prefetches into L2 before
-// waiting for the previous grid (0: none; default: the first batch of heads).
+// Head rows of its first units each thread row prefetches into L2 before
+// waiting for the previous grid (0: none; default: one batch of heads).
 #ifndef ROPE_VEC_PREFETCH_HEADS
 #define ROPE_VEC_PREFETCH_HEADS ROPE_VEC_UNROLL
 #endif
 constexpr int kVecPrefetchHeads = ROPE_VEC_PREFETCH_HEADS;
+// L2 prefetches of head rows: 1 = one bulk prefetch of the rotary span's exact
+// bytes per row (cp.async.bulk.prefetch.L2), 0 = prefetch.global.L2 of the
+// lines under each thread's two vectors.
+#ifndef ROPE_VEC_PREFETCH_BULK
+#define ROPE_VEC_PREFETCH_BULK 0
+#endif
+constexpr bool kVecPrefetchBulk = ROPE_VEC_PREFETCH_BULK != 0;
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
 constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;
 // NJ (16-byte vectors per half span) must fit in one CTA row: the register
-// and bulk kernels take rotary spans of up to 32 * kVecThreads bytes.
+// kernel takes rotary spans of up to 32 * kVecThreads bytes.
 constexpr int kMaxVectorsPerHalf = kVecThreads;
 
-// Attention with rotary Q/K (rope_attention.cu).
+// Attention with rotary Q/K (rope_attention.cuh).
 struct AttnArgs {
     const void *q, *k, *v;
     const void *k_rot;               // k rotated beforehand (rot(K), same layout), or nullptr
@@ -103,12 +109,31 @@ struct AttnArgs {
     float scale_log2;                // softmax scale * log2(e)
     int32_t causal;
     int32_t *flag;
+    const uint8_t *mask;             // attn_mask bytes (0 = hidden), or nullptr
+    int32_t mask_kind;               // 0: none, 1: [B, Sk], 2: [B, Sq, Sk]
+    int32_t mask_vec16;              // kind 2: rows 16-byte aligned (read as vectors)
 };
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
                              cudaStream_t st);
+// The same for calls with an attn_mask (rope_attention_masked.cu).
+cudaError_t launch_attention_masked(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
+                                    cudaStream_t st);
 // One bounded mbarrier wait that expires after `cycles` clock cycles and sets
 // bit 1 of *flag (rope_probe_wait_expiry).
 cudaError_t launch_wait_probe(int32_t *flag, long long cycles, cudaStream_t st);
+
+// Grid sizing of the register kernel (rope_tune_rotation_launch; 0 = the
+// default of each field).  ctas_per_sm caps the grid at that many CTAs per SM
+// (default: as many as are resident at once); min_units is the fewest
+// (token tile, head) units a lane group takes before the grid grows (default
+// 1); prefetch_next > 0 prefetches the first heads of a lane group's next tile
+// into L2 while it rotates the current one (default on; -1 turns it off).
+struct VecLaunchTuning {
+    int32_t ctas_per_sm;
+    int32_t min_units;
+    int32_t prefetch_next;
+};
+VecLaunchTuning vec_launch_tuning();
 
 // Per element type launchers (rope_apply_f32.cu, rope_apply_bf16.cu, rope_apply_f16.cu).
 cudaError_t launch_apply_f32(const ApplyArgs &a, int32_t layout, Variant v, cudaStream_t st);

@@ -34,6 +34,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "rope_internal.cuh"
 
 namespace rope {
@@ -180,8 +182,17 @@ cudaError_t launch_hot(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaSt
 // rotary_dim, neighbouring rows) the kernel never touches.
 __device__ __forceinline__ uint4 load_stream(const uint4 *p, bool whole = false)
 {
-    if (!whole)
-        return __ldcs(p);
+    if (!whole) {
+        if constexpr (kVecPartHint == 1) {
+            uint4 v;
+            asm volatile("ld.global.cs.L2::64B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "l"(p));
+            return v;
+        } else {
+            return __ldcs(p);
+        }
+    }
     if constexpr (kVecLoadMode == 1) {
         uint4 v;
         asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -310,79 +321,97 @@ __device__ __forceinline__ void copy_heads(const T *in0, T *out0, int64_t stride
 // ---------------------------------------------------------------------------
 // Register-staged vector kernel.
 //   blockDim = (NJ, TS): NJ = 16-byte vectors per half of the rotary span,
-//   TS = item rows per CTA.  An item is (token, head group): token t = b*S+s
-//   and the group's heads [g*HPG, min(P, (g+1)*HPG)) of the P = Hq + Hk
-//   heads.  With one group (the default for long head lists is several) a
-//   token's cos/sin values are loaded once and reused for all P heads; more
-//   groups shorten each thread's chain of dependent memory round trips.
-//   CTA c of G owns a balanced contiguous range of the items; its row y takes
-//   items i0 + y, i0 + y + TS, ...
+//   TS token rows, a whole number of lane groups.  A lane group is
+//   TT = max(1, 32 / NJ) consecutive rows: one warp when NJ <= 32 (TT tokens side by side), else
+//   one row of NJ threads.  It works on tiles of TT consecutive tokens of the
+//   flattened (batch, sequence) order, row r taking token tile * TT + r.
+//   The work is the list of units (tile, head), the P = Hq + Hk heads of a
+//   tile in order (Q heads, then K heads).  Lane group g of the grid takes a
+//   balanced contiguous run of units [u0, u1): every lane group does the same
+//   work to within one unit whatever the grid size, so the grid is sized to
+//   the CTAs that are resident at once and no partial last wave idles the
+//   GPU.  A run walks its tiles in order: for each, every row loads its
+//   token's cos/sin values once into registers and rotates the run's heads
+//   of that tile, the loads of the next kU heads issued before the current
+//   ones are rotated.  All rows of a lane group share the run, so their
+//   control flow is the same (except past the last token and for unrotated
+//   tokens).
 //   Split-half: vector j holds elements [jV, jV+V) and vector j+NJ holds
 //   their partners [rd/2 + jV, ...); cos/sin columns [jV, jV+V).
 //   Interleaved: vector j holds pairs [jV/2, jV/2 + V/2) and vector j+NJ
 //   holds pairs [(j+NJ)V/2, ...); the thread keeps both column ranges.
 // ---------------------------------------------------------------------------
+
+// Prefetch into L2 the row vectors of thread j of heads [hb, he) (unit head
+// indices: Q heads first, then K heads) of token (b, s).
+template <typename T>
+__device__ __forceinline__ void prefetch_heads(const ApplyArgs &p, int64_t b, int64_t s,
+                                               int32_t hb, int32_t he, int j, int NJ)
+{
+#pragma unroll
+    for (int ti = 0; ti < 2; ++ti) {
+        if (ti >= p.ntensors)
+            break;
+        const TensorRef t = p.t[ti];
+        const int32_t off = ti ? p.t[0].heads : 0;
+        const int32_t lo = (hb > off ? hb : off) - off;
+        const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
+        const T *in0 = static_cast<const T *>(t.base) + b * t.stride_b + s * t.stride_s;
+        for (int32_t hd = lo; hd < hi; ++hd) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(in0 + (int64_t)hd * t.stride_h);
+            if constexpr (kVecPrefetchBulk) {
+                // the rotary span exactly (2 NJ 16-byte vectors), one request
+                if (j == 0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                                 ::"l"(row), "r"((uint32_t)(32 * NJ)) : "memory");
+            } else {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j + NJ));
+            }
+        }
+    }
+}
+
 template <typename T, int LAYOUT, int U>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
-rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t heads_per_group,
-                int32_t TT)
+rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch_next)
 {
     constexpr int V = Elt<T>::V;
     const int NJ = blockDim.x;
-    const int TS = blockDim.y;
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
     const int32_t P = p.t[0].heads + (p.ntensors > 1 ? p.t[1].heads : 0);
     // rotary spans that are whole rows of a multiple of 256 bytes
     const bool whole = p.rotary_dim == p.D && (p.D * (int32_t)sizeof(T)) % 256 == 0;
-
     const int64_t total_tokens = p.B * p.S;
-    const int64_t G = gridDim.x;
-    const int64_t c = blockIdx.x;
-    const int64_t share = total_items / G;
-    const int64_t extra = total_items - share * G;
-    const int64_t i0 = c * share + (c < extra ? c : extra);
-    const int64_t i1 = i0 + share + (c < extra ? 1 : 0);
+
+    // this lane group's run of units
+    const int lgs = blockDim.y / TT;
+    const int lg = threadIdx.y / TT;
+    const int row = threadIdx.y - lg * TT;
+    const int64_t G = (int64_t)gridDim.x * lgs;
+    const int64_t g = (int64_t)blockIdx.x * lgs + lg;
+    const int64_t share = n_units / G;
+    const int64_t extra = n_units - share * G;
+    const int64_t u0 = g * share + (g < extra ? g : extra);
+    const int64_t u1 = u0 + share + (g < extra ? 1 : 0);
 
     if constexpr (kVecPrefetchHeads > 0) {
-        // Before waiting for the previous grid: pull this row's first item's
-        // head rows into L2.  A prefetch only fills L2, the coherence point
-        // that the previous grid's writes also reach, so it cannot make a
-        // later load see stale data; it overlaps DRAM latency with the
+        // Before waiting for the previous grid: pull the first head rows of
+        // this row's run into L2.  A prefetch only fills L2, the coherence
+        // point that the previous grid's writes also reach, so it cannot make
+        // a later load see stale data; it overlaps DRAM latency with the
         // previous launch's tail.
-        const int64_t item = i0 + threadIdx.y;
-        if (item < i1) {
-            int64_t tok = item;
-            int32_t g = 0;
-            if (groups > 1) {
-                const int64_t per_tile = (int64_t)groups * TT;
-                const int64_t tile = item / per_tile;
-                const int64_t rem = item - tile * per_tile;
-                g = static_cast<int32_t>(rem / TT);
-                tok = tile * TT + (rem - (int64_t)g * TT);
-            }
+        if (u0 < u1) {
+            const int64_t tile = u0 / P;
+            const int32_t hb = (int32_t)(u0 - tile * P);
+            int64_t he = hb + kVecPrefetchHeads;
+            he = he < P ? he : P;
+            he = he < hb + (u1 - u0) ? he : hb + (u1 - u0);
+            const int64_t tok = tile * TT + row;
             if (tok < total_tokens) {
                 const int64_t b = tok / p.S;
-                const int64_t s = tok - b * p.S;
-                const int32_t hb = g * heads_per_group;
-                int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
-                if (he > hb + kVecPrefetchHeads)
-                    he = hb + kVecPrefetchHeads;
-#pragma unroll
-                for (int ti = 0; ti < 2; ++ti) {
-                    if (ti >= p.ntensors)
-                        break;
-                    const TensorRef t = p.t[ti];
-                    const int32_t off = ti ? p.t[0].heads : 0;
-                    const int32_t lo = (hb > off ? hb : off) - off;
-                    const int32_t hi = (he < off + t.heads ? he : off + t.heads) - off;
-                    const T *in0 = static_cast<const T *>(t.base) + b * t.stride_b + s * t.stride_s;
-                    for (int32_t hd = lo; hd < hi; ++hd) {
-                        const uint4 *row = reinterpret_cast<const uint4 *>(in0 + (int64_t)hd * t.stride_h);
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j));
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + j + NJ));
-                    }
-                }
+                prefetch_heads<T>(p, b, tok - b * p.S, hb, (int32_t)he, j, NJ);
             }
         }
     }
@@ -390,25 +419,26 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
     pdl_wait();
     pdl_trigger();
 
-    for (int64_t item = i0 + threadIdx.y; item < i1; item += TS) {
-        // items run (tile of TT tokens, group, token in tile), so the rows of a
-        // warp hold consecutive tokens of one head group
-        int64_t tok = item;
-        int32_t g = 0;
-        if (groups > 1) {
-            const int64_t per_tile = (int64_t)groups * TT;
-            const int64_t tile = item / per_tile;
-            const int64_t rem = item - tile * per_tile;
-            g = static_cast<int32_t>(rem / TT);
-            tok = tile * TT + (rem - (int64_t)g * TT);
-        }
+    // the run, tile by tile (the launcher keeps every run below 2^30 units)
+    const int64_t tile0 = u0 / P;
+    int32_t hb = (int32_t)(u0 - tile0 * P);
+    int64_t tok = tile0 * TT + row;
+    for (int32_t left = (int32_t)(u1 - u0); left > 0; tok += TT, hb = 0) {
+        const int32_t he = P - hb < left ? P : hb + left;
+        left -= he - hb;
         if (tok >= total_tokens)
             continue;
         const int64_t b = tok / p.S;
         const int64_t s = tok - b * p.S;
 
-        const int32_t hb = g * heads_per_group;
-        const int32_t he = hb + heads_per_group < P ? hb + heads_per_group : P;
+        // the next tile of the run: its first heads into L2 now, so its
+        // first loads do not start the pipeline from DRAM latency
+        if (prefetch_next > 0 && left > 0 && tok + TT < total_tokens) {
+            const int64_t nt = tok + TT;
+            const int64_t nb = nt / p.S;
+            const int32_t nhe = (int32_t)(U < left ? U : left);
+            prefetch_heads<T>(p, nb, nt - nb * p.S, 0, nhe < P ? nhe : P, j, NJ);
+        }
 
         // position of this token: table row, -1 = leave unrotated
         int64_t r = s;
@@ -416,7 +446,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
         if (p.pos_idx != nullptr) {
             r = __ldg(p.pos_idx + b * p.pos_stride_b + s);
             if (r != -1 && (r < 0 || r >= p.table_rows)) {
-                if (j == 0 && g == 0)
+                if (j == 0)
                     atomicOr(p.range_flag, 1);
                 rotate = false;
             }
@@ -444,7 +474,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t total_items, int32_t groups, int32_t 
             continue;
         }
 
-        // this thread's cos/sin values, kept in registers for the group's heads
+        // this thread's cos/sin values, kept in registers for the tile's heads
         float c[V], sn[V];
         const float *crow = p.cos + r * h;
         const float *srow = p.sin + r * h;
@@ -570,6 +600,44 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
 }
 
 // ---------------------------------------------------------------------------
+// SM count and resident CTAs per SM of a kernel on the current device, looked
+// up once per device and pair layout and then cached.  The cache has internal
+// linkage: each translation unit (one element type) keeps its own, and two
+// copies of the library in one process never share one.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kCacheDevices = 64;
+std::atomic<int> g_cache_sms[kCacheDevices];
+std::atomic<int> g_cache_occ[2][kCacheDevices];
+
+cudaError_t resident_ctas(const void *kernel, int32_t layout, int *sms, int *per_sm)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kCacheDevices)
+        return cudaErrorInvalidDevice;
+    const int li = layout ? 1 : 0;
+    int n = g_cache_sms[dev].load(std::memory_order_relaxed);
+    int o = g_cache_occ[li][dev].load(std::memory_order_relaxed);
+    if (n <= 0 || o <= 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kVecThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        g_cache_sms[dev].store(n, std::memory_order_relaxed);
+        g_cache_occ[li][dev].store(o, std::memory_order_relaxed);
+    }
+    *sms = n;
+    *per_sm = o;
+    return cudaSuccess;
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // Host-side launcher for one element type.
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -578,27 +646,46 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
     if (v == kVector) {
         constexpr int V = Elt<T>::V;
         const int NJ = (a.rotary_dim / 2) / V;                 // vectors per half span
-        const int TS = NJ >= kVecThreads ? 1 : kVecThreads / NJ;
+        const int TT = NJ >= 32 ? 1 : 32 / NJ;                 // tokens per lane group
+        const int lgs = NJ >= kVecThreads ? 1 : (kVecThreads / NJ) / TT;   // lane groups per CTA
+        const int TS = lgs * TT;                               // token rows per CTA
         const int32_t P = a.t[0].heads + (a.ntensors > 1 ? a.t[1].heads : 0);
-        // Split the heads into groups only when one thread row per token
-        // leaves the GPU short of threads (small batches, few tokens, narrow
-        // rotary spans); at most one group per kVecUnroll heads.
-        const int64_t rows_threads = a.B * a.S * NJ;
-        int64_t want = rows_threads > 0 ? (kVecTargetThreads + rows_threads - 1) / rows_threads : 1;
-        const int32_t max_groups = (P + kVecUnroll - 1) / kVecUnroll;
-        const int32_t groups = (int32_t)(want < 1 ? 1 : (want > max_groups ? max_groups : want));
-        const int32_t hpg = (P + groups - 1) / groups;
-        // tokens per warp row group: a warp covers TT consecutive tokens
-        const int32_t TT = NJ >= 32 ? 1 : 32 / NJ;
         const int64_t tiles = (a.B * a.S + TT - 1) / TT;
-        const int64_t items = groups == 1 ? a.B * a.S : tiles * TT * groups;
-        int64_t grid = (items + TS - 1) / TS;                  // one item per thread row
-        if (grid > 0x7fffffffLL)
-            grid = 0x7fffffffLL;
+        const int64_t units = tiles * P;
         auto kernel = layout == 0 ? rope_vec_kernel<T, 0, kVecUnroll>
                                   : rope_vec_kernel<T, 1, kVecUnroll>;
-        return launch_hot(kernel, dim3((unsigned)grid), dim3(NJ, TS), 0, st, a, items, groups, hpg,
-                          TT);
+        // The grid.  Calls with at least one tile per lane group that can be
+        // resident at once take one tile (all P heads of TT tokens) per lane
+        // group, as many CTAs as that makes: the hardware hands the CTAs out
+        // as resident ones finish, which balances the load better than a
+        // fixed persistent split (measured).  Smaller calls cut their units
+        // into as many balanced runs as there are resident lane groups (at
+        // least one unit each), so a few tokens still occupy every SM.  The
+        // tuning entry point can force the cap and the run length instead.
+        const VecLaunchTuning tune = vec_launch_tuning();
+        int sms = 0, per_sm = 0;
+        cudaError_t e = resident_ctas(reinterpret_cast<const void *>(kernel), layout, &sms, &per_sm);
+        if (e != cudaSuccess)
+            return e;
+        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        const bool big = tiles >= resident * lgs;
+        int64_t runs;
+        if (tune.min_units > 0)
+            runs = (units + tune.min_units - 1) / tune.min_units;
+        else
+            runs = big ? tiles : (units < resident * lgs ? units : resident * lgs);
+        int64_t grid = (runs + lgs - 1) / lgs;
+        const int64_t cap = tune.ctas_per_sm > 0 ? (int64_t)sms * tune.ctas_per_sm
+                                                 : (big ? grid : resident);
+        if (grid > cap)
+            grid = cap;
+        const int64_t min_grid = units / ((int64_t)lgs << 30) + 1;   // runs below 2^30 units
+        if (grid < min_grid)
+            grid = min_grid;
+        if (grid > 0x7fffffffLL)
+            grid = 0x7fffffffLL;
+        return launch_hot(kernel, dim3((unsigned)grid), dim3(NJ, TS), 0, st, a, units, TT,
+                          tune.prefetch_next >= 0 ? 1 : 0);
     }
     const int64_t rows0 = a.B * a.S * a.t[0].heads;
     const int64_t rows1 = a.ntensors > 1 ? a.B * a.S * a.t[1].heads : 0;

@@ -16,6 +16,15 @@ import torch
 from . import _DTYPE_CODE, _LAYOUT_CODE, _shape4, rope_apply_qk_out, rope_attention_fwd
 
 
+def _on_streams(t: torch.Tensor, streams) -> torch.Tensor:
+    """Mark a staging tensor as used on the pipeline's streams, so that the
+    caching allocator does not reuse its memory, once it is dropped, before
+    the work queued there by then has finished."""
+    for s in streams:
+        t.record_stream(s)
+    return t
+
+
 def _head_groups(B: int, heads: tuple, chunks: int) -> int:
     """Groups per batch entry when a call is cut into more pieces than batch
     entries: the largest power of two with B * groups <= chunks that divides
@@ -47,7 +56,11 @@ class HostRotator:
         key = (tuple(q.shape), None if k is None else tuple(k.shape), q.dtype, dims_q, dims_k)
         if key != self._key:
             def dev(dims):
-                return torch.empty(dims, dtype=q.dtype, device=self.device)
+                return _on_streams(torch.empty(dims, dtype=q.dtype, device=self.device),
+                                   (self.s_in, self.s_run, self.s_out))
+            # the old slots may still be in use by copies and calls queued on
+            # the three streams: recorded on them at creation, their memory is
+            # not handed out again before that work is done
             self._slots = [(dev(dims_q), None if k is None else dev(dims_k)) for _ in range(2)]
             self._key = key
             self._free = [None, None]
@@ -160,8 +173,9 @@ class HostAttention:
         key = (tuple(q.shape), tuple(k.shape), q.dtype, nb, nkv)
         if key != self._key:
             def dev(t, heads):
-                return torch.empty((nb, heads) + tuple(t.shape[2:]), dtype=t.dtype,
-                                   device=self.device)
+                return _on_streams(torch.empty((nb, heads) + tuple(t.shape[2:]), dtype=t.dtype,
+                                               device=self.device),
+                                   (self.s_in, self.s_run, self.s_out))
             self._slots = [(dev(q, nkv * grp), dev(k, nkv), dev(k, nkv), dev(q, nkv * grp))
                            for _ in range(2)]
             # the calls all run on s_run, one after another: one workspace serves them

@@ -188,9 +188,9 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 def test_force_kernel_variant_rules(lib):
     try:
-        assert lib.rope_force_kernel_variant(4) == R.ROPE_ERR_INVALID_ARG
-        assert lib.rope_force_kernel_variant(-1) == R.ROPE_ERR_INVALID_ARG
-        for forced, aligned_want, unaligned_want in ((0, 3, 2), (1, 1, 0), (2, 2, 2), (3, 3, 0)):
+        for bad in (4, -1, 1):
+            assert lib.rope_force_kernel_variant(bad) == R.ROPE_ERR_INVALID_ARG
+        for forced, aligned_want, unaligned_want in ((0, 3, 2), (2, 2, 2), (3, 3, 0)):
             assert lib.rope_force_kernel_variant(forced) == R.ROPE_OK
             assert lib.rope_qk_kernel_variant(*qk_args()) == aligned_want
             assert lib.rope_qk_kernel_variant(*qk_args(q=A16 + 2)) == unaligned_want
@@ -228,12 +228,16 @@ def test_apply_out_rejects_bad_arguments(lib, over, status):
     assert lib.rope_apply_qk_out(*out_args(**over)) == status
 
 
-def test_bulk_kernel_refuses_out_of_place(lib):
+def test_tune_rotation_launch_rules(lib):
     try:
-        lib.rope_force_kernel_variant(1)
-        assert lib.rope_apply_qk_out(*out_args()) == R.ROPE_ERR_UNSUPPORTED
+        for bad in ((-1, 0, 0), (65, 0, 0), (0, -1, 0), (0, 0, 2), (0, 0, -2)):
+            assert lib.rope_tune_rotation_launch(*bad) == R.ROPE_ERR_INVALID_ARG
+        for good in ((0, 0, 0), (1, 1, -1), (64, 1000, 1), (3, 4, 0)):
+            assert lib.rope_tune_rotation_launch(*good) == R.ROPE_OK
+            # the kernel choice does not depend on the grid sizing
+            assert lib.rope_qk_kernel_variant(*qk_args()) == 3
     finally:
-        lib.rope_force_kernel_variant(0)
+        lib.rope_tune_rotation_launch(0, 0, 0)
 
 
 def test_apply_out_empty_is_noop(lib):
@@ -285,3 +289,31 @@ def test_attention_empty_is_noop(lib):
 def test_wait_probe_rejects_cycles_out_of_range(lib, cycles):
     # checked before any CUDA call: nothing is launched
     assert lib.rope_probe_wait_expiry(cycles, None) == R.ROPE_ERR_INVALID_ARG
+
+
+def masked_args(mask=A16 * 700, kind=1, **over):
+    a = list(attn_args(**over))
+    # rope_attention_fwd's arguments with (attn_mask, mask_kind) before the workspace
+    return tuple(a[:20] + [mask, kind] + a[20:])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=3), R.ROPE_ERR_UNSUPPORTED),                       # mask kind outside the enum
+    (dict(kind=-1), R.ROPE_ERR_UNSUPPORTED),
+    (dict(mask=None, kind=1), R.ROPE_ERR_INVALID_ARG),            # a mask kind needs a mask
+    (dict(mask=None, kind=2), R.ROPE_ERR_INVALID_ARG),
+    (dict(mask=A16 * 300 + 16, kind=1), R.ROPE_ERR_INVALID_ARG),   # mask inside o
+    (dict(mask=A16 * 300 - 64 * 64 + 16, kind=2), R.ROPE_ERR_INVALID_ARG),   # [B,Sq,Sk] reaches o
+    (dict(mask=A16 * 800, kind=1, ws=A16 * 800 - 16 * 1024, ws_bytes=1 << 20), R.ROPE_ERR_INVALID_ARG),
+    (dict(dtype=0), R.ROPE_ERR_UNSUPPORTED),                      # the plain call's rules apply
+    (dict(Hq=3), R.ROPE_ERR_INVALID_ARG),
+])
+def test_masked_attention_rejects_bad_arguments(lib, kw, status):
+    assert lib.rope_attention_fwd_masked(*masked_args(**kw)) == status
+
+
+def test_masked_attention_empty_and_no_mask(lib):
+    assert lib.rope_attention_fwd_masked(*masked_args(Sq=0, q=None, o=None)) == R.ROPE_OK
+    # kind 0 ignores the pointer: the same checks as rope_attention_fwd
+    assert lib.rope_attention_fwd_masked(*masked_args(mask=None, kind=0, dtype=0)) == \
+        lib.rope_attention_fwd(*attn_args(dtype=0))

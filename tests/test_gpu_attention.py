@@ -3,23 +3,23 @@ the fp64 rotary-attention oracle, on both key paths: keys rotated inside the
 attention kernel (no workspace) and keys rotated once into a workspace by the
 rotation kernel.  The two paths give the same bits.
 
-Tolerance: the kernel rounds P to the element type before the P.V product and
-rounds O once; each is within half a unit in the last place, so per element
-|o - o_ref| <= u * (max|v| + |o_ref|) with u = 2^-8 (bf16) or 2^-10 (fp16),
-a bound twice the two roundings' sum.  Everything else (fp32 accumulation,
-exp2) is far below it.
+Tolerance (attention_check.py): the kernel rounds P to the element type
+before the P.V product and rounds O once, so per output element
+|o - O| <= (u + 2^-14)(W + |O|) (+ 2^-25 A for fp16's subnormal P), with
+u = 2^-8 (bf16) or 2^-11 (fp16) and W = sum_j p_j |v_j| / l,
+A = sum_j vis_j |v_j| / l from the oracle.
 """
 import numpy as np
 import pytest
 import torch
 
+import attention_check as AC
 import oracle as O
 import workloads as W
 from gpu_util import lib, oracle_tables, require_gpu
 from oracle import attention as OA
 
 pytestmark = pytest.mark.gpu
-U = {"bf16": 2.0 ** -8, "f16": 2.0 ** -10}
 CODE = {"bf16": O.BF16, "f16": O.F16}
 
 
@@ -31,16 +31,10 @@ def _inputs(B, Hq, Hk, Sq, Sk, D, dtype, seed):
     return q, k, v
 
 
-def _check(got, q, k, v, dtype, rd, layout, c32, s32, pq, pk, causal, what=""):
-    ref = OA.attention(W.bits(q), W.bits(k), W.bits(v), CODE[dtype], rd, layout, c32, s32,
-                       pq, pk, causal)
-    g = got.float().cpu().numpy().astype(np.float64)
-    vmax = float(v.float().abs().max()) if v.numel() else 0.0
-    tol = U[dtype] * (vmax + np.abs(ref))
-    err = np.abs(g - ref)
-    assert np.all(np.isfinite(g)), what
-    assert np.all(err <= tol), "%s: %d of %d beyond tolerance, max err %.3g" % (
-        what, np.count_nonzero(err > tol), err.size, err.max())
+def _check(got, q, k, v, dtype, rd, layout, c32, s32, pq, pk, causal, what="", attn_mask=None):
+    ref, w, a = OA.attention(W.bits(q), W.bits(k), W.bits(v), CODE[dtype], rd, layout, c32, s32,
+                             pq, pk, causal, want_bounds=True, attn_mask=attn_mask)
+    return AC.check(got.float().cpu().numpy(), ref, w, a, dtype, what)
 
 
 CASES = [
@@ -67,9 +61,14 @@ CASES = [
 WS = {"ws": "auto", "inkernel": None}     # key workspace, or keys rotated in the kernel
 
 
+def _cid(c):
+    return "B%d_Hq%d_Hk%d_Sq%d_Sk%d_D%d_rd%d_%s_%s_c%d" % (
+        c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["rd"], c["dtype"], c["layout"],
+        c["causal"])
+
+
 @pytest.mark.parametrize("ws", sorted(WS))
-@pytest.mark.parametrize("c", CASES, ids=lambda c: "Sq%d_Sk%d_D%d_rd%d_%s_%s_c%d" % (
-    c["Sq"], c["Sk"], c["D"], c["rd"], c["dtype"], c["layout"], c["causal"]))
+@pytest.mark.parametrize("c", CASES, ids=_cid)
 def test_attention_against_oracle(c, ws):
     require_gpu()
     R = lib()
@@ -81,7 +80,7 @@ def test_attention_against_oracle(c, ws):
                     causal=c["causal"], k_workspace=WS[ws])
     assert R.rope_check_errors() == R.ROPE_OK
     _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, None, None,
-           c["causal"], str(c))
+           c["causal"], "case %s %s" % (_cid(c), ws))
 
 
 @pytest.mark.parametrize("ws", sorted(WS))
@@ -181,7 +180,7 @@ def test_attention_fuzz(c):
     assert R.rope_check_errors() == R.ROPE_OK
     assert torch.equal(o.view(torch.int16), o_in.view(torch.int16)), "key paths differ"
     _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, pq, pk, c["causal"],
-           str(c))
+           "fuzz%02d" % c["i"])
 
 
 def test_attention_full_size_sampled_rows():
@@ -205,14 +204,53 @@ def test_attention_full_size_sampled_rows():
     group = Hq // Hk
     for b, h, i in rows:
         kv = h // group
-        ref = OA.attention(W.bits(q[b:b + 1, h:h + 1, i:i + 1]), W.bits(k[b:b + 1, kv:kv + 1, :i + 1]),
-                           W.bits(v[b:b + 1, kv:kv + 1, :i + 1]), O.BF16, rd, O.SPLIT_HALF, c32, s32,
-                           np.array([i], dtype=np.int32), None, True)
-        got = o[b:b + 1, h:h + 1, i:i + 1].float().numpy().astype(np.float64)
-        vmax = float(v[b, kv, :i + 1].float().abs().max())
-        tol = U["bf16"] * (vmax + np.abs(ref))
-        assert np.all(np.abs(got - ref) <= tol), "row (%d, %d, %d): max err %.3g" % (
-            b, h, i, np.abs(got - ref).max())
+        ref, w, a = OA.attention(W.bits(q[b:b + 1, h:h + 1, i:i + 1]),
+                                 W.bits(k[b:b + 1, kv:kv + 1, :i + 1]),
+                                 W.bits(v[b:b + 1, kv:kv + 1, :i + 1]), O.BF16, rd, O.SPLIT_HALF,
+                                 c32, s32, np.array([i], dtype=np.int32), None, True,
+                                 want_bounds=True)
+        AC.check(o[b:b + 1, h:h + 1, i:i + 1].float().numpy(), ref, w, a, "bf16",
+                 "full size sampled rows: row (%d, %d, %d)" % (b, h, i))
+
+
+def tile_indicator_values(Sk, D):
+    """v[j, d] = 1 when (j // 128) % D == d: output column d of a row is the
+    softmax mass of the key tiles d, d + D, ... alone."""
+    v = torch.zeros((Sk, D), dtype=torch.bfloat16)
+    v[torch.arange(Sk), (torch.arange(Sk) // 128) % D] = 1.0
+    return v
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
+def test_attention_full_length_tile_indicator_values(ws):
+    """The Llama-shaped causal prefill at full length (Sq = Sk = 4096, GQA
+    32/8, D = 128, bf16) with values that mark their key tile: each output
+    column carries one key tile's softmax mass, so a skipped, repeated or
+    misplaced key tile moves whole columns far outside the bound (the CPU
+    test of attention_check shows the rule rejecting a skipped tile and a zero
+    output on these rows).  Sampled query rows against the oracle, on both
+    key paths."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, S, D, rd = 1, 32, 8, 4096, 128, 128
+    g = torch.Generator().manual_seed(6)
+    q = W.draw((B, Hq, S, D), "bf16", g)
+    k = W.draw((B, Hk, S, D), "bf16", g)
+    v = tile_indicator_values(S, D)[None, None].expand(B, Hk, S, D).contiguous()
+    c32, s32 = oracle_tables(5e5, rd, S)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, causal=True, k_workspace=WS[ws]).cpu()
+    assert R.rope_check_errors() == R.ROPE_OK
+    rng = np.random.default_rng(13)
+    rows = [(0, 0), (31, 4095), (5, 127), (17, 128), (30, 2047), (2, 4000), (9, 255), (12, 3071)]
+    rows += [(int(rng.integers(Hq)), int(rng.integers(S))) for _ in range(16)]
+    for h, i in rows:
+        kv = h // (Hq // Hk)
+        ref, w, a = OA.attention(W.bits(q[:, h:h + 1, i:i + 1]), W.bits(k[:, kv:kv + 1, :i + 1]),
+                                 W.bits(v[:, kv:kv + 1, :i + 1]), O.BF16, rd, O.SPLIT_HALF, c32,
+                                 s32, np.array([i], dtype=np.int32), None, True, want_bounds=True)
+        AC.check(o[:, h:h + 1, i:i + 1].float().numpy(), ref, w, a, "bf16",
+                 "tile indicator values (%s): head %d row %d" % (ws, h, i))
 
 
 @pytest.mark.parametrize("chunks", [1, 2, 3, 6])
@@ -236,3 +274,117 @@ def test_host_attention_pipeline_matches_device_call(chunks):
         assert R.rope_check_errors() == R.ROPE_OK
         assert torch.equal(ho, want.cpu())
     assert torch.equal(hq, q) and torch.equal(hk, k) and torch.equal(hv, v)
+
+
+MASK_CASES = [
+    dict(B=3, Hq=4, Hk=2, Sq=300, Sk=300, D=128, rd=128, dtype="bf16", layout="split_half", causal=True),
+    dict(B=3, Hq=4, Hk=2, Sq=200, Sk=333, D=128, rd=64, dtype="f16", layout="interleaved", causal=False),
+    dict(B=3, Hq=6, Hk=2, Sq=260, Sk=260, D=64, rd=32, dtype="bf16", layout="split_half", causal=True),
+    dict(B=3, Hq=3, Hk=1, Sq=129, Sk=400, D=64, rd=64, dtype="f16", layout="split_half", causal=False),
+]
+
+
+def _key_mask(B, Sk, seed):
+    """Per batch entry: all keys, a padded tail, a hidden whole key tile plus
+    scattered keys."""
+    m = np.ones((B, Sk), dtype=bool)
+    if B > 1:
+        m[1, Sk - 77:] = False
+    if B > 2:
+        m[2, 10:140] = False
+        m[2, np.random.default_rng(seed).integers(0, Sk, Sk // 5)] = False
+    return m
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
+@pytest.mark.parametrize("c", MASK_CASES, ids=_cid)
+def test_attention_key_padding_mask(c, ws):
+    """attn_mask [B, Sk] ("rotary-embedding-torch", Input Tensor Shapes):
+    padded batches, a whole key tile hidden, scattered keys; with and without
+    the causal mask, on both key paths."""
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], 51)
+    m = _key_mask(c["B"], c["Sk"], 5)
+    rows = max(c["Sq"], c["Sk"]) + 8
+    c32, s32 = oracle_tables(1e4, c["rd"], rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, rotary_dim=c["rd"], layout=c["layout"],
+                    causal=c["causal"], k_workspace=WS[ws], attn_mask=torch.from_numpy(m).cuda())
+    assert R.rope_check_errors() == R.ROPE_OK
+    _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, None, None,
+           c["causal"], "key mask %s %s" % (_cid(c), ws), attn_mask=m)
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
+@pytest.mark.parametrize("Sk", [320, 333])
+def test_attention_per_query_mask(Sk, ws):
+    """attn_mask [B, Sq, Sk]: random visibility, one query row with every key
+    hidden (zeros), one batch entry all visible; rows read as 16-byte vectors
+    (Sk = 320) or byte by byte (Sk = 333)."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, Sq, D, rd = 2, 4, 2, 200, 128, 128
+    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, "bf16", 52)
+    g = np.random.default_rng(9)
+    m = g.random((B, Sq, Sk)) < 0.7
+    m[0, 17] = False
+    m[1] = True
+    c32, s32 = oracle_tables(1e4, rd, Sk + 8)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    for causal in (False, True):
+        o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, causal=causal, k_workspace=WS[ws],
+                        attn_mask=torch.from_numpy(m).cuda())
+        assert R.rope_check_errors() == R.ROPE_OK
+        _check(o, q, k, v, "bf16", rd, O.SPLIT_HALF, c32, s32, None, None, causal,
+               "query mask Sk%d %s" % (Sk, ws), attn_mask=m)
+        if not causal:
+            assert torch.count_nonzero(o[0, :, 17]) == 0
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
+def test_attention_mask_causal_pattern_equals_causal(ws):
+    """A [B, Sq, Sk] mask shaped like the causal pattern gives the causal
+    call's bits: the hidden keys contribute exact zeros (p = 2^-inf) to the
+    sums and products the causal call skips; an all-False mask gives zeros."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, Sq, Sk, D = 1, 4, 2, 250, 390, 128
+    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, "bf16", 53)
+    c32, s32 = oracle_tables(1e4, 128, Sk + 8)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    pat = torch.arange(Sk)[None, :] <= (torch.arange(Sq)[:, None] + (Sk - Sq))
+    a = R.attention(qg, kg, vg, cg, sg, causal=True, k_workspace=WS[ws])
+    b = R.attention(qg, kg, vg, cg, sg, causal=False, k_workspace=WS[ws],
+                    attn_mask=pat[None].expand(B, Sq, Sk).contiguous().cuda())
+    z = R.attention(qg, kg, vg, cg, sg, causal=True, k_workspace=WS[ws],
+                    attn_mask=torch.zeros((B, Sk), dtype=torch.bool, device="cuda"))
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.count_nonzero(z) == 0
+
+
+def test_host_attention_shape_change_without_sync():
+    """HostAttention calls with different shapes back to back, no wait
+    between them: each equals the device call bit for bit (the staging and
+    workspace buffers of a replaced shape are not reused while queued work
+    still reads or writes them)."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostAttention
+
+    hat = HostAttention(chunks=2)
+    cos, sin = R.build_tables(10000.0, 128, 512)
+    outs = []
+    for i, (B, S) in enumerate(((2, 400), (3, 130), (2, 400))):
+        q, k, v = _inputs(B, 4, 2, S, S, 128, "bf16", seed=60 + i)
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        outs.append((q, k, v, ho, hat.forward(hq, hk, hv, ho, cos, sin, causal=True)))
+    for q, k, v, ho, done in outs:
+        done.synchronize()
+        want = R.attention(q.cuda(), k.cuda(), v.cuda(), cos, sin, causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(ho, want.cpu())
+    assert R.rope_check_errors() == R.ROPE_OK

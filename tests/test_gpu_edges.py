@@ -314,8 +314,8 @@ def restore_variant():
 ])
 @pytest.mark.parametrize("positions", ["none", "masked", "out_of_range"])
 def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
-    """Bulk-staged, register-vector and element-wise kernels give the same bits,
-    and touch nothing outside the rotated spans."""
+    """Register-vector and element-wise kernels give the same bits, and touch
+    nothing outside the rotated spans."""
     require_gpu()
     R = lib()
     rows = cfg["S"] + 8
@@ -332,7 +332,7 @@ def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
             pos[w.S - 1] = rows + 5
     pos_g = None if pos is None else pos_tensor(pos)
     results = {}
-    for v in (1, 3, 2):
+    for v in (3, 2):
         R.rope_force_kernel_variant(v)
         for backward in (False, True):
             qg = Guarded(q)
@@ -345,15 +345,14 @@ def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
             assert qg.intact() and (kg is None or kg.intact())
             results[(v, backward)] = (gpu_bits(qg.t), None if kg is None else gpu_bits(kg.t))
     for backward in (False, True):
-        for v in (3, 2):
-            a, b = results[(1, backward)], results[(v, backward)]
-            assert np.array_equal(a[0], b[0]), (v, backward)
-            if a[1] is not None:
-                assert np.array_equal(a[1], b[1]), (v, backward)
-    # and the bulk result against the oracle on the rows the oracle accepts
+        a, b = results[(3, backward)], results[(2, backward)]
+        assert np.array_equal(a[0], b[0]), backward
+        if a[1] is not None:
+            assert np.array_equal(a[1], b[1]), backward
+    # and the vector result against the oracle on the rows the oracle accepts
     good = np.ones(w.S, bool) if pos is None else (pos >= 0) & (pos < rows)
     sa = 1 if w.seq_before_head else 2
-    for x, H, got in ((q, w.Hq, results[(1, False)][0]), (k, w.Hk, results[(1, False)][1])):
+    for x, H, got in ((q, w.Hq, results[(3, False)][0]), (k, w.Hk, results[(3, False)][1])):
         if x is None or H == 0:
             continue
         idx = np.flatnonzero(good)
@@ -363,6 +362,65 @@ def test_all_kernel_variants_bit_identical(cfg, positions, restore_variant):
         assert_matches(w.dtype, np.ascontiguousarray(np.take(got, idx, axis=sa)), yb, y64)
         bad = np.flatnonzero(~good)
         assert np.array_equal(np.take(got, bad, axis=sa), np.take(W.bits(x), bad, axis=sa))
+
+
+@pytest.fixture
+def restore_tuning():
+    yield
+    lib().rope_tune_rotation_launch(0, 0, 0)
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(B=3, Hq=5, Hk=3, S=70, D=128, rd=128, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=2, Hq=4, Hk=2, S=45, D=128, rd=128, dtype="f16", layout="interleaved", sbh=True),
+    dict(B=5, Hq=6, Hk=6, S=301, D=64, rd=32, dtype="bf16", layout="split_half", sbh=False),
+    dict(B=1, Hq=3, Hk=1, S=33, D=64, rd=64, dtype="f32", layout="interleaved", sbh=False),
+])
+@pytest.mark.parametrize("tuning", [(1, 1, 0), (1, 7, -1), (2, 1000, 0), (0, 3, -1), (64, 1, 0)],
+                         ids=lambda t: "ctas%d_units%d_pf%d" % t)
+def test_vector_grid_sizing_does_not_change_results(cfg, tuning, restore_tuning):
+    """The vector kernel splits its (token tile, head) units into balanced
+    runs, one per lane group; a run may start and end inside a tile and cross
+    several tiles (and batch entries).  However the grid is sized -- one CTA
+    per SM, runs of 7 or 1000 units, more CTAs than are resident -- the bits
+    are those of the default launch, with positions gathered and masked, and
+    nothing outside the rotated spans is touched."""
+    require_gpu()
+    R = lib()
+    rows = cfg["S"] + 8
+    w = case(cfg["B"], cfg["Hq"], cfg["Hk"], cfg["S"], cfg["D"], cfg["rd"], cfg["dtype"],
+             cfg["layout"], cfg["sbh"], rows=rows)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    pos = (np.arange(w.S, dtype=np.int32) * 5 + 1) % rows
+    pos[0] = -1
+    pos[w.S // 3] = -1
+    pos_g = pos_tensor(pos)
+    got = {}
+    for t in ((0, 0, 0), tuning):
+        R.rope_tune_rotation_launch(*t)
+        qg, kg = Guarded(q), Guarded(k)
+        assert variant(w, qg.t, kg.t, cg, sg, pos_g) == 3
+        apply(w, qg.t, kg.t, cg, sg, pos=pos_g, backward=False)
+        first = (gpu_bits(qg.t), gpu_bits(kg.t))
+        apply(w, qg.t, kg.t, cg, sg, pos=pos_g, backward=True)
+        apply(w, qg.t, kg.t, cg, sg, pos=pos_g, backward=False)
+        assert R.rope_check_errors() == R.ROPE_OK
+        assert qg.intact() and kg.intact()
+        got[t] = first + (gpu_bits(qg.t), gpu_bits(kg.t))
+    a, b = got[(0, 0, 0)], got[tuning]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    # the first forward against the oracle; unrotated tokens bit-exact
+    sa = 1 if w.seq_before_head else 2
+    good = pos >= 0
+    idx, bad = np.flatnonzero(good), np.flatnonzero(~good)
+    for x, H, g in ((q, w.Hq, b[0]), (k, w.Hk, b[1])):
+        xb = np.ascontiguousarray(np.take(W.bits(x), idx, axis=sa))
+        yb, y64 = oracle_apply(w.with_sizes(S=len(idx)), xb, H, pos[idx], False, c32, s32)
+        assert_matches(w.dtype, np.ascontiguousarray(np.take(g, idx, axis=sa)), yb, y64,
+                       "tuning %s" % (tuning,))
+        assert np.array_equal(np.take(g, bad, axis=sa), np.take(W.bits(x), bad, axis=sa))
 
 
 def test_calls_replay_in_a_cuda_graph():

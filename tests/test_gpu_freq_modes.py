@@ -15,6 +15,7 @@ import torch
 
 import oracle as O
 import workloads as W
+import attention_check as AC
 from gpu_util import assert_matches, gpu_bits, lib, require_gpu
 
 pytestmark = pytest.mark.gpu
@@ -161,11 +162,9 @@ def test_attention_with_pixel_tables():
     out = R.attention(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(c32).cuda(),
                       torch.from_numpy(s32).cuda(), pos_q=pg, pos_k=pg, rotary_dim=64, causal=False)
     assert R.rope_check_errors() == R.ROPE_OK
-    ref = OA.attention(W.bits(q), W.bits(k), W.bits(v), O.BF16, 64, O.SPLIT_HALF, c32, s32, pos, pos,
-                       False)
-    got = out.float().cpu().numpy().astype(np.float64)
-    tol = 2.0 ** -8 * (float(v.float().abs().max()) + np.abs(ref))
-    assert np.all(np.abs(got - ref) <= tol)
+    ref, w, a = OA.attention(W.bits(q), W.bits(k), W.bits(v), O.BF16, 64, O.SPLIT_HALF, c32, s32,
+                             pos, pos, False, want_bounds=True)
+    AC.check(out.float().cpu().numpy(), ref, w, a, "bf16", "pixel tables")
 
 
 def _table_fuzz(n=16, seed=77):

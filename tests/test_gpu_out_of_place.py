@@ -187,3 +187,29 @@ def test_host_pipeline_head_pieces_q_only_and_seq_first(sbh, with_k):
     assert torch.equal(oq, dq.cpu())
     if with_k:
         assert torch.equal(ok_, dk.cpu())
+
+
+def test_host_pipeline_shape_change_without_sync():
+    """Back-to-back pipeline calls with different shapes and no wait between
+    them: the second call's new staging buffers must not reuse the first
+    call's memory while its copies are still queued.  Both results equal the
+    device calls bit for bit."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostRotator
+
+    rot = HostRotator(chunks=4)
+    outs = []
+    for i, (B, S) in enumerate(((4, 512), (2, 96), (4, 512))):
+        w = case(B, 8, 2, S, 128, 128, "bf16", rows=512, seed=30 + i)
+        q, k, _ = W.make_inputs(w)
+        cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+        hq, hk = q.pin_memory(), k.pin_memory()
+        oq, ok_ = torch.empty_like(q).pin_memory(), torch.empty_like(k).pin_memory()
+        done = rot.apply_qk(hq, hk, cos, sin, oq, ok_)
+        outs.append((w, q, k, cos, sin, oq, ok_, done))
+    for w, q, k, cos, sin, oq, ok_, done in outs:
+        done.synchronize()
+        dq, dk = q.cuda(), k.cuda()
+        R.apply_qk(dq, dk, cos, sin)
+        assert torch.equal(oq, dq.cpu()) and torch.equal(ok_, dk.cpu())

@@ -81,6 +81,17 @@ WORKLOADS = [
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
+# Launch-bound single calls of the Llama-3-8B-shaped layer: one decode step of
+# 64 sequences (one token each) and a short prefill.  Not among the five
+# workloads; the bench times them for the per-call cost of small calls.
+SMALL_CALLS = [
+    Workload("decode_b64_llama_bf16", 64, 32, 8, 1, 128, 128, 5e5, "bf16", "split_half",
+             False, 4096, "none", seed=7),
+    Workload("prefill_b1_s512_llama_bf16", 1, 32, 8, 512, 128, 128, 5e5, "bf16", "split_half",
+             False, 4096, "none", seed=8),
+]
+ALL_BY_NAME = dict(BY_NAME, **{w.name: w for w in SMALL_CALLS})
+
 
 def positions(w: Workload, gen: torch.Generator | None = None) -> np.ndarray | None:
     """int32 [S] position indices of the workload, or None for rows 0..S-1."""
