@@ -52,9 +52,10 @@ DEFAULT_WORKLOAD = "llama3_8b_gqa_bf16"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
-                  for f in ("rope_kernels.cuh", "rope_bulk.cuh", "rope_internal.cuh", "rope_api.cu")]
+                  for f in ("rope_kernels.cuh", "rope_internal.cuh", "rope_api.cu")]
 ATTN_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
-                for f in ("rope_attention.cu", "rope_kernels.cuh", "rope_internal.cuh", "rope_api.cu")]
+                for f in ("rope_attention.cuh", "rope_attention.cu", "rope_kernels.cuh", "rope_internal.cuh",
+                          "rope_api.cu")]
 
 
 def kernel_source_hash(sources=None) -> str:
@@ -212,7 +213,7 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_NAMES = {1: "rope_bulk_kernel", 2: "rope_scalar_kernel", 3: "rope_vec_kernel"}
+KERNEL_NAMES = {2: "rope_scalar_kernel", 3: "rope_vec_kernel"}
 
 
 def profiled_traffic(kernel: str, workload: str, sources=None):
@@ -325,6 +326,124 @@ def reference_step_seconds(args) -> float:
     """CPU seconds of one reference-arm step: at most 0.25 s, and about two
     minutes for all warm-up and timed steps together."""
     return min(0.25, 120.0 / max(1, args.steps + args.warmup))
+
+
+# --------------------------------------------------------------------------
+# every workload, forward and backward timed apart (the per_workload block)
+# --------------------------------------------------------------------------
+def rotating_sets(w, device, min_bytes: float, max_sets: int = 256):
+    """Device copies of the workload's Q, K: enough sets that one pass over
+    them moves at least min_bytes (so each call reads memory the previous
+    ones evicted from L2), two at least."""
+    q, k, pos = W.make_inputs(w)
+    per = sum(t.numel() * t.element_size() for t in (q, k) if t is not None)
+    n = int(min(max_sets, max(2, -(-min_bytes // per))))
+    sets = [(q.to(device), None if k is None else k.to(device)) for _ in range(n)]
+    return sets, (None if pos is None else torch.from_numpy(pos).to(device)), per
+
+
+def time_direction(R, w, sets, cos, sin, pos_g, stream, backward: int, device, min_ms: float,
+                   min_calls: int, graph_calls: int):
+    """Back-to-back calls of one direction over the rotating sets, events at
+    the two ends only (programmatic dependent launch stays on): eager through
+    the binding, eager through a prepared call, and the replay of a CUDA
+    graph of the same calls.  Returns a dict of µs per call, GB/s, fractions
+    and the clock record of the eager region."""
+    layout, sbh, dt = W.LAYOUTS[w.layout], int(w.seq_before_head), W.DTYPES[w.dtype]
+    nsets = len(sets)
+
+    def call(i):
+        qx, kx = sets[i % nsets]
+        R.rope_apply_qk(qx, kx, cos, sin, pos_g, w.B, w.Hq, w.Hk, w.S, w.D, w.rotary_dim, layout,
+                        sbh, backward, dt, w.table_rows, stream)
+
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    for i in range(10):
+        call(i)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for i in range(10):
+        call(i)
+    torch.cuda.synchronize(device)
+    est = max((time.perf_counter() - t0) / 10, 1e-7)
+    n = int(max(min_calls, min_ms * 1e-3 / est))
+
+    def region(fn, count):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(count):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / count
+
+    us = region(call, n)
+    sampler.stop()
+    prep = R.PreparedApply(sets[0][0], sets[0][1], cos, sin, pos_g, w.rotary_dim, w.layout,
+                           w.seq_before_head, stream)
+    pcall = (lambda i: prep(sets[i % nsets][0], sets[i % nsets][1], backward=bool(backward)))
+    for i in range(10):
+        pcall(i)
+    us_prep = region(pcall, n)
+    # the same calls captured once in a graph and replayed: device time
+    # without the host's launch cost
+    gcount = min(n, graph_calls)
+    gs = torch.cuda.Stream(device)
+    gs.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        with torch.cuda.graph(g, stream=gs):
+            for i in range(gcount):
+                qx, kx = sets[i % nsets]
+                R.rope_apply_qk(qx, kx, cos, sin, pos_g, w.B, w.Hq, w.Hk, w.S, w.D, w.rotary_dim,
+                                layout, sbh, backward, dt, w.table_rows, gs)
+    torch.cuda.synchronize(device)
+    g.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us_graph = e0.elapsed_time(e1) * 1e3 / gcount
+    del g
+    peak, _ = hbm_peak()
+    nbytes = W.algorithmic_bytes(w)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "gbs": round(gbs, 1),
+            "frac_of_hbm_measured": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+            "calls": n, "us_per_call_prepared": round(us_prep, 3),
+            "us_per_call_graph_replay": round(us_graph, 3), "graph_calls": gcount,
+            "gbs_graph_replay": round(nbytes / (us_graph * 1e-6) / 1e9, 1),
+            "clocks": sampler.summary()}
+
+
+def per_workload_block(R, device, stream, min_ms: float, min_calls: int, l2_bytes: int,
+                       names=None):
+    """Every workload (the five and two launch-bound single calls), forward
+    and backward apart."""
+    out = {}
+    for name in names or list(W.ALL_BY_NAME):
+        w = W.ALL_BY_NAME[name]
+        sets, pos_g, per = rotating_sets(w, device, 2.2 * l2_bytes)
+        cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32, device=device)
+        sin = torch.empty_like(cos)
+        R.rope_tables_build(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, cos, sin,
+                            stream)
+        entry = {"bytes_per_call": W.algorithmic_bytes(w),
+                 "config": {k: v for k, v in config_of(w).items() if k != "step"},
+                 "rotating_sets": len(sets),
+                 "l2": "%d sets of %.1f MB = %.0f MB per pass vs %.0f MB L2" % (
+                     len(sets), per / 1e6, len(sets) * per / 1e6, l2_bytes / 1e6)}
+        for backward, key in ((0, "forward"), (1, "backward")):
+            entry[key] = time_direction(R, w, sets, cos, sin, pos_g, stream, backward, device,
+                                        min_ms, min_calls, 400)
+        assert R.rope_check_errors(stream) == R.ROPE_OK
+        out[name] = entry
+        del sets
+        torch.cuda.empty_cache()
+    return out
 
 
 def config_of(w):
@@ -720,14 +839,24 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL_BY_NAME))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--per-workload-ms", type=float, default=20.0,
+                    help="rope: time every workload forward and backward apart, each region "
+                         "at least this long (and 200 calls) before the headline; 0 skips it")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="rope: rotating sets of Q, K, dQ, dK for the headline (0: enough that one "
+                         "pass moves at least 2.2 x the L2 size, at least one)")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="rope: run the workload with this sequence length instead (smaller "
+                         "cases for profiling runs)")
     ap.add_argument("--op", choices=["rope", "attention", "xpos"], default="rope",
                     help="rope: the fused Q+K rotation (default); attention: attention with the "
                          "rotation fused into the Q/K tile loads; xpos: the rotation with XPOS "
                          "tables, one launch per tensor")
     args = ap.parse_args()
+    args.e2e_steps = max(1, args.e2e_steps)
     if args.op == "xpos":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": "xpos",
@@ -738,7 +867,11 @@ def main():
         if args.impl == "reference":
             return attention_reference_arm(args)
         return attention_arm(args)
-    w = W.BY_NAME[args.workload]
+    w = W.ALL_BY_NAME[args.workload]
+    if args.seq > 0:
+        w = w.with_sizes(name="%s_S%d" % (w.name, args.seq), S=args.seq,
+                         table_rows=max(w.table_rows, args.seq) if w.positions == "none"
+                         else w.table_rows)
     if args.impl == "reference":
         return reference_arm(args, w)
 
@@ -757,16 +890,22 @@ def main():
     R.load_library()
     warmup = max(3, args.warmup)
     stream = torch.cuda.current_stream(device)
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+
+    # every workload, forward and backward timed apart, before the headline
+    # (it also brings the GPU to its working clocks)
+    per_workload = None
+    if args.per_workload_ms > 0:
+        per_workload = per_workload_block(R, device, stream, args.per_workload_ms, 200, l2_bytes)
 
     # inputs: seeded on the CPU, copied to rotating device sets so every call
     # reads memory last touched 3 steps (~1 GB of traffic) earlier: larger than L2
     q, k, pos = W.make_inputs(w)
     dq, dk, _ = W.make_inputs(w, seed_offset=100)
-    nsets = 4
+    set_bytes = sum(t.numel() * t.element_size() for t in (q, k, dq, dk) if t is not None)
+    nsets = args.sets if args.sets > 0 else max(1, -(-int(2.2 * l2_bytes) // set_bytes))
     sets = [(q.to(device), k.to(device), dq.to(device), dk.to(device)) for _ in range(nsets)]
     pos_g = None if pos is None else torch.from_numpy(pos).to(device)
-    set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
-    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
 
     cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32, device=device)
     sin = torch.empty_like(cos)
@@ -795,6 +934,10 @@ def main():
         if events is not None:
             events[2].record(stream)
 
+    # the clock sampler is set up and running before the warm-up, so nothing
+    # slow (NVML's set-up) leaves the GPU idle between warm-up and timed region
+    sampler = ClockSampler(local)
+    sampler.start()
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize(device)
@@ -804,11 +947,9 @@ def main():
     # events.  No event sits between launches inside it: an event there would
     # stop the next launch from becoming resident early (programmatic
     # dependent launch), which a user's stream does not do.
-    sampler = ClockSampler(local)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(device)
-    sampler.start()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
@@ -908,9 +1049,11 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic", "config": dict(
                 config_of(w),
-                l2=("inputs larger than L2: %d rotating sets of Q,K,dQ,dK, %.0f MB each, "
-                    "%.0f MB in all vs %.0f MB L2" % (nsets, set_bytes / 1e6,
-                                                      nsets * set_bytes / 1e6, l2_bytes / 1e6)),
+                l2=("inputs larger than L2: %d rotating set(s) of Q,K,dQ,dK, %.0f MB each, "
+                    "%.0f MB in all vs %.0f MB L2; each call's pair (%.0f MB) was last touched "
+                    "%.0f MB of traffic earlier" % (
+                        nsets, set_bytes / 1e6, nsets * set_bytes / 1e6, l2_bytes / 1e6,
+                        set_bytes / 2e6, (2 * nsets - 1) * set_bytes / 2e6)),
                 parallelism="replicas" if world > 1 else "single GPU"),
             "us_per_call": round(kernel_ms * 1e3, 3),
             "us_per_call_isolated": {"forward": round(fwd_ms * 1e3, 3),
@@ -931,6 +1074,8 @@ def main():
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if per_workload is not None:
+            line["per_workload"] = per_workload
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
