@@ -740,6 +740,62 @@ def attention_arm(args):
 
 
 # --------------------------------------------------------------------------
+# grid sizings of the rotation kernel side by side (--op sweep)
+# --------------------------------------------------------------------------
+def sweep_tunings(P: int, per_sm: int):
+    """(label, ctas_per_sm, min_units, prefetch_next) of rope_tune_rotation_launch."""
+    return [("rule", 0, 0, 0),
+            ("persistent_balanced", per_sm, 1, 0),
+            ("one_tile_per_lane_group", 64, P, 0),
+            ("half_tile_per_lane_group", 64, max(1, P // 2), 0),
+            ("quarter_tile_per_lane_group", 64, max(1, P // 4), 0),
+            ("rule_no_next_tile_prefetch", 0, 0, -1)]
+
+
+def sweep_arm(args):
+    """Every workload under each grid sizing of sweep_tunings: forward calls
+    back to back (as in per_workload), one JSON line per (workload, sizing).
+    The results do not depend on the sizing; only the time does."""
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from rotary_position_embedding_rope_gb300 import _build
+    if local == 0:
+        _build.build()
+    import rotary_position_embedding_rope_gb300 as R
+
+    R.load_library()
+    stream = torch.cuda.current_stream(device)
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+    per_sm = 4                                # resident CTAs of 128 threads (its launch bounds)
+    try:
+        for name in W.ALL_BY_NAME:
+            w = W.ALL_BY_NAME[name]
+            sets, pos_g, _ = rotating_sets(w, device, 2.2 * l2_bytes)
+            cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32,
+                              device=device)
+            sin = torch.empty_like(cos)
+            R.rope_tables_build(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, cos,
+                                sin, stream)
+            for label, cps, mu, pf in sweep_tunings(w.Hq + w.Hk, per_sm):
+                R.rope_tune_rotation_launch(cps, mu, pf)
+                r = time_direction(R, w, sets, cos, sin, pos_g, stream, 0, device,
+                                   args.per_workload_ms or 20.0, 200, 400)
+                if rank == 0:
+                    print(json.dumps({"op": "sweep", "workload": name, "grid": label,
+                                      "tuning": [cps, mu, pf], "us_per_call": r["us_per_call"],
+                                      "gbs": r["gbs"], "us_per_call_graph_replay":
+                                      r["us_per_call_graph_replay"],
+                                      "clocks": r["clocks"]}), flush=True)
+            assert R.rope_check_errors(stream) == R.ROPE_OK
+            del sets
+            torch.cuda.empty_cache()
+    finally:
+        R.rope_tune_rotation_launch(0, 0, 0)
+    return 0
+
+
+# --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
 # --------------------------------------------------------------------------
@@ -851,12 +907,19 @@ def main():
     ap.add_argument("--seq", type=int, default=0,
                     help="rope: run the workload with this sequence length instead (smaller "
                          "cases for profiling runs)")
-    ap.add_argument("--op", choices=["rope", "attention", "xpos"], default="rope",
+    ap.add_argument("--op", choices=["rope", "attention", "xpos", "sweep"], default="rope",
                     help="rope: the fused Q+K rotation (default); attention: attention with the "
                          "rotation fused into the Q/K tile loads; xpos: the rotation with XPOS "
-                         "tables, one launch per tensor")
+                         "tables, one launch per tensor; sweep: the rotation kernel's grid "
+                         "sizings side by side")
     args = ap.parse_args()
     args.e2e_steps = max(1, args.e2e_steps)
+    if args.op == "sweep":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "sweep",
+                              "unavailable": "the sweep compares grid sizings of the CUDA kernel"}))
+            return 0
+        return sweep_arm(args)
     if args.op == "xpos":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": "xpos",
