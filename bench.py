@@ -626,6 +626,33 @@ def attention_arm(args):
     inkernel = {"ms": round(ims, 4), "tflops": round(flops_of(a) / (ims * 1e-3) / 1e12, 1),
                 "what": "k_workspace=None: each CTA rotates its key tiles (rope_attn_kernel)"}
 
+    # context: the same call with an attn_mask -- all keys visible (the cost of
+    # the masked kernel instance), and key padding (batch entry b keeps its
+    # first S - 512 b keys)
+    masked = {}
+    for label, m in (("all_visible", torch.ones((a["B"], a["S"]), dtype=torch.bool,
+                                                device=device)),
+                     ("key_padding", torch.arange(a["S"], device=device)[None, :] <
+                      (a["S"] - 512 * torch.arange(a["B"], device=device))[:, None])):
+        def mstep(m=m):
+            R.attention(q, k, v, cos, sin, rotary_dim=a["rotary_dim"], causal=a["causal"], out=o,
+                        k_workspace=kws, attn_mask=m, stream=stream)
+        for _ in range(warmup):
+            mstep()
+        torch.cuda.synchronize(device)
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(steps):
+            mstep()
+        m1.record(stream)
+        torch.cuda.synchronize(device)
+        mms = m0.elapsed_time(m1) / steps
+        masked[label] = {"ms": round(mms, 4), "tflops_of_unmasked_flops":
+                         round(flops_of(a) / (mms * 1e-3) / 1e12, 1)}
+    masked["what"] = ("rope_attention_fwd_masked, workspace path, [B, Sk] mask: all keys visible, "
+                      "or batch entry b keeping its first S - 512 b keys (hidden key tiles are "
+                      "computed with P = 0)")
+
     # context: the same result from the unfused path (rotation kernel, then
     # torch's scaled_dot_product_attention on the rotated tensors)
     unfused = None
@@ -727,6 +754,7 @@ def attention_arm(args):
                                  "the launch that rotates K into the workspace"},
             "e2e": e2e,
             "inkernel_keys_context": inkernel,
+            "masked_context": masked,
             "unfused_context": unfused,
             "gpu_launches": 2 * steps,
             "clocks": sampler.summary(),

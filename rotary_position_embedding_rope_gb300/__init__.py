@@ -10,13 +10,15 @@ library, and a missing library is an error, never a fallback.
 
 ``build_tables``, ``apply_qk``, ``apply_q`` and ``rotate_qk`` are conveniences
 that read the sizes from tensor shapes and allocate tables and outputs with
-torch.  ``autograd.rotary_qk`` wraps the out-of-place call in a
+torch; ``PreparedApply`` checks a rotation's arguments once for calls
+repeated on tensors of one shape.  ``autograd.rotary_qk`` wraps the out-of-place call in a
 ``torch.autograd.Function`` (backward = rotation by the negated angle).
 ``build_tables_ex`` builds the table of a frequency mode ('lang', 'pixel',
 'constant') at given positions, optionally XPOS-scaled; ``apply_qk_xpos``
 rotates Q and K with their own XPOS tables.  ``attention`` calls
-``rope_attention_fwd``: attention with the rotation fused into the Q/K tile
-loads (or, with a key workspace, keys rotated once beforehand).
+``rope_attention_fwd`` (``rope_attention_fwd_masked`` with an ``attn_mask``):
+attention with the rotation fused into the Q/K tile loads (or, with a key
+workspace, keys rotated once beforehand).
 ``host.HostRotator`` and ``host.HostAttention`` run the rotation and the
 attention on tensors that live in pinned host memory, overlapping the copies
 with the calls.
@@ -32,14 +34,19 @@ from . import _build
 
 __all__ = [
     "RopeError", "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
-    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_ERR_KERNEL_TIMEOUT", "VARIANT_ELEMENTWISE",
-    "VARIANT_VECTOR", "rope_force_kernel_variant", "rope_tune_rotation_launch", "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16",
-    "ROPE_F16", "rope_tables_build", "rope_apply_qk", "rope_apply_q", "rope_check_errors",
-    "rope_status_string", "rope_qk_kernel_variant", "build_tables", "apply_qk", "apply_q",
-    "library_path", "load_library", "rope_apply_qk_out", "rotate_qk", "rope_attention_fwd",
-    "rope_attention_fwd_noalloc", "attention", "ROPE_FREQ_LANG", "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "rope_tables_build_ex",
-    "build_tables_ex", "apply_qk_xpos", "rope_probe_wait_expiry", "rope_attention_fwd_masked",
-    "ROPE_MASK_NONE", "ROPE_MASK_KEYS", "ROPE_MASK_QUERY_KEYS", "PreparedApply",
+    "ROPE_ERR_POS_OUT_OF_RANGE", "ROPE_ERR_KERNEL_TIMEOUT", "VARIANT_ELEMENTWISE", "VARIANT_VECTOR",
+    "ROPE_SPLIT_HALF", "ROPE_INTERLEAVED", "ROPE_F32", "ROPE_BF16", "ROPE_F16", "ROPE_FREQ_LANG",
+    "ROPE_FREQ_PIXEL", "ROPE_FREQ_CONSTANT", "ROPE_MASK_NONE", "ROPE_MASK_KEYS",
+    "ROPE_MASK_QUERY_KEYS", "library_path", "load_library",
+    # the C ABI, same names
+    "rope_tables_build", "rope_tables_build_ex", "rope_apply_qk", "rope_apply_q",
+    "rope_apply_qk_out", "rope_attention_fwd", "rope_attention_fwd_masked",
+    "rope_attention_fwd_noalloc", "rope_check_errors", "rope_probe_wait_expiry",
+    "rope_status_string", "rope_qk_kernel_variant", "rope_force_kernel_variant",
+    "rope_tune_rotation_launch",
+    # conveniences
+    "build_tables", "build_tables_ex", "apply_qk", "apply_q", "apply_qk_xpos", "rotate_qk",
+    "attention", "PreparedApply",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,

@@ -679,14 +679,18 @@ __device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t x)
 
 // attn_mask of the 128 keys k0 .. k0 + 127 for query row qi of batch b
 // (warp-collective): bit (i & 31) of vis[i >> 5] set when key k0 + i is
-// visible.  Keys at or past Sk, and rows at or past Sq, read as visible
-// (the tile's key count and the row's own bound hide them).
+// visible.  Keys at or past Sk, and rows at or past Sq, read as visible (the
+// tile's key count and the row's own bound hide them).
 //   a.mask_kind 1, [B, Sk]: lane l reads keys k0 + 32e + l (e = 0..3), four
 //     coalesced 32-byte reads shared by every row of the batch, and a ballot
 //     per e gives word e to all lanes;
 //   a.mask_kind 2, [B, Sq, Sk]: each row reads its own 128 bytes, as eight
 //     16-byte vectors when the rows are 16-byte aligned (a.mask_vec16), else
 //     byte by byte.
+// The softmax step calls it after the tensor-memory loads of S (holding the
+// mask's bytes across them would cost registers the step does not have);
+// mask_prefetch brings the next tile's bytes into L1 one step ahead, so that
+// these loads do not wait for L2.
 __device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t qi, int64_t k0,
                                           uint32_t (&vis)[4])
 {
@@ -727,6 +731,27 @@ __device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t 
     }
 }
 
+__device__ __forceinline__ void mask_prefetch(const AttnArgs &a, int64_t b, int64_t qi, int64_t k0)
+{
+    const int64_t k1 = k0 + kAttnKeys;              // the next tile
+    if (k1 >= a.Sk)
+        return;
+    const uint8_t *p;
+    if (a.mask_kind == 1) {
+        if ((threadIdx.x & 31) != 0)
+            return;                                 // one lane: the row is shared
+        p = a.mask + b * a.Sk + k1;
+    } else {
+        if (qi >= a.Sq)
+            return;
+        p = a.mask + (b * a.Sq + qi) * a.Sk + k1;
+    }
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+    const int64_t last = (a.Sk - k1 < kAttnKeys ? a.Sk - k1 : kAttnKeys) - 1;
+    if (((reinterpret_cast<uintptr_t>(p) & 127u) + (uint64_t)last) >= 128u)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p + last));
+}
+
 template <typename T, int D, bool PACKED, bool MASK, typename OReady = ONoWait>
 __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base, int64_t qi,
                                              int64_t k0, int64_t shift, const AttnArgs &a,
@@ -739,20 +764,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base,
         vis_end = qi + shift + 1;
     const int64_t nv = vis_end - k0;
     const int nvis = nv < 0 ? 0 : (nv > kAttnKeys ? kAttnKeys : (int)nv);
-    // the attn_mask of this tile, if any (before S is read: its loads do not
-    // wait behind the tensor-memory loads)
-    uint32_t vis[4];
-    bool unmasked = true;                  // no attn_mask bit clear in this tile
-    if constexpr (MASK) {
-        mask_bits(a, b, qi, k0, vis);
-        unmasked = __all_sync(0xffffffffu, (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu);
-    }
     const bool full = __all_sync(0xffffffffu, nvis == kAttnKeys);   // no causal/length mask
     float sv[kAttnKeys];
 #pragma unroll
     for (int c0 = 0; c0 < kAttnKeys; c0 += 32)
         tmem_ld32_nowait(acc_base + c0, sv + c0);
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    uint32_t vis[4];
+    bool unmasked = true;                  // no attn_mask bit clear in this tile
+    if constexpr (MASK) {
+        mask_bits(a, b, qi, k0, vis);
+        unmasked = __all_sync(0xffffffffu, (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu);
+        mask_prefetch(a, b, qi, k0);
+    }
     if (!full) {
 #pragma unroll
         for (int i = 0; i < kAttnKeys; ++i)

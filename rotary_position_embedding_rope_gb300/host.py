@@ -4,8 +4,10 @@ live in pinned host memory.
 The tensors are split along the batch dimension into chunks.  Chunk i is
 copied host->device on one stream, processed by the CUDA library on a second
 and copied device->host on a third, so the copies in both directions and the
-kernels of neighbouring chunks overlap.  Device staging buffers (two chunks
-per tensor) are allocated once per shape and reused.  Only argument
+kernels of neighbouring chunks overlap.  Device staging buffers (`slots`
+chunks per tensor, three by default: measured faster than two, no better
+with four) are allocated once per shape and reused, the pieces of successive
+calls taking them in turn.  Only argument
 marshalling and stream ordering happen here; the work is one library call
 per chunk.
 """
@@ -42,15 +44,17 @@ class HostRotator:
     split into equal groups of Q heads and of K heads.  Every head is rotated
     on its own, so every split gives the same bits."""
 
-    def __init__(self, device=None, chunks: int = 4):
+    def __init__(self, device=None, chunks: int = 4, slots: int = 3):
         self.device = torch.device("cuda") if device is None else torch.device(device)
         self.chunks = chunks
+        self.nslots = max(2, int(slots))
         self.s_in = torch.cuda.Stream(self.device)
         self.s_run = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
         self._key = None
         self._slots = None
-        self._free = [None, None]          # event: staging slot's device->host copy done
+        self._free = [None] * self.nslots  # event: staging slot's device->host copy done
+        self._next = 0                     # slot of the next piece (pieces of calls in turn)
 
     def _staging(self, q, k, dims_q, dims_k):
         key = (tuple(q.shape), None if k is None else tuple(k.shape), q.dtype, dims_q, dims_k)
@@ -61,9 +65,10 @@ class HostRotator:
             # the old slots may still be in use by copies and calls queued on
             # the three streams: recorded on them at creation, their memory is
             # not handed out again before that work is done
-            self._slots = [(dev(dims_q), None if k is None else dev(dims_k)) for _ in range(2)]
+            self._slots = [(dev(dims_q), None if k is None else dev(dims_k))
+                           for _ in range(self.nslots)]
             self._key = key
-            self._free = [None, None]
+            self._free = [None] * self.nslots
         return self._slots
 
     def apply_qk(self, q: torch.Tensor, k: torch.Tensor | None, cos: torch.Tensor,
@@ -99,8 +104,9 @@ class HostRotator:
             if after is not None:
                 s.wait_event(after)
         done = None
-        for c, (b0, b1, g, ng) in enumerate(pieces):
-            slot = c % 2
+        for b0, b1, g, ng in pieces:
+            slot = self._next
+            self._next = (self._next + 1) % self.nslots
             dq, dk = slots[slot]
             dq, dk = dq[: b1 - b0], None if dk is None else dk[: b1 - b0]
             if ng == 1:                    # whole batch entries
@@ -148,16 +154,18 @@ class HostAttention:
     streams, so neighbouring pieces overlap; more pieces leave less of the
     first copy in and the last copy out exposed."""
 
-    def __init__(self, device=None, chunks: int = 4):
+    def __init__(self, device=None, chunks: int = 4, slots: int = 3):
         self.device = torch.device("cuda") if device is None else torch.device(device)
         self.chunks = chunks
+        self.nslots = max(2, int(slots))
         self.s_in = torch.cuda.Stream(self.device)
         self.s_run = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
         self._key = None
         self._slots = None
         self._ws = None
-        self._free = [None, None]
+        self._free = [None] * self.nslots
+        self._next = 0
 
     def _pieces(self, B: int, Hk: int):
         """(b0, b1, kv0, kv1) ranges covering [0, B) x [0, Hk)."""
@@ -177,11 +185,11 @@ class HostAttention:
                                                device=self.device),
                                    (self.s_in, self.s_run, self.s_out))
             self._slots = [(dev(q, nkv * grp), dev(k, nkv), dev(k, nkv), dev(q, nkv * grp))
-                           for _ in range(2)]
+                           for _ in range(self.nslots)]
             # the calls all run on s_run, one after another: one workspace serves them
             self._ws = dev(k, nkv)
             self._key = key
-            self._free = [None, None]
+            self._free = [None] * self.nslots
         return self._slots, self._ws
 
     def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
@@ -213,8 +221,9 @@ class HostAttention:
             if after is not None:
                 s.wait_event(after)
         done = None
-        for c, (b0, b1, kv0, kv1) in enumerate(pieces):
-            slot = c % 2
+        for b0, b1, kv0, kv1 in pieces:
+            slot = self._next
+            self._next = (self._next + 1) % self.nslots
             hq0, hq1 = kv0 * grp, kv1 * grp
             # a piece is whole batch entries or one entry's heads: contiguous either way
             dq, dk, dv, do = slots[slot]

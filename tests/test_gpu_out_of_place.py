@@ -213,3 +213,30 @@ def test_host_pipeline_shape_change_without_sync():
         dq, dk = q.cuda(), k.cuda()
         R.apply_qk(dq, dk, cos, sin)
         assert torch.equal(oq, dq.cpu()) and torch.equal(ok_, dk.cpu())
+
+
+@pytest.mark.parametrize("slots,chunks", [(3, 5), (4, 4)])
+def test_host_pipeline_more_staging_slots(slots, chunks):
+    """With more staging slots than two, the pieces of successive calls take
+    the slots in turn; two calls back to back (forward, then backward on other
+    tensors) give the device calls' bits."""
+    require_gpu()
+    R = lib()
+    from rotary_position_embedding_rope_gb300.host import HostRotator
+
+    w = case(5, 4, 2, 64, 128, 128, "bf16", rows=64)
+    q, k, _ = W.make_inputs(w)
+    dq, dk, _ = W.make_inputs(w, seed_offset=9)
+    cos, sin = R.build_tables(w.theta, w.rotary_dim, w.table_rows)
+    rot = HostRotator(chunks=chunks, slots=slots)
+    outs = []
+    for x, y, backward in ((q, k, False), (dq, dk, True)):
+        hx, hy = x.pin_memory(), y.pin_memory()
+        ox, oy = torch.empty_like(x).pin_memory(), torch.empty_like(y).pin_memory()
+        outs.append((x, y, backward, ox, oy, rot.apply_qk(hx, hy, cos, sin, ox, oy,
+                                                         backward=backward)))
+    for x, y, backward, ox, oy, done in outs:
+        done.synchronize()
+        gx, gy = x.cuda(), y.cuda()
+        R.apply_qk(gx, gy, cos, sin, backward=backward)
+        assert torch.equal(ox, gx.cpu()) and torch.equal(oy, gy.cpu())
