@@ -687,10 +687,10 @@ __device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t x)
 //   a.mask_kind 2, [B, Sq, Sk]: each row reads its own 128 bytes, as eight
 //     16-byte vectors when the rows are 16-byte aligned (a.mask_vec16), else
 //     byte by byte.
-// The softmax step calls it after the tensor-memory loads of S (holding the
-// mask's bytes across them would cost registers the step does not have);
-// mask_prefetch brings the next tile's bytes into L1 one step ahead, so that
-// these loads do not wait for L2.
+// The softmax step calls it after the tensor-memory loads of S: holding the
+// mask's bytes across them costs registers the step does not have (spills),
+// and an L1 prefetch of the next tile's bytes one step ahead measured slower
+// than none.
 __device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t qi, int64_t k0,
                                           uint32_t (&vis)[4])
 {
@@ -731,27 +731,6 @@ __device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t 
     }
 }
 
-__device__ __forceinline__ void mask_prefetch(const AttnArgs &a, int64_t b, int64_t qi, int64_t k0)
-{
-    const int64_t k1 = k0 + kAttnKeys;              // the next tile
-    if (k1 >= a.Sk)
-        return;
-    const uint8_t *p;
-    if (a.mask_kind == 1) {
-        if ((threadIdx.x & 31) != 0)
-            return;                                 // one lane: the row is shared
-        p = a.mask + b * a.Sk + k1;
-    } else {
-        if (qi >= a.Sq)
-            return;
-        p = a.mask + (b * a.Sq + qi) * a.Sk + k1;
-    }
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-    const int64_t last = (a.Sk - k1 < kAttnKeys ? a.Sk - k1 : kAttnKeys) - 1;
-    if (((reinterpret_cast<uintptr_t>(p) & 127u) + (uint64_t)last) >= 128u)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(p + last));
-}
-
 template <typename T, int D, bool PACKED, bool MASK, typename OReady = ONoWait>
 __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base, int64_t qi,
                                              int64_t k0, int64_t shift, const AttnArgs &a,
@@ -775,7 +754,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base,
     if constexpr (MASK) {
         mask_bits(a, b, qi, k0, vis);
         unmasked = __all_sync(0xffffffffu, (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu);
-        mask_prefetch(a, b, qi, k0);
     }
     if (!full) {
 #pragma unroll

@@ -183,6 +183,47 @@ def test_attention_fuzz(c):
            "fuzz%02d" % c["i"])
 
 
+def _masked_fuzz_cases(n=16, seed=4048):
+    g = np.random.default_rng(seed)
+    cases = _fuzz_cases(n, seed)
+    for c in cases:
+        c["mask"] = str(g.choice(["keys", "query_keys"]))
+        c["density"] = float(g.choice([0.1, 0.5, 0.9, 1.0]))
+    return cases
+
+
+@pytest.mark.parametrize("c", _masked_fuzz_cases(), ids=lambda c: "mfuzz%02d" % c["i"])
+def test_attention_masked_fuzz(c):
+    """Seeded random shapes, spans, layouts, types, positions and attn_masks
+    ([B, Sk] or [B, Sq, Sk], 10 % to all keys visible, byte-aligned or not):
+    the workspace path against the oracle, the in-kernel key path bit for bit
+    against it."""
+    require_gpu()
+    R = lib()
+    q, k, v = _inputs(c["B"], c["Hq"], c["Hk"], c["Sq"], c["Sk"], c["D"], c["dtype"], c["seed"])
+    g = np.random.default_rng(c["seed"] + 1)
+    rows = max(c["Sq"], c["Sk"]) + 16
+    pq = pk = None
+    if c["pos"] == "random":
+        pq = g.integers(-1, rows, c["Sq"]).astype(np.int32)
+        pk = g.integers(-1, rows, c["Sk"]).astype(np.int32)
+    shape = (c["B"], c["Sk"]) if c["mask"] == "keys" else (c["B"], c["Sq"], c["Sk"])
+    m = g.random(shape) < c["density"]
+    c32, s32 = oracle_tables(1e4, c["rd"], rows)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    args = (q.cuda(), k.cuda(), v.cuda(), cg, sg)
+    kw = dict(pos_q=None if pq is None else torch.from_numpy(pq).cuda(),
+              pos_k=None if pk is None else torch.from_numpy(pk).cuda(),
+              rotary_dim=c["rd"], layout=c["layout"], causal=c["causal"],
+              attn_mask=torch.from_numpy(m).cuda())
+    o = R.attention(*args, **kw)
+    o_in = R.attention(*args, k_workspace=None, **kw)
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(o.view(torch.int16), o_in.view(torch.int16)), "key paths differ"
+    _check(o, q, k, v, c["dtype"], c["rd"], W.LAYOUTS[c["layout"]], c32, s32, pq, pk, c["causal"],
+           "mfuzz%02d" % c["i"], attn_mask=m)
+
+
 def test_attention_full_size_sampled_rows():
     """The bench's attention workload at full size (Q [4,32,4096,128], K/V
     [4,8,4096,128] bf16, causal, theta 5e5) through the workspace path, in
