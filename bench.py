@@ -446,6 +446,44 @@ def per_workload_block(R, device, stream, min_ms: float, min_calls: int, l2_byte
     return out
 
 
+def link_context(device, stream, nbytes: int = 256 << 20, reps: int = 3):
+    """GB/s of pinned-host <-> device copies: host to device, device to host,
+    and both at once on two streams (best of reps)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s2 = torch.cuda.Stream(device)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def both():
+        s2.wait_stream(stream)
+        d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+        stream.wait_stream(s2)
+
+    h2d = timed(lambda: d_a.copy_(h_in, non_blocking=True))
+    d2h = timed(lambda: h_out.copy_(d_b, non_blocking=True))
+    bi = timed(both)
+    gbs = lambda n, ms: round(n / (ms * 1e-3) / 1e9, 1)
+    return {"h2d_gbs": gbs(nbytes, h2d), "d2h_gbs": gbs(nbytes, d2h),
+            "both_directions_gbs": gbs(2 * nbytes, bi),
+            "what": "256 MiB pinned-host copies, best of %d" % reps}
+
+
 def config_of(w):
     return {"workload": w.name, "q_shape": list(w.q_shape), "k_shape": list(w.k_shape),
             "dtype": w.dtype, "layout": w.layout,
@@ -1103,6 +1141,11 @@ def main():
     e2e_value = e2e_bytes / (e2e_ms * 1e-3) / 1e9
     assert R.rope_check_errors(stream) == R.ROPE_OK
 
+    # the host link the e2e leg is bound by: 256 MiB copies between pinned
+    # host memory and the device, each direction alone and both at once on
+    # two streams (plain runtime copies, context for the e2e figure)
+    link = link_context(device, stream)
+
     # roofline of the dominant kernel.  The timed region holds only its
     # launches (2 per step), so its average launch duration is the region's
     # event time over the launch count.
@@ -1159,7 +1202,8 @@ def main():
                          "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": h2d, "steps": args.e2e_steps,
-                    "ms_per_step": round(e2e_ms / args.e2e_steps, 4)},
+                    "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
+                    "link_context": link},
             "gpu_launches": launches,
             "kernel_variant": variant,
             "clocks": clocks,
