@@ -49,6 +49,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "fused Q+K RoPE fwd/bwd achieved HBM GB/s (% of GB300 peak) and µs/call"
 DEFAULT_WORKLOAD = "llama3_8b_gqa_bf16"
+PRE_ROLL_CYCLES = 1_000_000          # GPU clock cycles slept before a timed region (~0.5 ms)
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "rotary_position_embedding_rope_gb300", "csrc", f)
@@ -1079,6 +1080,11 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(device)
+    # A GPU-side pause of ~0.5 ms before the start event (outside the timed
+    # region): while the GPU sleeps, the host enqueues the region's first
+    # launches, so a host-side delay at the start of a short region (thread
+    # scheduling, a driver query) cannot appear as idle GPU time inside it.
+    torch.cuda._sleep(PRE_ROLL_CYCLES)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
@@ -1183,6 +1189,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic", "config": dict(
                 config_of(w),
+                timed_region=("exactly %d steps between two events, after a synchronize and a "
+                              "%d-cycle GPU-side sleep outside the region (the host enqueues the "
+                              "first launches meanwhile)" % (args.steps, PRE_ROLL_CYCLES)),
                 l2=("inputs larger than L2: %d rotating set(s) of Q,K,dQ,dK, %.0f MB each, "
                     "%.0f MB in all vs %.0f MB L2; each call's pair (%.0f MB) was last touched "
                     "%.0f MB of traffic earlier" % (
