@@ -429,3 +429,35 @@ def test_host_attention_shape_change_without_sync():
         torch.cuda.synchronize()
         assert torch.equal(ho, want.cpu())
     assert R.rope_check_errors() == R.ROPE_OK
+
+
+@pytest.mark.parametrize("ws", sorted(WS))
+def test_attention_full_size_key_padding_sampled_rows(ws):
+    """The bench's masked attention call at full size: the Llama-shaped causal
+    prefill with a [B, Sk] key-padding mask (batch entry b keeps its first
+    S - 512 b keys).  Sampled query rows against the oracle: row i at its own
+    position against the keys 0..i with the batch entry's mask."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, S, D, rd = 4, 32, 8, 4096, 128, 128
+    q, k, v = _inputs(B, Hq, Hk, S, S, D, "bf16", 6)
+    keep = S - 512 * np.arange(B)
+    m = np.arange(S)[None, :] < keep[:, None]
+    c32, s32 = oracle_tables(5e5, rd, S)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    o = R.attention(q.cuda(), k.cuda(), v.cuda(), cg, sg, causal=True, k_workspace=WS[ws],
+                    attn_mask=torch.from_numpy(m).cuda()).cpu()
+    assert R.rope_check_errors() == R.ROPE_OK
+    rng = np.random.default_rng(21)
+    rows = [(0, 0, 4095), (3, 31, 4095), (3, 5, 2560), (2, 9, 3000), (1, 17, 3583), (1, 2, 3584)]
+    rows += [(int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(S))) for _ in range(12)]
+    group = Hq // Hk
+    for b, h, i in rows:
+        kv = h // group
+        ref, w, a = OA.attention(W.bits(q[b:b + 1, h:h + 1, i:i + 1]),
+                                 W.bits(k[b:b + 1, kv:kv + 1, :i + 1]),
+                                 W.bits(v[b:b + 1, kv:kv + 1, :i + 1]), O.BF16, rd, O.SPLIT_HALF,
+                                 c32, s32, np.array([i], dtype=np.int32), None, False,
+                                 want_bounds=True, attn_mask=m[b:b + 1, :i + 1])
+        AC.check(o[b:b + 1, h:h + 1, i:i + 1].float().numpy(), ref, w, a, "bf16",
+                 "full size key padding (%s): row (%d, %d, %d)" % (ws, b, h, i))

@@ -172,3 +172,24 @@ def test_full_size_sampled(name):
             del got_all, xb
         del qg, kg
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("backward", [False, True], ids=["fwd", "bwd"])
+@pytest.mark.parametrize("name", [w.name for w in W.SMALL_CALLS])
+def test_small_calls_all_elements(name, backward):
+    """The launch-bound calls the bench times (a decode step of 64 sequences
+    with one token each; a 512-token prefill), at their full size: they take
+    the launch rule's small-call branch (balanced runs over the resident
+    lane groups, runs shorter than a tile).  Every element against the
+    oracle."""
+    require_gpu()
+    w = W.ALL_BY_NAME[name]
+    q, k, pos = W.make_inputs(w)
+    cos32, sin32 = oracle_tables(w.theta, w.rotary_dim, w.table_rows)
+    cg, sg = torch.from_numpy(cos32).cuda(), torch.from_numpy(sin32).cuda()
+    qg, kg = q.cuda(), k.cuda()
+    run_apply(w, qg, kg, cg, sg, pos_tensor(pos), backward)
+    assert lib().rope_check_errors() == lib().ROPE_OK
+    for x, xg, H in ((q, qg, w.Hq), (k, kg, w.Hk)):
+        yb, y64 = oracle_apply(w, W.bits(x), H, pos, backward, cos32, sin32)
+        assert_matches(w.dtype, gpu_bits(xg), yb, y64, "%s %s" % (name, "bwd" if backward else "fwd"))
