@@ -340,7 +340,7 @@ def rotating_sets(w, device, min_bytes: float, max_sets: int = 256):
     per = sum(t.numel() * t.element_size() for t in (q, k) if t is not None)
     n = int(min(max_sets, max(2, -(-min_bytes // per))))
     sets = [(q.to(device), None if k is None else k.to(device)) for _ in range(n)]
-    return sets, (None if pos is None else torch.from_numpy(pos).to(device)), per
+    return sets, (None if pos is None else torch.from_numpy(pos).to(device)), per, (q, k, pos)
 
 
 def time_direction(R, w, sets, cos, sin, pos_g, stream, backward: int, device, min_ms: float,
@@ -421,13 +421,14 @@ def time_direction(R, w, sets, cos, sin, pos_g, stream, backward: int, device, m
 
 
 def per_workload_block(R, device, stream, min_ms: float, min_calls: int, l2_bytes: int,
-                       names=None):
+                       names=None, cpu_seconds: float = 0.0):
     """Every workload (the five and two launch-bound single calls), forward
-    and backward apart."""
+    and backward apart; with cpu_seconds > 0 also the single-threaded oracle
+    on growing prefixes of batch 0 for about that long per workload."""
     out = {}
     for name in names or list(W.ALL_BY_NAME):
         w = W.ALL_BY_NAME[name]
-        sets, pos_g, per = rotating_sets(w, device, 2.2 * l2_bytes)
+        sets, pos_g, per, host = rotating_sets(w, device, 2.2 * l2_bytes)
         cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32, device=device)
         sin = torch.empty_like(cos)
         R.rope_tables_build(w.theta, w.rotary_dim, w.table_rows, w.interpolate_factor, cos, sin,
@@ -441,6 +442,20 @@ def per_workload_block(R, device, stream, min_ms: float, min_calls: int, l2_byte
             entry[key] = time_direction(R, w, sets, cos, sin, pos_g, stream, backward, device,
                                         min_ms, min_calls, 400)
         assert R.rope_check_errors(stream) == R.ROPE_OK
+        if cpu_seconds > 0:
+            import oracle as O
+
+            q, k, pos = host
+            cos32, sin32 = O.load().tables(w.theta, w.rotary_dim, w.table_rows,
+                                           w.interpolate_factor, "f32")
+            threads = torch.get_num_threads()
+            torch.set_num_threads(1)
+            nb, el, toks = time_oracle(w, cpu_seconds, [(q, w.Hq), (k, w.Hk), (q, w.Hq),
+                                                        (k, w.Hk)], pos, cos32, sin32)
+            torch.set_num_threads(threads)
+            entry["cpu_oracle"] = {"gbs": round(nb / el / 1e9, 4), "cores": 1,
+                                   "sample": "batch 0, growing token prefixes (%d token-steps in "
+                                             "%.1f s), forward and backward" % (toks, el)}
         out[name] = entry
         del sets
         torch.cuda.empty_cache()
@@ -838,7 +853,7 @@ def sweep_arm(args):
     try:
         for name in W.ALL_BY_NAME:
             w = W.ALL_BY_NAME[name]
-            sets, pos_g, _ = rotating_sets(w, device, 2.2 * l2_bytes)
+            sets, pos_g, _, _ = rotating_sets(w, device, 2.2 * l2_bytes)
             cos = torch.empty((w.table_rows, w.rotary_dim // 2), dtype=torch.float32,
                               device=device)
             sin = torch.empty_like(cos)
@@ -1026,7 +1041,9 @@ def main():
     # (it also brings the GPU to its working clocks)
     per_workload = None
     if args.per_workload_ms > 0:
-        per_workload = per_workload_block(R, device, stream, args.per_workload_ms, 200, l2_bytes)
+        per_workload = per_workload_block(
+            R, device, stream, args.per_workload_ms, 200, l2_bytes,
+            cpu_seconds=min(1.5, args.cpu_seconds / 5) if rank == 0 and world == 1 else 0.0)
 
     # inputs: seeded on the CPU, copied to rotating device sets so every call
     # reads memory last touched 3 steps (~1 GB of traffic) earlier: larger than L2

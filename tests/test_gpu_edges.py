@@ -456,3 +456,25 @@ def test_calls_replay_in_a_cuda_graph():
     assert R.rope_check_errors() == R.ROPE_OK
     assert torch.equal(gq, eq) and torch.equal(gk, ek)
     assert torch.equal(gdq, edq) and torch.equal(gdk, edk)
+
+
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_launch_rule_boundary_against_oracle(delta):
+    """The launch rule switches from balanced runs over the resident lane
+    groups to one tile per lane group when the call has as many tiles as
+    there are resident lane groups (SM count x 4 CTAs x 4 lane groups for
+    bf16 rd = 128).  One tile below, at and above that count (4 tokens per
+    tile), against the oracle, forward and backward."""
+    require_gpu()
+    R = lib()
+    lanes = torch.cuda.get_device_properties(0).multi_processor_count * 4 * 4
+    S = 4 * (lanes + delta) - 2                    # ragged last tile
+    w = case(1, 2, 1, S, 128, 128, "bf16", rows=S)
+    q, k, _ = W.make_inputs(w)
+    c32, s32, cg, sg = tables(w)
+    for backward in (False, True):
+        qg, kg = q.cuda(), k.cuda()
+        apply(w, qg, kg, cg, sg, backward=backward)
+        assert R.rope_check_errors() == R.ROPE_OK
+        check_vs_oracle(w, q, qg, w.Hq, None, backward, c32, s32, "Q delta %d" % delta)
+        check_vs_oracle(w, k, kg, w.Hk, None, backward, c32, s32, "K delta %d" % delta)
