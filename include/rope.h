@@ -276,6 +276,13 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
  *    Dense, contiguous, shared by all heads; it must not overlap o or the
  *    workspace.  The mask applies together with `causal`; a query row that
  *    sees no key gets zeros.
+ * Key tiles a [B, Sk] mask hides entirely: with a k_workspace of at least
+ *    W + 4 B bytes, W = B * Hk * Sk * D * 2 rounded up to a multiple of 16,
+ *    the call also writes there (from byte W) the number of 128-key tiles up
+ *    to each batch entry's last visible key, and the attention kernels skip
+ *    the tiles past it (the result is the same bit for bit: hidden keys only
+ *    add exact zeros).  With a smaller workspace, or none, every tile is
+ *    computed.
  * Everything else as rope_attention_fwd.
  * Errors: as rope_attention_fwd; also ROPE_ERR_UNSUPPORTED for a mask_kind
  *    outside the enum and ROPE_ERR_INVALID_ARG for a NULL mask (with Sk > 0)

@@ -46,7 +46,7 @@ __all__ = [
     "rope_tune_rotation_launch",
     # conveniences
     "build_tables", "build_tables_ex", "apply_qk", "apply_q", "apply_qk_xpos", "rotate_qk",
-    "attention", "PreparedApply",
+    "attention", "attention_workspace", "PreparedApply",
 ]
 
 (ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA, ROPE_ERR_POS_OUT_OF_RANGE,
@@ -537,6 +537,17 @@ def rope_attention_fwd_noalloc(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq
     _check(st, "rope_attention_fwd_noalloc")
 
 
+def attention_workspace(k: torch.Tensor, attn_mask: torch.Tensor | None = None) -> torch.Tensor:
+    """A key workspace for rope_attention_fwd(_masked) on keys like k: rot(K)
+    and, for a [B, Sk] attn_mask, the per-batch key-tile counts after it (with
+    them the kernels skip the key tiles the mask hides entirely)."""
+    kb = k.numel() * k.element_size()
+    n = kb
+    if attn_mask is not None and attn_mask.dim() == 2:
+        n = (kb + 15) // 16 * 16 + 4 * k.shape[0]
+    return torch.empty(n, dtype=torch.uint8, device=k.device)
+
+
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor,
               sin: torch.Tensor, pos_q: torch.Tensor | None = None,
               pos_k: torch.Tensor | None = None, rotary_dim: int | None = None,
@@ -545,11 +556,11 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
               attn_mask: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """softmax(scale * rot(q) rot(k)^T + mask) v with q [B,Hq,Sq,D], k/v [B,Hk,Sk,D].
 
-    k_workspace: "auto" allocates a buffer like k that receives rot(K) (the
-    keys are rotated once, then read rotated by the attention kernel); a
-    tensor of k's size is used as that buffer; None rotates the key tiles
-    inside the attention kernel instead (nothing extra is written).  The
-    result is the same bit for bit.
+    k_workspace: "auto" allocates a buffer (attention_workspace) that receives
+    rot(K) (the keys are rotated once, then read rotated by the attention
+    kernel); a tensor of at least k's size is used as that buffer; None
+    rotates the key tiles inside the attention kernel instead (nothing extra
+    is written).  The result is the same bit for bit.
     attn_mask: None, or a bool (or uint8) CUDA tensor [B, Sk] (one entry per
     key) or [B, Sq, Sk] (one per query and key); False hides the key from the
     query, together with the causal mask.
@@ -563,7 +574,7 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
     if isinstance(k_workspace, str):
         if k_workspace != "auto":
             raise ValueError("k_workspace must be 'auto', None or a tensor")
-        k_workspace = torch.empty_like(k)
+        k_workspace = attention_workspace(k, attn_mask)
     ws_bytes = 0 if k_workspace is None else k_workspace.numel() * k_workspace.element_size()
     args = (q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq, Sk, D, rd, _LAYOUT_CODE[layout],
             int(causal), -1.0 if scale is None else scale, _DTYPE_CODE[q.dtype], cos.shape[0])

@@ -58,6 +58,40 @@ __global__ void take_flag_kernel(int32_t *flag, int32_t *taken)
     *taken = atomicExch(flag, 0);
 }
 
+// Key tiles of 128 up to the last visible key of each batch entry of a
+// [B, Sk] attn_mask: one CTA per entry; each thread scans its keys from the
+// end down and stops at its first visible one, then the CTA takes the max.
+constexpr int kMaskTileKeys = 128;         // the attention kernels' key tile
+__global__ void mask_tiles_kernel(const uint8_t *mask, int64_t Sk, int32_t *tiles)
+{
+    __shared__ int32_t warp_last[8];
+    const uint8_t *row = mask + (int64_t)blockIdx.x * Sk;
+    int32_t last = -1;
+    for (int64_t i = Sk - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
+        if (row[i] != 0) {
+            last = (int32_t)i;
+            break;
+        }
+    }
+    last = __reduce_max_sync(0xffffffffu, last);
+    if ((threadIdx.x & 31) == 0)
+        warp_last[threadIdx.x >> 5] = last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t m = -1;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+            m = warp_last[w] > m ? warp_last[w] : m;
+        tiles[blockIdx.x] = m < 0 ? 0 : m / kMaskTileKeys + 1;
+    }
+}
+
+cudaError_t launch_mask_tiles(const uint8_t *mask, int64_t B, int64_t Sk, int32_t *tiles,
+                              cudaStream_t st)
+{
+    mask_tiles_kernel<<<(unsigned)B, 256, 0, st>>>(mask, Sk, tiles);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // cos/sin table ("rotary-embedding-torch", RotaryEmbedding / Key Parameters:
 // theta base, interpolate_factor scales positions; "Rotary Embedding (RoPE)
@@ -446,6 +480,20 @@ struct AttnCall {
     int64_t workspace_bytes;
 };
 
+// Bytes of the key workspace a call uses: rot(K) (kb bytes); with a [B, Sk]
+// mask and room for them, then B int32 key-tile counts from the first
+// 16-byte boundary after rot(K).
+static int64_t mask_tiles_offset(int64_t kb) { return (kb + 15) / 16 * 16; }
+
+static int64_t workspace_extent(const AttnCall &c, int64_t kb)
+{
+    const int64_t tiles_end = mask_tiles_offset(kb) + 4 * c.B;
+    if (c.mask_kind == ROPE_MASK_KEYS && c.Sk <= 0x7fffffffLL && c.B <= 0x7fffffffLL &&
+        c.workspace_bytes >= tiles_end)
+        return tiles_end;
+    return kb;
+}
+
 // Host checks of an attention call, in order; *empty is set when the call
 // has no output rows (nothing to do).  No CUDA calls.
 static rope_status attention_check(const AttnCall &c, bool *empty, int64_t *kbytes)
@@ -495,18 +543,20 @@ static rope_status attention_check(const AttnCall &c, bool *empty, int64_t *kbyt
         ranges_overlap(o, qb, c.pos_k, c.Sk * 4) || ranges_overlap(o, qb, c.mask, mb))
         return ROPE_ERR_INVALID_ARG;
     // the key workspace receives rot(K): at least kb bytes, aligned, and
-    // disjoint from every other buffer of the call
+    // disjoint from every other buffer of the call (with the key tiles of a
+    // [B, Sk] mask after them when it has room for those too)
     const void *ws = c.Sk > 0 ? c.k_workspace : nullptr;
     if (ws != nullptr) {
         if (c.workspace_bytes < kb)
             return ROPE_ERR_INVALID_ARG;
         if (!aligned16(ws))
             return ROPE_ERR_UNSUPPORTED;
-        if (ranges_overlap(ws, kb, c.q, qb) || ranges_overlap(ws, kb, c.k, kb) ||
-            ranges_overlap(ws, kb, c.v, kb) || ranges_overlap(ws, kb, o, qb) ||
-            ranges_overlap(ws, kb, c.cos, tabb) || ranges_overlap(ws, kb, c.sin, tabb) ||
-            ranges_overlap(ws, kb, c.pos_q, c.Sq * 4) || ranges_overlap(ws, kb, c.pos_k, c.Sk * 4) ||
-            ranges_overlap(ws, kb, c.mask, mb))
+        const int64_t used = workspace_extent(c, kb);
+        if (ranges_overlap(ws, used, c.q, qb) || ranges_overlap(ws, used, c.k, kb) ||
+            ranges_overlap(ws, used, c.v, kb) || ranges_overlap(ws, used, o, qb) ||
+            ranges_overlap(ws, used, c.cos, tabb) || ranges_overlap(ws, used, c.sin, tabb) ||
+            ranges_overlap(ws, used, c.pos_q, c.Sq * 4) ||
+            ranges_overlap(ws, used, c.pos_k, c.Sk * 4) || ranges_overlap(ws, used, c.mask, mb))
             return ROPE_ERR_INVALID_ARG;
     }
     return ROPE_OK;
@@ -546,6 +596,15 @@ static rope_status attention_call(const AttnCall &c, void *stream)
         const rope_status s = apply_call(r, stream);
         if (s != ROPE_OK)
             return s;
+        // a [B, Sk] mask: the key tiles each batch entry shows, after rot(K)
+        if (a.mask_kind == ROPE_MASK_KEYS && workspace_extent(c, kb) > kb) {
+            int32_t *tiles = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) +
+                                                         mask_tiles_offset(kb));
+            if (launch_mask_tiles(c.mask, c.B, c.Sk, tiles, static_cast<cudaStream_t>(stream)) !=
+                cudaSuccess)
+                return ROPE_ERR_CUDA;
+            a.kv_tiles = tiles;
+        }
     }
     return launch_attention(a, c.D, c.layout, c.dtype, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess

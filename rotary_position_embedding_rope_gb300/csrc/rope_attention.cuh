@@ -607,6 +607,13 @@ __device__ __forceinline__ AttnWork attn_work(const AttnArgs &a, int32_t pair_he
         if (t < w.n_tiles)
             w.n_tiles = t;
     }
+    // key tiles past the last key the batch entry's attn_mask shows hold only
+    // hidden keys: every role reads the same count, so all skip them alike
+    if (a.kv_tiles != nullptr) {
+        const int64_t t = __ldg(a.kv_tiles + w.b);
+        if (t < w.n_tiles)
+            w.n_tiles = t;
+    }
     return w;
 }
 

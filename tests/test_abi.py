@@ -317,3 +317,21 @@ def test_masked_attention_empty_and_no_mask(lib):
     # kind 0 ignores the pointer: the same checks as rope_attention_fwd
     assert lib.rope_attention_fwd_masked(*masked_args(mask=None, kind=0, dtype=0)) == \
         lib.rope_attention_fwd(*attn_args(dtype=0))
+
+
+def test_masked_attention_workspace_with_key_tiles(lib):
+    """A workspace with room for the key-tile counts of a [B, Sk] mask is
+    checked over its whole used extent: rot(K), then B int32 counts from the
+    next 16-byte boundary."""
+    kb = 1 * 2 * 64 * 128 * 2                 # B * Hk * Sk * D * 2
+    used = (kb + 15) // 16 * 16 + 4 * 1
+    ws = A16 * 800
+    # a mask right after rot(K) overlaps the counts of a workspace with room
+    # for them (refused before anything touches the device)
+    assert lib.rope_attention_fwd_masked(*masked_args(mask=ws + kb, kind=1, ws=ws,
+                                                      ws_bytes=used)) == R.ROPE_ERR_INVALID_ARG
+    # a per-query mask never uses the counts: the same placement then only
+    # has to clear rot(K)'s kb bytes -- checked here through the overlap with
+    # o instead, which is refused either way
+    assert lib.rope_attention_fwd_masked(*masked_args(mask=A16 * 300, kind=2, ws=ws,
+                                                      ws_bytes=used)) == R.ROPE_ERR_INVALID_ARG

@@ -461,3 +461,43 @@ def test_attention_full_size_key_padding_sampled_rows(ws):
                                  want_bounds=True, attn_mask=m[b:b + 1, :i + 1])
         AC.check(o[b:b + 1, h:h + 1, i:i + 1].float().numpy(), ref, w, a, "bf16",
                  "full size key padding (%s): row (%d, %d, %d)" % (ws, b, h, i))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_skips_key_tiles_a_key_mask_hides(D, causal):
+    """With room for them after rot(K) in the workspace, a [B, Sk] mask's
+    per-entry key-tile counts are written there and the kernels skip the
+    tiles past each entry's last visible key.  Entries: all keys visible;
+    the first 130 (two tiles); none (zero tiles, an entry in the middle);
+    exactly the first tile; only the last key.  The skipping call, a call
+    with a workspace of rot(K)'s size only (no counts, every tile computed)
+    and the in-kernel key path give the same bits, and match the oracle."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, Sq, Sk = 5, 4, 2, 300, 700
+    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, "bf16", 71)
+    m = np.zeros((B, Sk), dtype=bool)
+    m[0] = True
+    m[1, :130] = True
+    m[3, :128] = True
+    m[4, Sk - 1] = True
+    c32, s32 = oracle_tables(1e4, D, Sk + 8)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    qg, kg, vg, mg = q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(m).cuda()
+    ws = R.attention_workspace(kg, mg)
+    kb = kg.numel() * kg.element_size()
+    assert ws.numel() == (kb + 15) // 16 * 16 + 4 * B
+    kw = dict(rotary_dim=D, causal=causal, attn_mask=mg)
+    skip = R.attention(qg, kg, vg, cg, sg, k_workspace=ws, **kw)
+    torch.cuda.synchronize()
+    tiles = ws[(kb + 15) // 16 * 16:].view(torch.int32).cpu().tolist()
+    assert tiles == [6, 2, 0, 1, 6]
+    full = R.attention(qg, kg, vg, cg, sg, k_workspace=torch.empty_like(kg), **kw)
+    inker = R.attention(qg, kg, vg, cg, sg, k_workspace=None, **kw)
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(skip.view(torch.int16), full.view(torch.int16))
+    assert torch.equal(skip.view(torch.int16), inker.view(torch.int16))
+    assert torch.count_nonzero(skip[2]) == 0
+    _check(skip, q, k, v, "bf16", D, O.SPLIT_HALF, c32, s32, None, None, causal,
+           "tile skipping D%d c%d" % (D, causal), attn_mask=m)
