@@ -81,7 +81,7 @@ constexpr long long kAttnWaitCycles = 4000000000LL;
 // [table_rows][rotary_dim / 2] fp32 (box: 32 values x 128 rows).  A box lands
 // as 128 rows of 128 bytes, the 16-byte chunk c of row r at chunk c ^ (r & 7).
 struct AttnMaps {
-    CUtensorMap k, v, cos, sin, q;
+    CUtensorMap k, v, cos, sin, q, o;             // o: rope_attn_2sm_kernel's output tiles
 };
 
 __device__ __forceinline__ uint32_t attn_smem_u32(const void *p)
@@ -883,6 +883,47 @@ __device__ __forceinline__ void store_o_row(uint32_t o_base, T *O, int64_t qi, i
     }
 }
 
+// Row r of a 128-row output block, as store_o_row computes it, into a
+// staging tile of two swizzled 128-byte boxes (features 0 .. 63, then
+// 64 .. 127) for a TMA store: in each 16-byte store of a warp, the rows r and
+// r + 8 share a bank group and the eight row residues fill all eight, the
+// fewest shared-memory wavefronts for 512 bytes.
+template <typename T>
+__device__ __forceinline__ void stage_o_row(uint32_t o_base, uint8_t *sO, int r, bool any_key,
+                                            float l_run)
+{
+    const float inv = (any_key && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+        float ov[32];
+        if (any_key) {
+            tmem_ld32(o_base + c0, ov);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ov[i] = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                f[e] = ov[c * 8 + e] * inv;
+            *reinterpret_cast<uint4 *>(sO + sw128(r, c0 / 8 + c)) = Elt<T>::pack(f);
+        }
+    }
+}
+
+// TMA store of one swizzled box from shared memory (bulk-group completion).
+// Rows past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y,
+                                             int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(map), "r"(attn_smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 template <typename T, int LAYOUT, int D, bool STAGED, bool MASK>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     rope_attn_kernel(const AttnArgs a, const __grid_constant__ AttnMaps maps, const int32_t pair_heads)
@@ -1530,6 +1571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     uint8_t *sQ = smem;
     uint8_t *sStages = sQ + kTile;
     uint8_t *sT = sStages + k2Stages * 2 * k2Half;     // the query tile's table rows
+    uint8_t *sO = sT + 4 * kBoxBytes;                  // the output block, staged for TMA
     auto sK = [&](int st) { return sStages + st * 2 * k2Half; };
     auto sV = [&](int st) { return sStages + st * 2 * k2Half + k2Half; };
     // both CTAs' key / value halves landed (leader only: TMA bytes of both);
@@ -1617,7 +1659,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             const int32_t hq = w.hq_first + (int32_t)rank * w.hq_step;
             const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
             const int64_t qi = q0 + tid;
-            T *O = static_cast<T *>(a.o) + ((w.b * a.Hq + hq) * a.Sq) * D;
             const int64_t n_tiles = w.n_tiles;     // the same in both CTAs
             float m_ref = -INFINITY, l_run = 0.0f;
             if (n_tiles > 0) {
@@ -1681,9 +1722,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ok)
                 break;
-            store_o_row<T, D>(o_base, O, qi, a.Sq, n_tiles > 0, l_run);
+            // O / l of the warp's 32 rows: staged in shared memory once the
+            // warp's store of the previous unit has read it, then one TMA
+            // store per 64 features (rows past Sq are not written)
+            if (lane == 0)
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+            stage_o_row<T>(o_base, sO, tid, n_tiles > 0, l_run);
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            const int64_t y0 = q0 + warp * 32;
+            if (lane == 0 && y0 < a.Sq) {
+                const int z = (int)(w.b * a.Hq + hq);
+                tma_store_3d(&maps.o, sO + warp * 32 * 128, 0, (int)y0, z);
+                tma_store_3d(&maps.o, sO + kBoxBytes + warp * 32 * 128, 64, (int)y0, z);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
         }
+        // the warp's last output stores have completed
+        if (lane == 0)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
         if (!ok)
             raise_abort();
     } else if (warp == k2SIssueWarp && leader) {
@@ -1938,10 +1998,12 @@ static bool encode_table(EncodeTiledFn enc, CUtensorMap *m, const float *base, i
 // of key and value tiles.  With D = 64 the request is raised so that one CTA
 // holds an SM (its 512 TMEM columns are the whole SM's).
 // rope_attn_2sm_kernel (D = 128): the query tile, three stages of a key
-// half and a value half, the query tile's table rows.
+// half and a value half, the query tile's table rows, the output block
+// (224 KB).
 static size_t attn_2sm_smem_bytes()
 {
-    return (size_t)kAttnRows * 128 * 2 + (size_t)k2Stages * 2 * k2Half + 4 * (size_t)kBoxBytes;
+    return (size_t)kAttnRows * 128 * 2 + (size_t)k2Stages * 2 * k2Half + 4 * (size_t)kBoxBytes +
+           (size_t)kAttnRows * 128 * 2;
 }
 
 static size_t attn_smem_bytes(int D, bool prerotated)
@@ -2091,7 +2153,8 @@ cudaError_t launch_attention_t(const AttnArgs &a, int32_t D, int32_t layout, int
         if (!encode_kv(enc, &maps.k, a.k_rot != nullptr ? a.k_rot : a.k, dt, heads, a.Sk, D,
                        two_sm ? 64u : (uint32_t)kAttnKeys) ||
             !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D) ||
-            (a.k_rot != nullptr && !encode_kv(enc, &maps.q, a.q, dt, a.B * a.Hq, a.Sq, D)))
+            (a.k_rot != nullptr && !encode_kv(enc, &maps.q, a.q, dt, a.B * a.Hq, a.Sq, D)) ||
+            (two_sm && !encode_kv(enc, &maps.o, a.o, dt, a.B * a.Hq, a.Sq, D, 32u)))
             return cudaErrorInvalidValue;
         // the table boxes: of the key tiles (keys rotated in the kernel) or
         // of the query tiles (keys rotated beforehand)
