@@ -1654,26 +1654,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         uint32_t sb = 0, s_ph = 0;                 // S buffer g mod 3 and its phase parity
         uint32_t ob = 0, o_ph = 0;                 // the same for tile g - 1 (O barriers)
         uint32_t qn = 0;                           // units with key tiles so far
-        for (int64_t L = cid; ok && L < n_units; L += clusters) {
-            const AttnWork w = unit_work(L);
-            const int32_t hq = w.hq_first + (int32_t)rank * w.hq_step;
-            const int64_t q0 = w.q0_first + (int64_t)rank * w.q_step;
-            const int64_t qi = q0 + tid;
-            const int64_t n_tiles = w.n_tiles;     // the same in both CTAs
+        // Pass L: the key tiles of unit L, then the query tile of unit
+        // L + clusters, then the epilogue of unit L.  The next unit's query
+        // tile is loaded once unit L's last S has finished; rotated before
+        // unit L's epilogue, it lets the next unit's first S products run
+        // while the epilogue waits for the last O += P V and stores O.  The
+        // first pass (L = cid - clusters) only rotates the first query tile.
+        for (int64_t L = cid - clusters; ok && L < n_units; L += clusters) {
+            const bool real = L >= cid;
+            const AttnWork w = unit_work(real ? L : cid);
+            const int64_t qi = w.q0_first + (int64_t)rank * w.q_step + tid;
+            const int64_t n_tiles = real ? w.n_tiles : 0;     // the same in both CTAs
             float m_ref = -INFINITY, l_run = 0.0f;
-            if (n_tiles > 0) {
-                ok = __all_sync(0xffffffffu, attn_wait(&bar_q, qn & 1u, abort));
-                if (!ok)
-                    break;
-                rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(sQ, sT, q0, a.pos_q, a.Sq, a, tid);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                // this warp's rows are rotated: one arrival per row warp of
-                // both CTAs on the leader's barrier (once per unit)
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_remote(peer_addr(&bar_qr, 0));
-                ++qn;
-            }
             for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
                 const uint32_t b = sb;
                 ok = __all_sync(0xffffffffu, attn_wait(&bar_s[b], s_ph, abort));
@@ -1716,6 +1708,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             }
             if (!ok)
                 break;
+            // the next unit's query tile, once it has landed: rotated in
+            // place, then one arrival per row warp of both CTAs on the
+            // leader's barrier
+            if (L + clusters < n_units && unit_work(L + clusters).n_tiles > 0) {
+                const AttnWork wn = unit_work(L + clusters);
+                ok = __all_sync(0xffffffffu, attn_wait(&bar_q, qn & 1u, abort));
+                if (!ok)
+                    break;
+                rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(
+                    sQ, sT, wn.q0_first + (int64_t)rank * wn.q_step, a.pos_q, a.Sq, a, tid);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_remote(peer_addr(&bar_qr, 0));
+                ++qn;
+            }
+            if (!real)
+                continue;
             // the unit's last O += P V (products finish in order), then O / l
             if (n_tiles > 0)
                 ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
@@ -1732,9 +1742,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            const int64_t y0 = q0 + warp * 32;
+            const AttnWork we = unit_work(L);     // recomputed: fewer values live across the rotation
+            const int64_t y0 = we.q0_first + (int64_t)rank * we.q_step + warp * 32;
             if (lane == 0 && y0 < a.Sq) {
-                const int z = (int)(w.b * a.Hq + hq);
+                const int z = (int)(we.b * a.Hq + we.hq_first + (int32_t)rank * we.hq_step);
                 tma_store_3d(&maps.o, sO + warp * 32 * 128, 0, (int)y0, z);
                 tma_store_3d(&maps.o, sO + kBoxBytes + warp * 32 * 128, 64, (int)y0, z);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
