@@ -884,17 +884,17 @@ __device__ __forceinline__ void store_o_row(uint32_t o_base, T *O, int64_t qi, i
 }
 
 // Row r of a 128-row output block, as store_o_row computes it, into a
-// staging tile of two swizzled 128-byte boxes (features 0 .. 63, then
+// staging tile of D / 64 swizzled 128-byte boxes (features 0 .. 63, then
 // 64 .. 127) for a TMA store: in each 16-byte store of a warp, the rows r and
 // r + 8 share a bank group and the eight row residues fill all eight, the
 // fewest shared-memory wavefronts for 512 bytes.
-template <typename T>
+template <typename T, int D>
 __device__ __forceinline__ void stage_o_row(uint32_t o_base, uint8_t *sO, int r, bool any_key,
                                             float l_run)
 {
     const float inv = (any_key && l_run > 0.0f) ? 1.0f / l_run : 0.0f;
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+    for (int c0 = 0; c0 < D; c0 += 32) {
         float ov[32];
         if (any_key) {
             tmem_ld32(o_base + c0, ov);
@@ -922,6 +922,49 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
                  ::"l"(map), "r"(attn_smem_u32(src)), "r"(x), "r"(y), "r"(z)
                  : "memory");
+}
+
+// Epilogue of one row warp (warp-collective): its 32 rows 32 wq .. 32 wq + 31
+// of a 128-row output block (row r of this thread) staged in the block's
+// 128 x D staging tile sO once the warp's previous store from it has read
+// it, then one TMA store per 64 features from lane 0 (a 64 x 32 box of map:
+// O as [B Hq][Sq][D]).  where(q0, z) gives the block's first query row and
+// its output head; it is called after the staging (fewer values live across
+// it).  Only the warp's own bulk group is waited for, so no warp waits on
+// another.
+template <typename T, int D, typename Where>
+__device__ __forceinline__ void store_o_warp(const CUtensorMap *map, uint32_t o_base, uint8_t *sO,
+                                             int r, int wq, int64_t Sq, bool any_key, float l_run,
+                                             const Where &where)
+{
+    const bool lead = (threadIdx.x & 31) == 0;
+    if (lead)
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    stage_o_row<T, D>(o_base, sO, r, any_key, l_run);
+    // O's columns are read (the caller's next tensor-core work may follow)
+    // and the staged rows are visible to the copy engine
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    int64_t q0;
+    int z;
+    where(q0, z);
+    const int64_t y0 = q0 + wq * 32;
+    if (lead && y0 < Sq) {
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_3d(map, sO + bx * kBoxBytes + wq * 32 * 128, bx * 64, (int)y0, z);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
+// Before a CTA ends: the warp's output stores have completed.
+__device__ __forceinline__ void drain_o_stores()
+{
+    if ((threadIdx.x & 31) == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
 }
 
 template <typename T, int LAYOUT, int D, bool STAGED, bool MASK>
@@ -1034,9 +1077,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ok) {
             *abort = 1;
+        } else if (n_tiles > 0) {
+            // epilogue: O / l of the warp's rows, staged in the block's query
+            // tile (no S product reads it any more) and stored by TMA
+            store_o_warp<T, D>(&maps.o, acc_base + kAttnKeys, sQ + j * kTile, row, wq, a.Sq, true,
+                               l_run, [&](int64_t &q0r, int &z) {
+                                   q0r = q0;
+                                   z = (int)(w.b * a.Hq + hq);
+                               });
+            drain_o_stores();
         } else {
-            // epilogue: O / l for this row
-            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, n_tiles > 0, l_run);
+            // no key tile (nor, without keys, a tensor map): zeros
+            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, false, l_run);
         }
     } else {
         // ---- issue warp: TMA copies one tile ahead, the MMAs (lane 0)
@@ -1323,10 +1375,20 @@ __global__ void __launch_bounds__(kPpThreads, 1)
             ok = __all_sync(0xffffffffu,
                             attn_wait(&bar_o[j], (uint32_t)((n_tiles - 1) & 1), abort));
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!ok)
+        if (!ok) {
             *abort = 1;
-        else
-            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, n_tiles > 0, l_run);
+        } else if (n_tiles > 0) {
+            // O / l of the warp's rows, staged in the block's query tile (no
+            // S product reads it any more) and stored by TMA
+            store_o_warp<T, D>(&maps.o, acc_base + kAttnKeys, sQ + j * kTile, row, wq, a.Sq, true,
+                               l_run, [&](int64_t &q0r, int &z) {
+                                   q0r = q0;
+                                   z = (int)(w.b * a.Hq + hq);
+                               });
+            drain_o_stores();
+        } else {
+            store_o_row<T, D>(acc_base + kAttnKeys, O, qi, a.Sq, false, l_run);
+        }
     } else if (warp < kPpTmaWarp) {
         // ---- MMA issue of row block jb (lane 0 issues; the waits are warp-wide)
         const int jb = warp - kPpMmaWarp;
@@ -1735,10 +1797,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             // O / l of the warp's 32 rows: staged in shared memory once the
             // warp's store of the previous unit has read it, then one TMA
             // store per 64 features (rows past Sq are not written)
+            // (store_o_warp's steps, written out: this kernel's register
+            // allocation spills more with the shared helper)
             if (lane == 0)
                 asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
-            stage_o_row<T>(o_base, sO, tid, n_tiles > 0, l_run);
+            stage_o_row<T, D>(o_base, sO, tid, n_tiles > 0, l_run);
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
@@ -1751,10 +1815,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
         }
-        // the warp's last output stores have completed
-        if (lane == 0)
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        __syncwarp();
+        drain_o_stores();
         if (!ok)
             raise_abort();
     } else if (warp == k2SIssueWarp && leader) {
@@ -2165,7 +2226,7 @@ cudaError_t launch_attention_t(const AttnArgs &a, int32_t D, int32_t layout, int
                        two_sm ? 64u : (uint32_t)kAttnKeys) ||
             !encode_kv(enc, &maps.v, a.v, dt, heads, a.Sk, D) ||
             (a.k_rot != nullptr && !encode_kv(enc, &maps.q, a.q, dt, a.B * a.Hq, a.Sq, D)) ||
-            (two_sm && !encode_kv(enc, &maps.o, a.o, dt, a.B * a.Hq, a.Sq, D, 32u)))
+            !encode_kv(enc, &maps.o, a.o, dt, a.B * a.Hq, a.Sq, D, 32u))
             return cudaErrorInvalidValue;
         // the table boxes: of the key tiles (keys rotated in the kernel) or
         // of the query tiles (keys rotated beforehand)
