@@ -680,15 +680,18 @@ def attention_arm(args):
     inkernel = {"ms": round(ims, 4), "tflops": round(flops_of(a) / (ims * 1e-3) / 1e12, 1),
                 "what": "k_workspace=None: each CTA rotates its key tiles (rope_attn_kernel)"}
 
-    # context: the same call with an attn_mask -- all keys visible (the cost of
-    # the masked kernel instance), and key padding (batch entry b keeps its
-    # first S - 512 b keys)
+    # context: the same call with an attn_mask -- all keys visible and key
+    # padding (batch entry b keeps its first S - 512 b keys), both prefixes of
+    # the keys, and a mask that hides a seeded ~10 % of the keys everywhere
+    # (not a prefix: the kernel reads its bytes)
     masked = {}
+    gm = torch.Generator(device=device).manual_seed(12)
     for label, m in (("all_visible", torch.ones((a["B"], a["S"]), dtype=torch.bool,
                                                 device=device)),
                      ("key_padding", torch.arange(a["S"], device=device)[None, :] <
-                      (a["S"] - 512 * torch.arange(a["B"], device=device))[:, None])):
-        mws = R.attention_workspace(k, m)   # rot(K), then the mask's key-tile counts
+                      (a["S"] - 512 * torch.arange(a["B"], device=device))[:, None]),
+                     ("scattered", torch.rand((a["B"], a["S"]), generator=gm, device=device) > 0.1)):
+        mws = R.attention_workspace(k, m)   # rot(K), the key-tile counts, the prefix lengths
 
         def mstep(m=m, mws=mws):
             R.attention(q, k, v, cos, sin, rotary_dim=a["rotary_dim"], causal=a["causal"], out=o,
@@ -706,8 +709,10 @@ def attention_arm(args):
         masked[label] = {"ms": round(mms, 4), "tflops_of_unmasked_flops":
                          round(flops_of(a) / (mms * 1e-3) / 1e12, 1)}
     masked["what"] = ("rope_attention_fwd_masked, workspace path with the mask's key-tile "
-                      "counts, [B, Sk] mask: all keys visible, or batch entry b keeping its first "
-                      "S - 512 b keys (the key tiles past them skipped)")
+                      "counts and prefix lengths, [B, Sk] mask: all keys visible, or batch entry b "
+                      "keeping its first S - 512 b keys (the key tiles past them skipped; both "
+                      "prefixes, computed without reading the mask), or ~10 % of the keys hidden "
+                      "at random (mask bytes read per key tile)")
 
     # context: the same result from the unfused path (rotation kernel, then
     # torch's scaled_dot_product_attention on the rotated tensors)

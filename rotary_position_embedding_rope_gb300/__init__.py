@@ -540,11 +540,13 @@ def rope_attention_fwd_noalloc(q, k, v, o, cos, sin, pos_q, pos_k, B, Hq, Hk, Sq
 def attention_workspace(k: torch.Tensor, attn_mask: torch.Tensor | None = None) -> torch.Tensor:
     """A key workspace for rope_attention_fwd(_masked) on keys like k: rot(K)
     and, for a [B, Sk] attn_mask, the per-batch key-tile counts after it (with
-    them the kernels skip the key tiles the mask hides entirely)."""
+    them the kernels skip the key tiles the mask hides entirely), then the
+    per-batch prefix lengths (an entry whose mask shows exactly its first L
+    keys, as padding does, is then computed without reading the mask)."""
     kb = k.numel() * k.element_size()
     n = kb
     if attn_mask is not None and attn_mask.dim() == 2:
-        n = (kb + 15) // 16 * 16 + 4 * k.shape[0]
+        n = (kb + 15) // 16 * 16 + 8 * k.shape[0]
     return torch.empty(n, dtype=torch.uint8, device=k.device)
 
 

@@ -61,10 +61,14 @@ __global__ void take_flag_kernel(int32_t *flag, int32_t *taken)
 // Key tiles of 128 up to the last visible key of each batch entry of a
 // [B, Sk] attn_mask: one CTA per entry; each thread scans its keys from the
 // end down and stops at its first visible one, then the CTA takes the max.
+// With lens: also the entry's prefix length, L when the mask shows exactly
+// the keys [0, L) (its first hidden key comes after its last visible one:
+// padding), else -1; each thread scans its keys from the start up to its
+// first hidden one, then the CTA takes the min.
 constexpr int kMaskTileKeys = 128;         // the attention kernels' key tile
-__global__ void mask_tiles_kernel(const uint8_t *mask, int64_t Sk, int32_t *tiles)
+__global__ void mask_tiles_kernel(const uint8_t *mask, int64_t Sk, int32_t *tiles, int32_t *lens)
 {
-    __shared__ int32_t warp_last[8];
+    __shared__ int32_t warp_last[8], warp_first[8];
     const uint8_t *row = mask + (int64_t)blockIdx.x * Sk;
     int32_t last = -1;
     for (int64_t i = Sk - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
@@ -73,22 +77,38 @@ __global__ void mask_tiles_kernel(const uint8_t *mask, int64_t Sk, int32_t *tile
             break;
         }
     }
+    int32_t first = (int32_t)Sk;               // first hidden key (Sk: none)
+    if (lens != nullptr) {
+        for (int64_t i = threadIdx.x; i < Sk; i += blockDim.x) {
+            if (row[i] == 0) {
+                first = (int32_t)i;
+                break;
+            }
+        }
+    }
     last = __reduce_max_sync(0xffffffffu, last);
-    if ((threadIdx.x & 31) == 0)
+    first = __reduce_min_sync(0xffffffffu, first);
+    if ((threadIdx.x & 31) == 0) {
         warp_last[threadIdx.x >> 5] = last;
+        warp_first[threadIdx.x >> 5] = first;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        int32_t m = -1;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+        int32_t m = -1, f = (int32_t)Sk;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
             m = warp_last[w] > m ? warp_last[w] : m;
+            f = warp_first[w] < f ? warp_first[w] : f;
+        }
         tiles[blockIdx.x] = m < 0 ? 0 : m / kMaskTileKeys + 1;
+        if (lens != nullptr)
+            lens[blockIdx.x] = f > m ? m + 1 : -1;
     }
 }
 
 cudaError_t launch_mask_tiles(const uint8_t *mask, int64_t B, int64_t Sk, int32_t *tiles,
-                              cudaStream_t st)
+                              int32_t *lens, cudaStream_t st)
 {
-    mask_tiles_kernel<<<(unsigned)B, 256, 0, st>>>(mask, Sk, tiles);
+    mask_tiles_kernel<<<(unsigned)B, 256, 0, st>>>(mask, Sk, tiles, lens);
     return cudaGetLastError();
 }
 
@@ -482,14 +502,18 @@ struct AttnCall {
 
 // Bytes of the key workspace a call uses: rot(K) (kb bytes); with a [B, Sk]
 // mask and room for them, then B int32 key-tile counts from the first
-// 16-byte boundary after rot(K).
+// 16-byte boundary after rot(K), and with room for them too, B int32 prefix
+// lengths right after the counts.
 static int64_t mask_tiles_offset(int64_t kb) { return (kb + 15) / 16 * 16; }
 
 static int64_t workspace_extent(const AttnCall &c, int64_t kb)
 {
+    if (c.mask_kind != ROPE_MASK_KEYS || c.Sk > 0x7fffffffLL || c.B > 0x7fffffffLL)
+        return kb;
     const int64_t tiles_end = mask_tiles_offset(kb) + 4 * c.B;
-    if (c.mask_kind == ROPE_MASK_KEYS && c.Sk <= 0x7fffffffLL && c.B <= 0x7fffffffLL &&
-        c.workspace_bytes >= tiles_end)
+    if (c.workspace_bytes >= tiles_end + 4 * c.B)
+        return tiles_end + 4 * c.B;
+    if (c.workspace_bytes >= tiles_end)
         return tiles_end;
     return kb;
 }
@@ -596,14 +620,18 @@ static rope_status attention_call(const AttnCall &c, void *stream)
         const rope_status s = apply_call(r, stream);
         if (s != ROPE_OK)
             return s;
-        // a [B, Sk] mask: the key tiles each batch entry shows, after rot(K)
-        if (a.mask_kind == ROPE_MASK_KEYS && workspace_extent(c, kb) > kb) {
+        // a [B, Sk] mask: the key tiles each batch entry shows, after rot(K),
+        // then (room permitting) the entries' prefix lengths
+        const int64_t used = workspace_extent(c, kb);
+        if (a.mask_kind == ROPE_MASK_KEYS && used > kb) {
             int32_t *tiles = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) +
                                                          mask_tiles_offset(kb));
-            if (launch_mask_tiles(c.mask, c.B, c.Sk, tiles, static_cast<cudaStream_t>(stream)) !=
-                cudaSuccess)
+            int32_t *lens = used > mask_tiles_offset(kb) + 4 * c.B ? tiles + c.B : nullptr;
+            if (launch_mask_tiles(c.mask, c.B, c.Sk, tiles, lens,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
                 return ROPE_ERR_CUDA;
             a.kv_tiles = tiles;
+            a.kv_len = lens;
         }
     }
     return launch_attention(a, c.D, c.layout, c.dtype, static_cast<cudaStream_t>(stream)) ==

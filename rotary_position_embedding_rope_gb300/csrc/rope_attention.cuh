@@ -738,14 +738,17 @@ __device__ __forceinline__ void mask_bits(const AttnArgs &a, int64_t b, int64_t 
     }
 }
 
+// sk: keys the row may see at most (a [B, Sk] mask that shows a prefix of
+// the keys), -1: all Sk.
 template <typename T, int D, bool PACKED, bool MASK, typename OReady = ONoWait>
 __device__ __forceinline__ void softmax_tile(uint32_t acc_base, uint32_t o_base, int64_t qi,
                                              int64_t k0, int64_t shift, const AttnArgs &a,
                                              int64_t b, bool not_first, float &m_ref,
-                                             float &l_run, const OReady &o_ready = OReady())
+                                             float &l_run, const OReady &o_ready = OReady(),
+                                             int64_t sk = -1)
 {
     // columns of this tile visible to this row: [0, nvis)
-    int64_t vis_end = a.Sk;                // first invisible key
+    int64_t vis_end = sk >= 0 ? sk : a.Sk;   // first invisible key
     if (a.causal && qi + shift + 1 < vis_end)
         vis_end = qi + shift + 1;
     const int64_t nv = vis_end - k0;
@@ -1728,6 +1731,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             const int64_t qi = w.q0_first + (int64_t)rank * w.q_step + tid;
             const int64_t n_tiles = real ? w.n_tiles : 0;     // the same in both CTAs
             float m_ref = -INFINITY, l_run = 0.0f;
+            // the key tiles; M: the softmax reads the attn_mask's bytes, else
+            // the row sees at most the first sk keys (-1: all)
+            auto key_tiles = [&](auto m_tag, int64_t sk) {
+            constexpr bool M = decltype(m_tag)::value;
             for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
                 const uint32_t b = sb;
                 ok = __all_sync(0xffffffffu, attn_wait(&bar_s[b], s_ph, abort));
@@ -1743,9 +1750,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                     o_ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
                     return o_ok;
                 };
-                softmax_tile<T, D, true, MASK>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
-                                         kt * kAttnKeys, shift, a, w.b, kt > 0, m_ref, l_run,
-                                         o_ready);
+                softmax_tile<T, D, true, M>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
+                                      kt * kAttnKeys, shift, a, w.b, kt > 0, m_ref, l_run, o_ready,
+                                      sk);
                 ok = o_ok;
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1768,6 +1775,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 if (!ok)
                     break;
             }
+            };
+            if constexpr (MASK) {
+                // a [B, Sk] mask that shows exactly the keys [0, L) of this
+                // batch entry (padding): the unmasked softmax over L keys
+                const int64_t len = real && a.kv_len != nullptr ? __ldg(a.kv_len + w.b) : -1;
+                if (len >= 0)
+                    key_tiles(std::false_type(), len);
+                else
+                    key_tiles(std::true_type(), (int64_t)-1);
+            } else {
+                key_tiles(std::false_type(), (int64_t)-1);
+            }
             if (!ok)
                 break;
             // the next unit's query tile, once it has landed: rotated in
@@ -1778,7 +1797,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
                 ok = __all_sync(0xffffffffu, attn_wait(&bar_q, qn & 1u, abort));
                 if (!ok)
                     break;
-                rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(
+                // items in flight per thread: 2 (1 in the masked kernel),
+                // which frees the registers the tile loop needs (4 spilled
+                // and measured 5 % slower)
+                rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, MASK ? 1 : 2>(
                     sQ, sT, wn.q0_first + (int64_t)rank * wn.q_step, a.pos_q, a.Sq, a, tid);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();

@@ -114,10 +114,13 @@ struct AttnArgs {
     int32_t mask_vec16;              // kind 2: rows 16-byte aligned (read as vectors)
     const int32_t *kv_tiles;         // [B]: key tiles up to the last key a [B, Sk] mask
                                      // shows (0: none), or nullptr (no skipping)
+    const int32_t *kv_len;           // [B]: L when a [B, Sk] mask shows exactly the keys
+                                     // [0, L), else -1; or nullptr
 };
-// Writes kv_tiles for a [B, Sk] attn_mask (rope_api.cu).
+// Writes kv_tiles, and kv_len when lens is not null, for a [B, Sk]
+// attn_mask (rope_api.cu).
 cudaError_t launch_mask_tiles(const uint8_t *mask, int64_t B, int64_t Sk, int32_t *tiles,
-                              cudaStream_t st);
+                              int32_t *lens, cudaStream_t st);
 cudaError_t launch_attention(const AttnArgs &a, int32_t D, int32_t layout, int32_t dtype,
                              cudaStream_t st);
 // The same for calls with an attn_mask (rope_attention_masked.cu).

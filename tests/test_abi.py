@@ -335,3 +335,7 @@ def test_masked_attention_workspace_with_key_tiles(lib):
     # o instead, which is refused either way
     assert lib.rope_attention_fwd_masked(*masked_args(mask=A16 * 300, kind=2, ws=ws,
                                                       ws_bytes=used)) == R.ROPE_ERR_INVALID_ARG
+    # with room for the prefix lengths too (4 bytes per entry), the extent
+    # grows by them: a mask right after the counts now overlaps
+    assert lib.rope_attention_fwd_masked(*masked_args(mask=ws + used, kind=1, ws=ws,
+                                                      ws_bytes=used + 4)) == R.ROPE_ERR_INVALID_ARG

@@ -470,9 +470,12 @@ def test_attention_skips_key_tiles_a_key_mask_hides(D, causal):
     per-entry key-tile counts are written there and the kernels skip the
     tiles past each entry's last visible key.  Entries: all keys visible;
     the first 130 (two tiles); none (zero tiles, an entry in the middle);
-    exactly the first tile; only the last key.  The skipping call, a call
-    with a workspace of rot(K)'s size only (no counts, every tile computed)
-    and the in-kernel key path give the same bits, and match the oracle."""
+    exactly the first tile; only the last key.  After the counts come the
+    entries' prefix lengths (-1 for the last entry, whose mask is not a
+    prefix).  The call with both, one with room for the counts only (every
+    mask byte read), one with a workspace of rot(K)'s size only (no counts,
+    every tile computed) and the in-kernel key path give the same bits, and
+    match the oracle."""
     require_gpu()
     R = lib()
     B, Hq, Hk, Sq, Sk = 5, 4, 2, 300, 700
@@ -487,16 +490,20 @@ def test_attention_skips_key_tiles_a_key_mask_hides(D, causal):
     qg, kg, vg, mg = q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(m).cuda()
     ws = R.attention_workspace(kg, mg)
     kb = kg.numel() * kg.element_size()
-    assert ws.numel() == (kb + 15) // 16 * 16 + 4 * B
+    w0 = (kb + 15) // 16 * 16
+    assert ws.numel() == w0 + 8 * B
     kw = dict(rotary_dim=D, causal=causal, attn_mask=mg)
     skip = R.attention(qg, kg, vg, cg, sg, k_workspace=ws, **kw)
     torch.cuda.synchronize()
-    tiles = ws[(kb + 15) // 16 * 16:].view(torch.int32).cpu().tolist()
+    tiles = ws[w0:w0 + 4 * B].view(torch.int32).cpu().tolist()
     assert tiles == [6, 2, 0, 1, 6]
+    assert ws[w0 + 4 * B:].view(torch.int32).cpu().tolist() == [Sk, 130, 0, 128, -1]
+    counts = R.attention(qg, kg, vg, cg, sg, k_workspace=ws[:w0 + 4 * B].clone(), **kw)
     full = R.attention(qg, kg, vg, cg, sg, k_workspace=torch.empty_like(kg), **kw)
     inker = R.attention(qg, kg, vg, cg, sg, k_workspace=None, **kw)
     assert R.rope_check_errors() == R.ROPE_OK
     assert torch.equal(skip.view(torch.int16), full.view(torch.int16))
+    assert torch.equal(skip.view(torch.int16), counts.view(torch.int16))
     assert torch.equal(skip.view(torch.int16), inker.view(torch.int16))
     assert torch.count_nonzero(skip[2]) == 0
     _check(skip, q, k, v, "bf16", D, O.SPLIT_HALF, c32, s32, None, None, causal,
