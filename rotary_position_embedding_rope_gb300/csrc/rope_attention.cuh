@@ -1334,7 +1334,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
     if (math) {
         q_ok = __all_sync(0xffffffffu, attn_wait(&bar_q, 0u));
         if (q_ok)
-            rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 4>(sQ + j * kTile, sK(1), q0, a.pos_q,
+            rotate_tile<T, LAYOUT, STAGED_Q, kAttnRows, 1>(sQ + j * kTile, sK(1), q0, a.pos_q,
                                                            a.Sq, a, row);
         else
             abort_flag = 1;
@@ -1351,6 +1351,10 @@ __global__ void __launch_bounds__(kPpThreads, 1)
         // ---- row-block warps: the softmax of row qi, tile after tile
         const uint32_t acc_base = tmem + (uint32_t)j * kBlockCols + ((uint32_t)(wq * 32) << 16);
         float m_ref = -INFINITY, l_run = 0.0f;
+        // the key tiles; M: the softmax reads the attn_mask's bytes, else the
+        // row sees at most the first sk keys (-1: all)
+        auto key_tiles = [&](auto m_tag, int64_t sk) {
+        constexpr bool M = decltype(m_tag)::value;
         for (int64_t kt = 0; kt < n_tiles; ++kt) {
             // S of this block is ready (its previous O += P V has finished:
             // the issuer waited for it before issuing S), and it is this
@@ -1366,12 +1370,24 @@ __global__ void __launch_bounds__(kPpThreads, 1)
             if (!ok)
                 break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            softmax_tile<T, D, true, MASK>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
-                                     w.b, kt > 0, m_ref, l_run);
+            softmax_tile<T, D, true, M>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
+                                  w.b, kt > 0, m_ref, l_run, ONoWait(), sk);
             mbar_arrive(&bar_sm[j]);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&bar_p[j]);
+        }
+        };
+        if constexpr (MASK) {
+            // a [B, Sk] mask that shows exactly the keys [0, L) of this batch
+            // entry (padding): the unmasked softmax over L keys
+            const int64_t len = a.kv_len != nullptr ? __ldg(a.kv_len + w.b) : -1;
+            if (len >= 0)
+                key_tiles(std::false_type(), len);
+            else
+                key_tiles(std::true_type(), (int64_t)-1);
+        } else {
+            key_tiles(std::false_type(), (int64_t)-1);
         }
         // the last O += P V
         if (ok && n_tiles > 0)
