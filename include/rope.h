@@ -285,9 +285,9 @@ rope_status rope_attention_fwd(const void *q, const void *k, const void *v, void
  *    computed.
  * Padding: with at least W + 8 B bytes, the call also writes (from byte
  *    W + 4 B) each entry's prefix length, L when its mask shows exactly the
- *    keys [0, L), else -1; the D = 128 kernel then computes such an entry
- *    as an unmasked one with L keys, without reading its mask (the same
- *    bits).
+ *    keys [0, L), else -1; the attention kernels of the workspace path
+ *    then compute such an entry as an unmasked one with L keys, without
+ *    reading its mask (the same bits).
  * Everything else as rope_attention_fwd.
  * Errors: as rope_attention_fwd; also ROPE_ERR_UNSUPPORTED for a mask_kind
  *    outside the enum and ROPE_ERR_INVALID_ARG for a NULL mask (with Sk > 0)
