@@ -59,32 +59,36 @@ __global__ void take_flag_kernel(int32_t *flag, int32_t *taken)
 }
 
 // Key tiles of 128 up to the last visible key of each batch entry of a
-// [B, Sk] attn_mask: one CTA per entry; each thread scans its keys from the
-// end down and stops at its first visible one, then the CTA takes the max.
-// With lens: also the entry's prefix length, L when the mask shows exactly
-// the keys [0, L) (its first hidden key comes after its last visible one:
-// padding), else -1; each thread scans its keys from the start up to its
-// first hidden one, then the CTA takes the min.
+// [B, Sk] attn_mask, and (lens not null) the entry's prefix length: L when
+// the mask shows exactly the keys [0, L) (its first hidden key comes after
+// its last visible one: padding), else -1.  One CTA per entry reads the
+// whole row once, 16 bytes per load when the row is 16-byte aligned, with no
+// early exit (so the loads do not wait on one another), keeping the last
+// visible and the first hidden key; the CTA then takes the max and the min.
 constexpr int kMaskTileKeys = 128;         // the attention kernels' key tile
 __global__ void mask_tiles_kernel(const uint8_t *mask, int64_t Sk, int32_t *tiles, int32_t *lens)
 {
     __shared__ int32_t warp_last[8], warp_first[8];
     const uint8_t *row = mask + (int64_t)blockIdx.x * Sk;
-    int32_t last = -1;
-    for (int64_t i = Sk - 1 - threadIdx.x; i >= 0; i -= blockDim.x) {
-        if (row[i] != 0) {
-            last = (int32_t)i;
-            break;
+    int32_t last = -1, first = (int32_t)Sk;    // last visible, first hidden key
+    const int64_t nvec = (reinterpret_cast<uintptr_t>(row) & 15) == 0 ? Sk / 16 : 0;
+    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row) + c);
+        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int32_t i = (int32_t)(c * 16 + e);
+            if ((wd[e >> 2] >> (8 * (e & 3))) & 0xFFu)
+                last = i;                      // increasing i: the last one wins
+            else
+                first = first < i ? first : i;
         }
     }
-    int32_t first = (int32_t)Sk;               // first hidden key (Sk: none)
-    if (lens != nullptr) {
-        for (int64_t i = threadIdx.x; i < Sk; i += blockDim.x) {
-            if (row[i] == 0) {
-                first = (int32_t)i;
-                break;
-            }
-        }
+    for (int64_t i = nvec * 16 + threadIdx.x; i < Sk; i += blockDim.x) {
+        if (row[i] != 0)
+            last = (int32_t)i;
+        else
+            first = first < (int32_t)i ? first : (int32_t)i;
     }
     last = __reduce_max_sync(0xffffffffu, last);
     first = __reduce_min_sync(0xffffffffu, first);

@@ -508,3 +508,41 @@ def test_attention_skips_key_tiles_a_key_mask_hides(D, causal):
     assert torch.count_nonzero(skip[2]) == 0
     _check(skip, q, k, v, "bf16", D, O.SPLIT_HALF, c32, s32, None, None, causal,
            "tile skipping D%d c%d" % (D, causal), attn_mask=m)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_key_mask_prefix_lengths(D):
+    """Prefix lengths of a [B, Sk] mask whose rows are 16-byte aligned (Sk =
+    1024: read 16 bytes at a time): all keys visible (1024); the first 1000
+    (1000, the first hidden key in another 16-byte chunk than the last
+    visible one); the first 1000 and key 1020 (not a prefix: -1); all but
+    key 5 (-1).  Entries with a length are computed without reading their
+    mask: the same bits as the call that reads every byte (room for the
+    counts only) and as the in-kernel key path, and the oracle's result."""
+    require_gpu()
+    R = lib()
+    B, Hq, Hk, Sq, Sk = 4, 4, 2, 200, 1024
+    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, "bf16", 79)
+    m = np.ones((B, Sk), dtype=bool)
+    m[1, 1000:] = False
+    m[2, 1000:] = False
+    m[2, 1020] = True
+    m[3, 5] = False
+    c32, s32 = oracle_tables(1e4, D, Sk + 8)
+    cg, sg = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    qg, kg, vg, mg = q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(m).cuda()
+    ws = R.attention_workspace(kg, mg)
+    kb = kg.numel() * kg.element_size()
+    w0 = (kb + 15) // 16 * 16
+    kw = dict(rotary_dim=D, causal=False, attn_mask=mg)
+    got = R.attention(qg, kg, vg, cg, sg, k_workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert ws[w0:w0 + 4 * B].view(torch.int32).cpu().tolist() == [8, 8, 8, 8]
+    assert ws[w0 + 4 * B:].view(torch.int32).cpu().tolist() == [1024, 1000, -1, -1]
+    counts = R.attention(qg, kg, vg, cg, sg, k_workspace=ws[:w0 + 4 * B].clone(), **kw)
+    inker = R.attention(qg, kg, vg, cg, sg, k_workspace=None, **kw)
+    assert R.rope_check_errors() == R.ROPE_OK
+    assert torch.equal(got.view(torch.int16), counts.view(torch.int16))
+    assert torch.equal(got.view(torch.int16), inker.view(torch.int16))
+    _check(got, q, k, v, "bf16", D, O.SPLIT_HALF, c32, s32, None, None, False,
+           "prefix lengths D%d" % D, attn_mask=m)
