@@ -1354,29 +1354,29 @@ __global__ void __launch_bounds__(kPpThreads, 1)
         // the key tiles; M: the softmax reads the attn_mask's bytes, else the
         // row sees at most the first sk keys (-1: all)
         auto key_tiles = [&](auto m_tag, int64_t sk) {
-        constexpr bool M = decltype(m_tag)::value;
-        for (int64_t kt = 0; kt < n_tiles; ++kt) {
-            // S of this block is ready (its previous O += P V has finished:
-            // the issuer waited for it before issuing S), and it is this
-            // block's turn: the softmax steps alternate between the blocks
-            // (block 0 on tile kt after block 1 on tile kt - 1, block 1 after
-            // block 0 on the same tile), so each has the exponential unit to
-            // itself while the tensor cores run the other block's products
-            ok = __all_sync(0xffffffffu,
-                            attn_wait(&bar_s[j], (uint32_t)(kt & 1), abort) &&
-                                (j == 0 ? kt == 0 || attn_wait(&bar_sm[1], (uint32_t)((kt - 1) & 1),
-                                                               abort)
-                                        : attn_wait(&bar_sm[0], (uint32_t)(kt & 1), abort)));
-            if (!ok)
-                break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            softmax_tile<T, D, true, M>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
-                                  w.b, kt > 0, m_ref, l_run, ONoWait(), sk);
-            mbar_arrive(&bar_sm[j]);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&bar_p[j]);
-        }
+            constexpr bool M = decltype(m_tag)::value;
+            for (int64_t kt = 0; kt < n_tiles; ++kt) {
+                // S of this block is ready (its previous O += P V has finished:
+                // the issuer waited for it before issuing S), and it is this
+                // block's turn: the softmax steps alternate between the blocks
+                // (block 0 on tile kt after block 1 on tile kt - 1, block 1 after
+                // block 0 on the same tile), so each has the exponential unit to
+                // itself while the tensor cores run the other block's products
+                ok = __all_sync(0xffffffffu,
+                                attn_wait(&bar_s[j], (uint32_t)(kt & 1), abort) &&
+                                    (j == 0 ? kt == 0 || attn_wait(&bar_sm[1], (uint32_t)((kt - 1) & 1),
+                                                                   abort)
+                                            : attn_wait(&bar_sm[0], (uint32_t)(kt & 1), abort)));
+                if (!ok)
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                softmax_tile<T, D, true, M>(acc_base, acc_base + kAttnKeys, qi, kt * kAttnKeys, shift, a,
+                                      w.b, kt > 0, m_ref, l_run, ONoWait(), sk);
+                mbar_arrive(&bar_sm[j]);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                mbar_arrive(&bar_p[j]);
+            }
         };
         if constexpr (MASK) {
             // a [B, Sk] mask that shows exactly the keys [0, L) of this batch
@@ -1750,47 +1750,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
             // the key tiles; M: the softmax reads the attn_mask's bytes, else
             // the row sees at most the first sk keys (-1: all)
             auto key_tiles = [&](auto m_tag, int64_t sk) {
-            constexpr bool M = decltype(m_tag)::value;
-            for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
-                const uint32_t b = sb;
-                ok = __all_sync(0xffffffffu, attn_wait(&bar_s[b], s_ph, abort));
-                if (!ok)
-                    break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                // O may still be updated by the products of tiles g - 2 and
-                // g - 1 (that of g - 3 had finished before S(g) was issued): a
-                // rescale waits for the later one, which finishes after the
-                // earlier (rare: the row max moved by more than 8)
-                bool o_ok = true;
-                auto o_ready = [&]() {
-                    o_ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
-                    return o_ok;
-                };
-                softmax_tile<T, D, true, M>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
-                                      kt * kAttnKeys, shift, a, w.b, kt > 0, m_ref, l_run, o_ready,
-                                      sk);
-                ok = o_ok;
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                // this warp's P rows are in TMEM: one arrival per row warp of
-                // both CTAs on the leader's barrier
-                __syncwarp();
-                if (lane == 0) {
-                    if (leader)
-                        mbar_arrive(&bar_p[b]);
-                    else
-                        mbar_arrive_remote(peer_addr(&bar_p[b], 0));
+                constexpr bool M = decltype(m_tag)::value;
+                for (int64_t kt = 0; kt < n_tiles; ++kt, ++g) {
+                    const uint32_t b = sb;
+                    ok = __all_sync(0xffffffffu, attn_wait(&bar_s[b], s_ph, abort));
+                    if (!ok)
+                        break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    // O may still be updated by the products of tiles g - 2 and
+                    // g - 1 (that of g - 3 had finished before S(g) was issued): a
+                    // rescale waits for the later one, which finishes after the
+                    // earlier (rare: the row max moved by more than 8)
+                    bool o_ok = true;
+                    auto o_ready = [&]() {
+                        o_ok = __all_sync(0xffffffffu, attn_wait(&bar_o[ob], o_ph, abort));
+                        return o_ok;
+                    };
+                    softmax_tile<T, D, true, M>(tmem + (uint32_t)b * kAttnKeys + lanes, o_base, qi,
+                                          kt * kAttnKeys, shift, a, w.b, kt > 0, m_ref, l_run, o_ready,
+                                          sk);
+                    ok = o_ok;
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    // this warp's P rows are in TMEM: one arrival per row warp of
+                    // both CTAs on the leader's barrier
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(&bar_p[b]);
+                        else
+                            mbar_arrive_remote(peer_addr(&bar_p[b], 0));
+                    }
+                    // tile g becomes the "previous" tile; advance to g + 1
+                    ob = sb;
+                    o_ph = s_ph;
+                    if (++sb == k2SBufs) {
+                        sb = 0;
+                        s_ph ^= 1u;
+                    }
+                    if (!ok)
+                        break;
                 }
-                // tile g becomes the "previous" tile; advance to g + 1
-                ob = sb;
-                o_ph = s_ph;
-                if (++sb == k2SBufs) {
-                    sb = 0;
-                    s_ph ^= 1u;
-                }
-                if (!ok)
-                    break;
-            }
             };
             if constexpr (MASK) {
                 // a [B, Sk] mask that shows exactly the keys [0, L) of this
