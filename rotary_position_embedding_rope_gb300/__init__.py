@@ -71,7 +71,10 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIBRARY
+    """lib/librope.so, or the library ROPE_LIBRARY names (a build of the same
+    sources with other compile-time settings, made with
+    ``_build.build(extra_flags=[...], output=...)``, for timing variants)."""
+    return os.environ.get("ROPE_LIBRARY") or _build.LIBRARY
 
 
 def load_library() -> ctypes.CDLL:
