@@ -219,7 +219,10 @@ KERNEL_NAMES = {2: "rope_scalar_kernel", 3: "rope_vec_kernel"}
 
 def profiled_traffic(kernel: str, workload: str, sources=None):
     """DRAM bytes per launch of a kernel from a committed ncu summary, or None
-    when there is none or the kernel sources changed since."""
+    when there is none, the kernel sources changed since, or the library
+    loaded is another build (ROPE_LIBRARY: a compile-time variant)."""
+    if os.environ.get("ROPE_LIBRARY"):
+        return None
     path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel, workload))
     try:
         text = open(path).read()
