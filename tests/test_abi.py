@@ -339,3 +339,18 @@ def test_masked_attention_workspace_with_key_tiles(lib):
     # grows by them: a mask right after the counts now overlaps
     assert lib.rope_attention_fwd_masked(*masked_args(mask=ws + used, kind=1, ws=ws,
                                                       ws_bytes=used + 4)) == R.ROPE_ERR_INVALID_ARG
+
+
+def test_attention_workspace_sizes():
+    """attention_workspace: rot(K)'s bytes; for a [B, Sk] mask also the B
+    key-tile counts from the next 16-byte boundary and the B prefix lengths
+    after them; a [B, Sq, Sk] mask uses neither."""
+    import torch
+    B, Hk, Sk, D = 3, 2, 37, 64
+    k = torch.empty((B, Hk, Sk, D), dtype=torch.bfloat16)
+    kb = B * Hk * Sk * D * 2
+    assert R.attention_workspace(k).numel() == kb
+    assert R.attention_workspace(k, torch.ones((B, Sk), dtype=torch.bool)).numel() == \
+        (kb + 15) // 16 * 16 + 8 * B
+    assert R.attention_workspace(k, torch.ones((B, 5, Sk), dtype=torch.bool)).numel() == kb
+    assert R.attention_workspace(k).dtype == torch.uint8
