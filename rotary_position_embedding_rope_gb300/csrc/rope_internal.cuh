@@ -80,13 +80,15 @@ constexpr bool kPdl = ROPE_PDL != 0;
 #define ROPE_VEC_PREFETCH_HEADS ROPE_VEC_UNROLL
 #endif
 constexpr int kVecPrefetchHeads = ROPE_VEC_PREFETCH_HEADS;
-// L2 prefetches of head rows: 1 = one bulk prefetch of the rotary span's exact
-// bytes per row (cp.async.bulk.prefetch.L2), 0 = prefetch.global.L2 of the
-// lines under each thread's two vectors.
+// L2 prefetches of head rows: a bulk prefetch of the rotary span's exact
+// bytes per row (cp.async.bulk.prefetch.L2) or prefetch.global.L2 of the
+// lines under each thread's two vectors (whole lines): 0 = lines always,
+// 1 = bulk always, 2 = bulk for spans that are not whole rows (a partial
+// rotary span, where whole lines would fetch the tail too), else lines.
 #ifndef ROPE_VEC_PREFETCH_BULK
-#define ROPE_VEC_PREFETCH_BULK 0
+#define ROPE_VEC_PREFETCH_BULK 2
 #endif
-constexpr bool kVecPrefetchBulk = ROPE_VEC_PREFETCH_BULK != 0;
+constexpr int kVecPrefetchBulk = ROPE_VEC_PREFETCH_BULK;
 constexpr int kVecThreads = ROPE_VEC_THREADS;
 constexpr int kVecUnroll = ROPE_VEC_UNROLL;
 constexpr int kVecMinBlocks = ROPE_VEC_MIN_BLOCKS;

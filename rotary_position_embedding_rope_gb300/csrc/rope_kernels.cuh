@@ -343,11 +343,14 @@ __device__ __forceinline__ void copy_heads(const T *in0, T *out0, int64_t stride
 // ---------------------------------------------------------------------------
 
 // Prefetch into L2 the row vectors of thread j of heads [hb, he) (unit head
-// indices: Q heads first, then K heads) of token (b, s).
-template <typename T>
+// indices: Q heads first, then K heads) of token (b, s); WHOLE: the kernel
+// instance for rotary spans that are whole rows (kVecPrefetchBulk picks the
+// form of the prefetch).
+template <typename T, bool WHOLE>
 __device__ __forceinline__ void prefetch_heads(const ApplyArgs &p, int64_t b, int64_t s,
                                                int32_t hb, int32_t he, int j, int NJ)
 {
+    constexpr bool bulk = kVecPrefetchBulk == 1 || (kVecPrefetchBulk == 2 && !WHOLE);
 #pragma unroll
     for (int ti = 0; ti < 2; ++ti) {
         if (ti >= p.ntensors)
@@ -359,7 +362,7 @@ __device__ __forceinline__ void prefetch_heads(const ApplyArgs &p, int64_t b, in
         const T *in0 = static_cast<const T *>(t.base) + b * t.stride_b + s * t.stride_s;
         for (int32_t hd = lo; hd < hi; ++hd) {
             const uint4 *row = reinterpret_cast<const uint4 *>(in0 + (int64_t)hd * t.stride_h);
-            if constexpr (kVecPrefetchBulk) {
+            if constexpr (bulk) {
                 // the rotary span exactly (2 NJ 16-byte vectors), one request
                 if (j == 0)
                     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
@@ -372,7 +375,11 @@ __device__ __forceinline__ void prefetch_heads(const ApplyArgs &p, int64_t b, in
     }
 }
 
-template <typename T, int LAYOUT, int U>
+// WHOLE: the rotary spans are whole rows of a multiple of 256 bytes
+// (rotary_dim == D, D elements a multiple of 256 bytes); the launcher picks
+// the instance.  The other instance still tests this at run time: with the
+// test folded away its code measured slower on partial rotary spans.
+template <typename T, int LAYOUT, int U, bool WHOLE>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
 rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch_next)
 {
@@ -381,8 +388,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
     const int32_t P = p.t[0].heads + (p.ntensors > 1 ? p.t[1].heads : 0);
-    // rotary spans that are whole rows of a multiple of 256 bytes
-    const bool whole = p.rotary_dim == p.D && (p.D * (int32_t)sizeof(T)) % 256 == 0;
+    const bool whole = WHOLE || (p.rotary_dim == p.D && (p.D * (int32_t)sizeof(T)) % 256 == 0);
     const int64_t total_tokens = p.B * p.S;
 
     // this lane group's run of units
@@ -411,7 +417,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch
             const int64_t tok = tile * TT + row;
             if (tok < total_tokens) {
                 const int64_t b = tok / p.S;
-                prefetch_heads<T>(p, b, tok - b * p.S, hb, (int32_t)he, j, NJ);
+                prefetch_heads<T, WHOLE>(p, b, tok - b * p.S, hb, (int32_t)he, j, NJ);
             }
         }
     }
@@ -437,7 +443,7 @@ rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch
             const int64_t nt = tok + TT;
             const int64_t nb = nt / p.S;
             const int32_t nhe = (int32_t)(U < left ? U : left);
-            prefetch_heads<T>(p, nb, nt - nb * p.S, 0, nhe < P ? nhe : P, j, NJ);
+            prefetch_heads<T, WHOLE>(p, nb, nt - nb * p.S, 0, nhe < P ? nhe : P, j, NJ);
         }
 
         // position of this token: table row, -1 = leave unrotated
@@ -608,17 +614,18 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
 namespace {
 constexpr int kCacheDevices = 64;
 std::atomic<int> g_cache_sms[kCacheDevices];
-std::atomic<int> g_cache_occ[2][kCacheDevices];
+std::atomic<int> g_cache_occ[4][kCacheDevices];
 
-cudaError_t resident_ctas(const void *kernel, int32_t layout, int *sms, int *per_sm)
+// inst: the kernel instance (0 .. 3: pair layout * 2 + whole rows)
+cudaError_t resident_ctas(const void *kernel, int inst, int *sms, int *per_sm)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kCacheDevices)
+    if (dev < 0 || dev >= kCacheDevices || inst < 0 || inst > 3)
         return cudaErrorInvalidDevice;
-    const int li = layout ? 1 : 0;
+    const int li = inst;
     int n = g_cache_sms[dev].load(std::memory_order_relaxed);
     int o = g_cache_occ[li][dev].load(std::memory_order_relaxed);
     if (n <= 0 || o <= 0) {
@@ -652,8 +659,12 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         const int32_t P = a.t[0].heads + (a.ntensors > 1 ? a.t[1].heads : 0);
         const int64_t tiles = (a.B * a.S + TT - 1) / TT;
         const int64_t units = tiles * P;
-        auto kernel = layout == 0 ? rope_vec_kernel<T, 0, kVecUnroll>
-                                  : rope_vec_kernel<T, 1, kVecUnroll>;
+        // rotary spans that are whole rows of a multiple of 256 bytes
+        const bool whole = a.rotary_dim == a.D && (a.D * (int32_t)sizeof(T)) % 256 == 0;
+        auto kernel = layout == 0 ? (whole ? rope_vec_kernel<T, 0, kVecUnroll, true>
+                                           : rope_vec_kernel<T, 0, kVecUnroll, false>)
+                                  : (whole ? rope_vec_kernel<T, 1, kVecUnroll, true>
+                                           : rope_vec_kernel<T, 1, kVecUnroll, false>);
         // The grid.  Calls with at least one tile per lane group that can be
         // resident at once take one tile (all P heads of TT tokens) per lane
         // group, as many CTAs as that makes: the hardware hands the CTAs out
@@ -664,7 +675,8 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         // tuning entry point can force the cap and the run length instead.
         const VecLaunchTuning tune = vec_launch_tuning();
         int sms = 0, per_sm = 0;
-        cudaError_t e = resident_ctas(reinterpret_cast<const void *>(kernel), layout, &sms, &per_sm);
+        cudaError_t e = resident_ctas(reinterpret_cast<const void *>(kernel),
+                                      (layout ? 2 : 0) + (whole ? 1 : 0), &sms, &per_sm);
         if (e != cudaSuccess)
             return e;
         const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
