@@ -83,6 +83,8 @@ def load_library() -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     path = library_path()
+    if not os.path.exists(path) and os.environ.get("ROPE_LIBRARY"):
+        raise RuntimeError("ROPE_LIBRARY names %s, which does not exist" % path)
     if not os.path.exists(path):
         raise RuntimeError(
             "librope.so is not built (%s); run `python -c \"import __graft_entry__ as g; "
