@@ -510,8 +510,9 @@ def test_attention_skips_key_tiles_a_key_mask_hides(D, causal):
            "tile skipping D%d c%d" % (D, causal), attn_mask=m)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("D", [64, 128])
-def test_key_mask_prefix_lengths(D):
+def test_key_mask_prefix_lengths(D, dtype):
     """Prefix lengths of a [B, Sk] mask whose rows are 16-byte aligned (Sk =
     1024: read 16 bytes at a time): all keys visible (1024); the first 1000
     (1000, the first hidden key in another 16-byte chunk than the last
@@ -522,7 +523,7 @@ def test_key_mask_prefix_lengths(D):
     require_gpu()
     R = lib()
     B, Hq, Hk, Sq, Sk = 4, 4, 2, 200, 1024
-    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, "bf16", 79)
+    q, k, v = _inputs(B, Hq, Hk, Sq, Sk, D, dtype, 79)
     m = np.ones((B, Sk), dtype=bool)
     m[1, 1000:] = False
     m[2, 1000:] = False
@@ -544,5 +545,5 @@ def test_key_mask_prefix_lengths(D):
     assert R.rope_check_errors() == R.ROPE_OK
     assert torch.equal(got.view(torch.int16), counts.view(torch.int16))
     assert torch.equal(got.view(torch.int16), inker.view(torch.int16))
-    _check(got, q, k, v, "bf16", D, O.SPLIT_HALF, c32, s32, None, None, False,
-           "prefix lengths D%d" % D, attn_mask=m)
+    _check(got, q, k, v, dtype, D, O.SPLIT_HALF, c32, s32, None, None, False,
+           "prefix lengths D%d %s" % (D, dtype), attn_mask=m)
