@@ -576,6 +576,10 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tens
     _, Hk, Sk, _ = k.shape
     if v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("k and v must have the same shape, and q, k, v the same dtype")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("attention takes bf16 or fp16 q, k, v (the tensor-core products are 16-bit); "
+                        "got %s: convert the inputs first (e.g. q.bfloat16()), a rounding that is "
+                        "the caller's choice" % q.dtype)
     rd = 2 * cos.shape[1] if rotary_dim is None else rotary_dim
     o = torch.empty_like(q) if out is None else out
     if isinstance(k_workspace, str):

@@ -354,3 +354,13 @@ def test_attention_workspace_sizes():
         (kb + 15) // 16 * 16 + 8 * B
     assert R.attention_workspace(k, torch.ones((B, 5, Sk), dtype=torch.bool)).numel() == kb
     assert R.attention_workspace(k).dtype == torch.uint8
+
+
+def test_attention_binding_names_the_dtypes_it_takes():
+    """The Python attention call refuses fp32 tensors before any device work,
+    naming bf16 / fp16 (the C entry point returns ROPE_ERR_UNSUPPORTED)."""
+    import torch
+    q = torch.zeros(1, 8, 16, 64)
+    c = torch.zeros(16, 32)
+    with pytest.raises(TypeError, match="bf16 or fp16"):
+        R.attention(q, q.clone(), q.clone(), c, c.clone())
