@@ -364,3 +364,22 @@ def test_attention_binding_names_the_dtypes_it_takes():
     c = torch.zeros(16, 32)
     with pytest.raises(TypeError, match="bf16 or fp16"):
         R.attention(q, q.clone(), q.clone(), c, c.clone())
+
+
+def test_rope_library_override(lib):
+    """ROPE_LIBRARY makes the binding load another build (here the in-tree one
+    under its own path); a missing file is named in the error.  Subprocesses:
+    the binding keeps the library it loaded first."""
+    import subprocess
+    import sys
+    code = ("import rotary_position_embedding_rope_gb300 as R; L = R.load_library(); "
+            "print(L._name)")
+    env = dict(os.environ, ROPE_LIBRARY=_build.LIBRARY)
+    p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=ROOT)
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == _build.LIBRARY
+    env["ROPE_LIBRARY"] = os.path.join(ROOT, "no_such_dir", "librope.so")
+    p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=ROOT)
+    assert p.returncode != 0 and "ROPE_LIBRARY names" in p.stderr
