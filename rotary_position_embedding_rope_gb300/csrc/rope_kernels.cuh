@@ -379,12 +379,15 @@ __device__ __forceinline__ void prefetch_heads(const ApplyArgs &p, int64_t b, in
 // (rotary_dim == D, D elements a multiple of 256 bytes); the launcher picks
 // the instance.  The other instance still tests this at run time: with the
 // test folded away its code measured slower on partial rotary spans.
-template <typename T, int LAYOUT, int U, bool WHOLE>
+// NJC: NJ known at compile time (then TT and the lane groups per CTA are
+// too), or 0: NJ = blockDim.x and TT as passed.
+template <typename T, int LAYOUT, int U, bool WHOLE, int NJC>
 __global__ void __launch_bounds__(kVecThreads, kVecMinBlocks)
-rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch_next)
+rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT_arg, int32_t prefetch_next)
 {
     constexpr int V = Elt<T>::V;
-    const int NJ = blockDim.x;
+    const int NJ = NJC > 0 ? NJC : (int)blockDim.x;
+    const int32_t TT = NJC > 0 ? (NJC >= 32 ? 1 : 32 / NJC) : TT_arg;
     const int j = threadIdx.x;
     const int h = p.rotary_dim >> 1;
     const int32_t P = p.t[0].heads + (p.ntensors > 1 ? p.t[1].heads : 0);
@@ -392,7 +395,8 @@ rope_vec_kernel(const ApplyArgs p, int64_t n_units, int32_t TT, int32_t prefetch
     const int64_t total_tokens = p.B * p.S;
 
     // this lane group's run of units
-    const int lgs = blockDim.y / TT;
+    const int lgs = NJC > 0 ? (NJC >= kVecThreads ? 1 : (kVecThreads / NJC) / TT)
+                            : (int)blockDim.y / TT;
     const int lg = threadIdx.y / TT;
     const int row = threadIdx.y - lg * TT;
     const int64_t G = (int64_t)gridDim.x * lgs;
@@ -614,16 +618,17 @@ __global__ void rope_scalar_kernel(const ApplyArgs p, int64_t rows0, int64_t tot
 namespace {
 constexpr int kCacheDevices = 64;
 std::atomic<int> g_cache_sms[kCacheDevices];
-std::atomic<int> g_cache_occ[4][kCacheDevices];
+constexpr int kVecInstances = 6;               // pair layout x (partial, whole, whole with NJ = 8)
+std::atomic<int> g_cache_occ[kVecInstances][kCacheDevices];
 
-// inst: the kernel instance (0 .. 3: pair layout * 2 + whole rows)
+// inst: the kernel instance, 0 .. kVecInstances - 1
 cudaError_t resident_ctas(const void *kernel, int inst, int *sms, int *per_sm)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= kCacheDevices || inst < 0 || inst > 3)
+    if (dev < 0 || dev >= kCacheDevices || inst < 0 || inst >= kVecInstances)
         return cudaErrorInvalidDevice;
     const int li = inst;
     int n = g_cache_sms[dev].load(std::memory_order_relaxed);
@@ -659,12 +664,18 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         const int32_t P = a.t[0].heads + (a.ntensors > 1 ? a.t[1].heads : 0);
         const int64_t tiles = (a.B * a.S + TT - 1) / TT;
         const int64_t units = tiles * P;
-        // rotary spans that are whole rows of a multiple of 256 bytes
+        // rotary spans that are whole rows of a multiple of 256 bytes; the
+        // commonest of them (8 vectors per half: 16-bit D = 128, fp32 D = 64)
+        // with NJ fixed at compile time
         const bool whole = a.rotary_dim == a.D && (a.D * (int32_t)sizeof(T)) % 256 == 0;
-        auto kernel = layout == 0 ? (whole ? rope_vec_kernel<T, 0, kVecUnroll, true>
-                                           : rope_vec_kernel<T, 0, kVecUnroll, false>)
-                                  : (whole ? rope_vec_kernel<T, 1, kVecUnroll, true>
-                                           : rope_vec_kernel<T, 1, kVecUnroll, false>);
+        const int kind = whole ? (NJ == 8 ? 2 : 1) : 0;
+        using Kernel = void (*)(const ApplyArgs, int64_t, int32_t, int32_t);
+        const Kernel kernels[2][3] = {
+            {rope_vec_kernel<T, 0, kVecUnroll, false, 0>, rope_vec_kernel<T, 0, kVecUnroll, true, 0>,
+             rope_vec_kernel<T, 0, kVecUnroll, true, 8>},
+            {rope_vec_kernel<T, 1, kVecUnroll, false, 0>, rope_vec_kernel<T, 1, kVecUnroll, true, 0>,
+             rope_vec_kernel<T, 1, kVecUnroll, true, 8>}};
+        const Kernel kernel = kernels[layout ? 1 : 0][kind];
         // The grid.  Calls with at least one tile per lane group that can be
         // resident at once take one tile (all P heads of TT tokens) per lane
         // group, as many CTAs as that makes: the hardware hands the CTAs out
@@ -676,7 +687,7 @@ cudaError_t launch_apply(const ApplyArgs &a, int32_t layout, Variant v, cudaStre
         const VecLaunchTuning tune = vec_launch_tuning();
         int sms = 0, per_sm = 0;
         cudaError_t e = resident_ctas(reinterpret_cast<const void *>(kernel),
-                                      (layout ? 2 : 0) + (whole ? 1 : 0), &sms, &per_sm);
+                                      (layout ? 3 : 0) + kind, &sms, &per_sm);
         if (e != cudaSuccess)
             return e;
         const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
